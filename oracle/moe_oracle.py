@@ -1,0 +1,316 @@
+"""fp64 CPU oracle for the forward pass of a token-choice sparse MoE FFN layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may use it.  It shares no code with the CUDA library and reads the
+same stored input values (bf16 or fp32), widened exactly to float64.
+
+Every step is the plain definition from the pages, written out in float64 with
+numpy; a library matmul, exp, sort or floor serves as a step, with no blocking,
+fusion or reordering beyond the definition.  Sources (page title, section):
+
+[MoE-ch30]  "Mixture of Experts", LLM Transformer book (waylandz.com), ch. 30:
+            §30.2.3 router (linear -> softmax -> top-k -> renormalise),
+            §30.2.4 SwiGLU expert, §30.2.6 load-balancing loss,
+            §30.4.5 shared expert, §30.5.2 capacity, §30.6.1 MoELayer.
+[MoE-guide] "Mixture of Experts guide" (ai-native-b2y.pages.dev):
+            "MoEの核心：ルーターの仕組み", "解決策1：補助損失".
+[MoE-memo]  "Mixture of Experts (MoE) memo" (iwashi.co): "補助損失" worked
+            example, "DeepSeek-V3のアプローチ → Aux-loss-free（バイアス）",
+            "Kimi K3 → Quantile Balancing".
+[MoE-prac]  "混合エキスパートモデル（MoE）実践" (deepseekmodel.com):
+            "ルーティングの数学的な形" (TopKRouter), "capacity factor、token
+            dropping", "ロードバランシング損失" (BiasBalancedRouter),
+            "expert parallelism と all-to-all" (stable grouping by expert).
+
+Readings where the pages are silent or disagree (each restated where used):
+  R1  f_e = count_e / (T*k): fraction of all routed assignments, so sum f = 1
+      and uniform routing gives aux = 1 for every k.
+  R2  aux is returned without the 0.01 coefficient.
+  R3  f counts router assignments before capacity drops; p is the mean of the
+      unbiased softmax probability over all T tokens.
+  R4  the selection bias is added to the softmax probabilities (default) or,
+      on request, to the logits; weights always come from the unbiased probs.
+  R5  top-k order is descending score; exactly equal scores: lower expert
+      index first.
+  R6  capacity C = ceil(cf*T*k/E); per expert the first C assignments in
+      flattened (t*k + j) order are kept, the rest dropped; a dropped slot
+      contributes 0 and the surviving weights are not renormalised.
+  R7  quantile bias b_e = -Q(probs[:, e], 1 - k/E) with Q the linear
+      interpolation between order statistics (h = (T-1) q).
+
+Pins (tests/test_oracle_pins.py): the printed worked examples (top-2
+renormalisation, 4-token aux loss, selection-bias example), brute-force top-k
+over all subsets, softmax of log-probabilities, E=1 and k=E reductions to a
+dense FFN / dense mixture computed with torch.nn.functional, identical experts,
+numpy.quantile, a hand-built capacity case, and dispatch invariants.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "router_logits", "softmax", "topk_desc", "renormalise", "route",
+    "quantile_linear", "quantile_select_bias", "capacity", "dispatch",
+    "expert_ffn", "load_stats", "moe_forward", "RouterOut", "DispatchOut",
+]
+
+
+def _f64(a) -> np.ndarray:
+    """Widen a torch tensor or array to float64 (exact for fp32/bf16 inputs)."""
+    if hasattr(a, "detach"):
+        a = a.detach().cpu()
+        if str(a.dtype) == "torch.bfloat16":
+            a = a.float()
+        a = a.numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Router: [MoE-ch30] §30.2.3 steps 1-4, [MoE-prac] TopKRouter.forward
+# --------------------------------------------------------------------------
+
+def router_logits(x, w_r, logit_bias=None) -> np.ndarray:
+    """logits[t, e] = sum_i x[t, i] * W_r[e, i]  (+ logit_bias[e]).
+
+    The router is a bias-free linear layer hidden -> E ([MoE-ch30] §30.2.3
+    step 1, [MoE-prac] "ルーターが bias を持たない").  W_r is stored like an
+    nn.Linear weight, [E, d].  ``logit_bias`` is a fixed per-expert offset
+    that the synthetic workloads use to skew expert popularity.
+    """
+    lg = _f64(x) @ _f64(w_r).T
+    if logit_bias is not None:
+        lg = lg + _f64(logit_bias)[None, :]
+    return lg
+
+
+def softmax(logits: np.ndarray) -> np.ndarray:
+    """probs = exp(l - max) / sum exp(l - max) over the expert axis (step 2)."""
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def topk_desc(scores: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest scores per row, largest first (step 3).
+
+    Reading R5: exactly equal scores are ordered by lower expert index.  A
+    stable ascending sort of the negated scores gives exactly that order.
+    """
+    order = np.argsort(-scores, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def renormalise(probs: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """w[t, j] = probs[t, idx[t, j]] / sum_j' probs[t, idx[t, j']] (step 4).
+
+    [MoE-ch30] §30.2.3 step 4; [MoE-prac] calls this the step that must not
+    be skipped.  With a selection bias the weights still come from the
+    unbiased probabilities ([MoE-memo] aux-loss-free section, [MoE-prac]
+    BiasBalancedRouter).
+    """
+    sel = np.take_along_axis(probs, idx, axis=1)
+    return sel / sel.sum(axis=1, keepdims=True)
+
+
+def quantile_linear(values: np.ndarray, q: float) -> float:
+    """Q(values, q) by linear interpolation between order statistics.
+
+    Sort ascending into v_(0..n-1); h = (n-1) q; Q = v_(floor h) +
+    (h - floor h) (v_(floor h + 1) - v_(floor h)).  Reading R7.
+    """
+    v = np.sort(np.asarray(values, dtype=np.float64))
+    n = v.shape[0]
+    h = (n - 1) * q
+    lo = int(math.floor(h))
+    if lo >= n - 1:
+        return float(v[n - 1])
+    return float(v[lo] + (h - lo) * (v[lo + 1] - v[lo]))
+
+
+def quantile_select_bias(probs: np.ndarray, k: int) -> np.ndarray:
+    """Per-batch quantile balancing: b_e = -Q(probs[:, e], 1 - k/E).
+
+    [MoE-memo] "Kimi K3 → Quantile Balancing" sets, per expert, the bias
+    that makes the target share of tokens enter the top-k, read off the
+    score distribution instead of stepping it.  With b_e at the (1 - k/E)
+    quantile, about a k/E share of each expert's column has probs + b > 0.
+    """
+    T, E = probs.shape
+    q = 1.0 - k / E
+    return np.array([-quantile_linear(probs[:, e], q) for e in range(E)])
+
+
+@dataclass
+class RouterOut:
+    logits: np.ndarray        # [T, E] float64
+    probs: np.ndarray         # [T, E] unbiased softmax
+    scores: np.ndarray        # [T, E] the values top-k ran on
+    idx: np.ndarray           # [T, k] int64, descending score
+    w: np.ndarray             # [T, k] renormalised gate weights
+    select_bias: Optional[np.ndarray]   # [E] bias used for selection
+
+
+def route(x, w_r, k: int, logit_bias=None, select_bias=None,
+          select_space: str = "probs", quantile_balance: bool = False
+          ) -> RouterOut:
+    """Router linear -> softmax -> (bias for selection) -> top-k -> renorm.
+
+    Reading R4: the selection bias goes on the probs ([MoE-prac]
+    BiasBalancedRouter adds it to the softmax output) unless
+    ``select_space == "logits"``.
+    """
+    logits = router_logits(x, w_r, logit_bias)
+    probs = softmax(logits)
+    base = probs if select_space == "probs" else logits
+    bias = None
+    if quantile_balance:
+        bias = quantile_select_bias(probs, k)
+    elif select_bias is not None:
+        bias = _f64(select_bias)
+    scores = base if bias is None else base + bias[None, :]
+    idx = topk_desc(scores, k)
+    w = renormalise(probs, idx)
+    return RouterOut(logits, probs, scores, idx, w, bias)
+
+
+# --------------------------------------------------------------------------
+# Capacity and dispatch: [MoE-prac] "capacity factor、token dropping",
+# "expert parallelism と all-to-all" (stable grouping by expert)
+# --------------------------------------------------------------------------
+
+def capacity(T: int, k: int, E: int, capacity_factor: float) -> int:
+    """C = ceil(cf * k * T / E) ([MoE-prac] capacity section); no limit
+    (returns T*k) when cf <= 0.  Reading R6 picks this among the pages'
+    variants."""
+    if capacity_factor <= 0:
+        return T * k
+    return int(math.ceil(float(capacity_factor) * T * k / E))
+
+
+@dataclass
+class DispatchOut:
+    counts: np.ndarray        # [E] assignments per expert before drops
+    kept_counts: np.ndarray   # [E] min(counts, C)
+    offsets: np.ndarray       # [E+1] exclusive scan of kept_counts
+    perm: np.ndarray          # [sum kept] flat slot (t*k+j) of each sorted row
+    inv: np.ndarray           # [T*k] sorted row of each flat slot, -1 if dropped
+    keep: np.ndarray          # [T, k] bool
+    n_dropped: int
+
+
+def dispatch(idx: np.ndarray, E: int, C: int) -> DispatchOut:
+    """Group the T*k assignments by expert, stably, and apply capacity.
+
+    Flatten (t, j) to f = t*k + j; order the slots by expert, keeping the f
+    order inside each expert (the stable argsort of [MoE-prac]'s dispatch);
+    within an expert the slot of rank r (0-based, in f order) is kept iff
+    r < C (reading R6: drops go in token-index order).
+    """
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    order = np.argsort(flat, kind="stable")          # slots grouped by expert
+    starts = np.concatenate([[0], np.cumsum(counts)[:-1]])
+    rank_sorted = np.arange(T * k) - starts[flat[order]]
+    keep_sorted = rank_sorted < C
+    perm = order[keep_sorted]
+    kept_counts = np.minimum(counts, C)
+    offsets = np.concatenate([[0], np.cumsum(kept_counts)]).astype(np.int64)
+    inv = np.full(T * k, -1, dtype=np.int64)
+    inv[perm] = np.arange(perm.shape[0])
+    keep = (inv >= 0).reshape(T, k)
+    return DispatchOut(counts, kept_counts, offsets, perm.astype(np.int64), inv,
+                       keep, int(T * k - perm.shape[0]))
+
+
+# --------------------------------------------------------------------------
+# Expert FFN: [MoE-ch30] §30.2.4 / §30.6.1 Expert
+# --------------------------------------------------------------------------
+
+def _silu(a: np.ndarray) -> np.ndarray:
+    return a / (1.0 + np.exp(-a))
+
+
+def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str) -> np.ndarray:
+    """One expert on the rows x_rows [n, d] (float64).
+
+    SwiGLU: w2(silu(w1 x) * w3 x)  ([MoE-ch30] §30.2.4), ReLU: w2(relu(w1 x)).
+    Weights are nn.Linear-shaped: w1, w3 [F, d], w2 [d, F]; no biases.
+    """
+    a = x_rows @ _f64(w1).T
+    if act == "swiglu":
+        h = _silu(a) * (x_rows @ _f64(w3).T)
+    elif act == "relu":
+        h = np.maximum(a, 0.0)
+    else:
+        raise ValueError(act)
+    return h @ _f64(w2).T
+
+
+# --------------------------------------------------------------------------
+# Load statistics: [MoE-ch30] §30.2.6, [MoE-memo] 補助損失, [MoE-prac]
+# load_balance_loss
+# --------------------------------------------------------------------------
+
+def load_stats(probs: np.ndarray, idx: np.ndarray, E: int) -> Dict[str, np.ndarray]:
+    """f, p, aux = E * sum_e f_e p_e, and the load max/mean ratio.
+
+    f_e = (number of (t, j) with idx = e) / (T*k)   (reading R1, before drops)
+    p_e = mean over tokens of probs[t, e]
+    """
+    T, k = idx.shape
+    counts = np.bincount(idx.reshape(-1), minlength=E).astype(np.int64)
+    f = counts / float(T * k)
+    p = probs.mean(axis=0)
+    aux = E * float(np.sum(f * p))
+    mean_load = T * k / float(E)
+    return {"counts": counts, "f": f, "p": p, "aux": aux,
+            "load_max_over_mean": float(counts.max()) / mean_load}
+
+
+# --------------------------------------------------------------------------
+# Whole layer: [MoE-ch30] §30.6.1 MoELayer.forward, §30.4.5 shared expert
+# --------------------------------------------------------------------------
+
+def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
+                select_space: str = "probs", quantile_balance: bool = False,
+                tokens: Optional[Sequence[int]] = None) -> Dict:
+    """Forward of the token-choice MoE layer.
+
+    y[t] = sum_j keep[t,j] * w[t,j] * FFN_{idx[t,j]}(x[t]) + shared(x[t]).
+    Routing, dispatch and statistics are computed for all T tokens (capacity
+    couples them); y is computed for ``tokens`` only (all when None), since
+    each token's output depends on nothing else once its slots are known.
+    """
+    x = _f64(inp["x"])
+    T = x.shape[0]
+    E = inp["w_r"].shape[0]
+    r = route(x, inp["w_r"], k, inp.get("logit_bias"), inp.get("select_bias"),
+              select_space, quantile_balance)
+    C = capacity(T, k, E, capacity_factor)
+    dp = dispatch(r.idx, E, C)
+    st = load_stats(r.probs, r.idx, E)
+    rows = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
+    y = np.zeros((rows.shape[0], x.shape[1]))
+    pos = {int(t): i for i, t in enumerate(rows)}
+    groups: Dict[int, list] = {}
+    for t in rows:
+        for j in range(k):
+            if dp.keep[t, j]:
+                groups.setdefault(int(r.idx[t, j]), []).append((int(t), j))
+    for e, tj in sorted(groups.items()):
+        tt = np.array([t for t, _ in tj])
+        ww = np.array([r.w[t, j] for t, j in tj])
+        out = expert_ffn(x[tt], inp["w1"][e], None if inp.get("w3") is None else inp["w3"][e],
+                         inp["w2"][e], act)
+        for n, (t, _) in enumerate(tj):
+            y[pos[int(t)]] += ww[n] * out[n]
+    if inp.get("ws1") is not None:
+        y += expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu")
+    return {"router": r, "dispatch": dp, "stats": st, "capacity": C,
+            "rows": rows, "y": y}
