@@ -38,6 +38,13 @@ Readings where the pages are silent or disagree (each restated where used):
       contributes 0 and the surviving weights are not renormalised.
   R7  quantile bias b_e = -Q(probs[:, e], 1 - k/E) with Q the linear
       interpolation between order statistics (h = (T-1) q).
+  R8  the layer's activations are stored in the layer dtype: for a bf16 layer
+      the expert's intermediate activation h (the input of W2) is a bf16
+      tensor, so it is rounded once, to nearest even, from its exact value
+      before the down projection.  The pages run the model in
+      torch.bfloat16 ([MoE-ch30] §30.6.3), and the Switch workload is
+      specified with bf16 weights and activations.  Everything else stays
+      exact float64.
 
 Pins (tests/test_oracle_pins.py): the printed worked examples (top-2
 renormalisation, 4-token aux loss, selection-bias example), brute-force top-k
@@ -56,7 +63,8 @@ import numpy as np
 __all__ = [
     "router_logits", "softmax", "topk_desc", "renormalise", "route",
     "quantile_linear", "quantile_select_bias", "capacity", "dispatch",
-    "expert_ffn", "load_stats", "moe_forward", "RouterOut", "DispatchOut",
+    "expert_ffn", "load_stats", "moe_forward", "RouterOut", "DispatchOut", "round_to_bf16",
+    "round_to_fp32",
 ]
 
 
@@ -236,11 +244,33 @@ def _silu(a: np.ndarray) -> np.ndarray:
     return a / (1.0 + np.exp(-a))
 
 
-def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str) -> np.ndarray:
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value, ties to even.
+
+    bf16 keeps 8 significant bits: for |a| in [2^(e-1), 2^e) the spacing is
+    2^(e-8); below the smallest normal 2^-126 the spacing is 2^-133.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)
+    e = np.maximum(e, -125)
+    q = np.ldexp(1.0, e - 8)
+    return np.round(a / q) * q
+
+
+def round_to_fp32(a: np.ndarray) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+ACT_ROUNDING = {"fp64": lambda a: a, "fp32": round_to_fp32, "bf16": round_to_bf16}
+
+
+def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str, act_dtype: str = "fp64") -> np.ndarray:
     """One expert on the rows x_rows [n, d] (float64).
 
     SwiGLU: w2(silu(w1 x) * w3 x)  ([MoE-ch30] §30.2.4), ReLU: w2(relu(w1 x)).
     Weights are nn.Linear-shaped: w1, w3 [F, d], w2 [d, F]; no biases.
+    ``act_dtype`` is the storage type of the intermediate activation h
+    (reading R8): "fp64" keeps it exact, "fp32"/"bf16" round it once.
     """
     a = x_rows @ _f64(w1).T
     if act == "swiglu":
@@ -249,6 +279,7 @@ def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str) -> np.ndarray:
         h = np.maximum(a, 0.0)
     else:
         raise ValueError(act)
+    h = ACT_ROUNDING[act_dtype](h)
     return h @ _f64(w2).T
 
 
@@ -279,13 +310,15 @@ def load_stats(probs: np.ndarray, idx: np.ndarray, E: int) -> Dict[str, np.ndarr
 
 def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
                 select_space: str = "probs", quantile_balance: bool = False,
-                tokens: Optional[Sequence[int]] = None) -> Dict:
+                tokens: Optional[Sequence[int]] = None, act_dtype: str = "fp64") -> Dict:
     """Forward of the token-choice MoE layer.
 
     y[t] = sum_j keep[t,j] * w[t,j] * FFN_{idx[t,j]}(x[t]) + shared(x[t]).
     Routing, dispatch and statistics are computed for all T tokens (capacity
     couples them); y is computed for ``tokens`` only (all when None), since
     each token's output depends on nothing else once its slots are known.
+    ``act_dtype`` is the storage type of the experts' intermediate
+    activation (reading R8).
     """
     x = _f64(inp["x"])
     T = x.shape[0]
@@ -307,10 +340,10 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
         tt = np.array([t for t, _ in tj])
         ww = np.array([r.w[t, j] for t, j in tj])
         out = expert_ffn(x[tt], inp["w1"][e], None if inp.get("w3") is None else inp["w3"][e],
-                         inp["w2"][e], act)
+                         inp["w2"][e], act, act_dtype)
         for n, (t, _) in enumerate(tj):
             y[pos[int(t)]] += ww[n] * out[n]
     if inp.get("ws1") is not None:
-        y += expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu")
+        y += expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
     return {"router": r, "dispatch": dp, "stats": st, "capacity": C,
             "rows": rows, "y": y}

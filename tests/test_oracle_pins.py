@@ -270,12 +270,40 @@ def pin_quantile_balance_share():
     assert after < before
 
 
+def pin_round_to_bf16():
+    # fp32-representable values: torch's float32 -> bfloat16 conversion rounds
+    # to nearest even in one step, the same definition.
+    v = (RNG.normal(size=5000) * np.exp(RNG.uniform(-30, 30, size=5000))).astype(np.float32)
+    v = np.concatenate([v, np.float32([0.0, -0.0, 1.0, 3.0, 1e-40, -2.5e-39])])
+    ref = torch.tensor(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(om.round_to_bf16(v.astype(np.float64)), ref)
+    # ties go to the even neighbour (spacing 2^-7 on [1, 2))
+    assert om.round_to_bf16(np.array([1 + 2.0 ** -8]))[0] == 1.0
+    assert om.round_to_bf16(np.array([1 + 3 * 2.0 ** -8]))[0] == 1 + 2.0 ** -6
+    assert om.round_to_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -30]))[0] == 1 + 2.0 ** -7
+
+
+def pin_bf16_activation_ffn():
+    # E = 1 with a bf16 intermediate: the page's Expert in a bf16 model stores
+    # h in bf16 before w2; torch.nn.functional in float64 with h rounded by torch.
+    inp = _rand_layer(13, 16, 1, 24, "swiglu")
+    out = om.moe_forward(inp, 1, "swiglu", act_dtype="bf16")
+    x, w1, w3, w2 = (torch.tensor(np.asarray(a, dtype=np.float64))
+                     for a in (inp["x"], inp["w1"][0], inp["w3"][0], inp["w2"][0]))
+    h = Fnn.silu(Fnn.linear(x, w1)) * Fnn.linear(x, w3)
+    h = h.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    ref = Fnn.linear(h, w2).numpy()
+    assert np.allclose(out["y"], ref, atol=1e-12)
+    exact = om.moe_forward(inp, 1, "swiglu")
+    assert not np.allclose(out["y"], exact["y"], atol=1e-6)   # the rounding is visible
+
+
 PINS = [pin_top2_example, pin_aux_worked_example, pin_selection_bias_example,
         pin_uniform_aux_is_one, pin_topk_bruteforce, pin_softmax_closed_forms,
         pin_router_logits_layout, pin_single_expert_is_dense_ffn, pin_identical_experts,
         pin_all_experts_is_dense_mixture, pin_shared_expert_added, pin_capacity_cases,
         pin_capacity_switch_workload, pin_dispatch_invariants, pin_quantile_vs_numpy,
-        pin_quantile_balance_share]
+        pin_quantile_balance_share, pin_round_to_bf16, pin_bf16_activation_ffn]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -362,6 +390,12 @@ def _mut_softmax_no_max(logits):
     return e / e.sum(axis=0, keepdims=True)         # normalised over the wrong axis
 
 
+def _mut_round_truncate(a):
+    _, e = np.frexp(a)
+    q = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    return np.trunc(a / q) * q                      # truncation instead of nearest-even
+
+
 def _mut_capacity_floor(T, k, E, cf):
     return T * k if cf <= 0 else int(cf * T / E)    # drops k (one of the page variants)
 
@@ -379,6 +413,7 @@ MUTATIONS = [
     ("quantile_linear", _mut_quantile_floor_only),
     ("softmax", _mut_softmax_no_max),
     ("capacity", _mut_capacity_floor),
+    ("round_to_bf16", _mut_round_truncate),
 ]
 
 
