@@ -1,0 +1,381 @@
+#!/usr/bin/env python
+"""Throughput of the token-choice MoE layer forward on B300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mixtral] [--T 16384] [--no-cpu-baseline]
+
+A step is one moe_layer_forward (router, dispatch, stats, gather, expert up
+and down projections, shared expert when present, combine) over one batch of
+T synthetic tokens of the named workload (default: the Mixtral-8x7B-shaped
+layer, d=4096, E=8, k=2, SwiGLU d_ff=14336, bf16, T=16384), inputs resident
+in HBM.  The weights (2.8 GB) are larger than L2, so every step streams them
+from HBM; no L2 flush is needed.
+
+Metric: tokens/s over the whole job (all ranks).  Under torchrun each rank
+runs its own batch on its own GPU (weak scaling, no collective on the data
+path); the time is the max over ranks.
+
+Extra keys: roofline of the dominant kernel (the grouped up projection,
+timed live with CUDA events around it on the launching stream), the layer's
+own roofline fraction, per-stage times, e2e (host buffers through the same
+C ABI call, H2D/D2H copies inside the timed region), clocks sampled during
+the timed region, gpu_launches counted by the library, and cpu_baseline (the
+fp64 oracle on a bounded sample, on the host cores).
+
+--impl reference times the oracle (the only other implementation of the
+layer) on the host cores, each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(w, T, n_kept, counts_nonzero):
+    """Work the method itself must do (dense work it avoids is not counted).
+
+    FLOPs: router 2*d*E per token + per kept (token, slot) 2*m*d*F (m = 3
+    SwiGLU, 2 ReLU) + shared 6*d*Fs per token.  Bytes: weights of experts with
+    at least one token, shared weights, W_r, x read once, y written once
+    (bf16)."""
+    d, E, F, Fs = w.d_model, w.n_experts, w.d_ff, w.d_ff_shared
+    m = 3 if w.act == "swiglu" else 2
+    eb = 2 if w.dtype == "bf16" else 4
+    flops = 2.0 * d * E * T + 2.0 * m * d * F * n_kept + 6.0 * d * Fs * T
+    bytes_ = (m * d * F * eb) * counts_nonzero + 3 * d * Fs * eb + 4 * d * E + 2 * T * d * eb
+    up_flops = 2.0 * d * F * n_kept * (2 if w.act == "swiglu" else 1)
+    return flops, bytes_, up_flops
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+def oracle_sample_run(w, inp_cpu64, S):
+    """The oracle as it stands on a batch of the first S tokens."""
+    import oracle.moe_oracle as om
+    sub = dict(inp_cpu64)
+    sub["x"] = inp_cpu64["x"][:S]
+    t0 = time.perf_counter()
+    om.moe_forward(sub, w.top_k, w.act, w.capacity_factor, "probs", w.quantile_balance,
+                   None, w.dtype)
+    return time.perf_counter() - t0
+
+
+def host_inputs_f64(inp):
+    """Widen the generated inputs to float64 numpy once (input preparation)."""
+    out = {}
+    for k, v in inp.items():
+        if v is None:
+            out[k] = None
+        else:
+            out[k] = v.detach().float().cpu().numpy().astype(np.float64)
+    return out
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def sample_size(w):
+    # about 10-30 s of fp64 CPU work per timed sample on a many-core host
+    per_token = 2.0 * (3 if w.act == "swiglu" else 2) * w.d_model * w.d_ff * w.top_k
+    return int(max(8, min(512, 4e10 / per_token)))
+
+
+# --------------------------------------------------------------------------- arms
+
+def run_reference(args, w, T):
+    # Under torchrun only rank 0 times the oracle; the other ranks exit at once.
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    S = min(T, sample_size(w))
+    inp = mi.generate(w, S, "cpu")
+    inp64 = host_inputs_f64(inp)
+    for _ in range(args.warmup):
+        oracle_sample_run(w, inp64, S)
+    times = [oracle_sample_run(w, inp64, S) for _ in range(args.steps)]
+    total = sum(times)
+    value = S * args.steps / total
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": "MoE-layer fwd tokens/s on 1 B300 (bf16) and % of roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}-shaped layer d={w.d_model} E={w.n_experts} "
+                               f"k={w.top_k} d_ff={w.d_ff} T={T}", "sample_tokens": S},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {S} tokens of the T={T} batch as one batch "
+                                   "(routing, dispatch, stats, FFN, combine), per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def traffic_record(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    with open(os.path.join(ROOT, "sparse_mixture_experts_47_b300", "csrc", kernel_file), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    rec = None
+    for line in open(path):
+        line = line.strip()
+        if line.startswith("{") and line.endswith("}"):
+            try:
+                r = json.loads(line)
+            except ValueError:
+                continue
+            if r.get("source_sha256_16") == h:
+                rec = r
+    return rec
+
+
+def run_ours(args, w, T):
+    import sparse_mixture_experts_47_b300 as moe
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    inp = mi.generate(w, T, dev)
+    if world > 1:      # each rank its own batch of tokens (weak scaling)
+        g = torch.Generator(device=dev)
+        g.manual_seed(1000 + rank)
+        inp["x"] = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
+    cfg = moe.config_for(w, T, out_dtype=moe.DTYPE_BF16)
+    weights = {k: inp.get(k) for k in moe._WEIGHT_KEYS}
+    ws = moe.Workspace(dev)
+    outs = moe.layer_forward(cfg, inp["x"], weights, workspace=ws)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        moe.layer_forward(cfg, inp["x"], weights, workspace=ws, outputs=outs)
+    torch.cuda.synchronize(dev)
+    assert moe.device_status(dev) == 0
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    moe.stage_timing(True)
+    l0 = moe.kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        moe.layer_forward(cfg, inp["x"], weights, workspace=ws, outputs=outs)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    launches = moe.kernel_launches() - l0
+    stage_ms, calls = moe.stage_times()
+    moe.stage_timing(False)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    assert moe.device_status(dev) == 0
+
+    # end to end through the same C ABI call with host buffers
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty(outs["y"].shape, dtype=outs["y"].dtype).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer_forward(cfg, x_dev, weights, workspace=ws, outputs=outs)
+        y_host.copy_(outs["y"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer_forward(cfg, x_dev, weights, workspace=ws, outputs=outs)
+        y_host.copy_(outs["y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+
+    n_dropped = int(outs["n_dropped"][0])
+    counts = outs["counts"].cpu().numpy()
+    n_kept = T * w.top_k - n_dropped
+    nz = int((counts > 0).sum()) if w.capacity_factor <= 0 else int((counts > 0).sum())
+    flops, bytes_, up_flops = algorithmic(w, T, n_kept, nz)
+    peaks, src = load_peaks()
+    step_s = ms / 1e3 / args.steps
+    tc_peak = peaks["bf16_tflops_sustained"] * 1e12
+    tc_burst = peaks["bf16_tflops"] * 1e12
+    hbm = peaks["hbm_gbs"] * 1e9
+    roof_s = max(flops / tc_peak, bytes_ / hbm)
+    up_ms = stage_ms["up"] / max(calls, 1)
+    up_tflops = up_flops / (up_ms / 1e3) / 1e12
+    tr = traffic_record("gemm_tcgen05.cu")
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        S = min(T, sample_size(w))
+        inp64 = host_inputs_f64({k: (v[:S] if k == "x" else v) for k, v in inp.items()})
+        t = oracle_sample_run(w, inp64, S)
+        cpu = {"value": S / t, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"first {S} of the {T} tokens as one batch (routing, dispatch, "
+                         "stats, FFN, combine), fp64 numpy, one run"}
+    value = world * T * args.steps / (ms / 1e3)
+    line = {
+        "metric": "MoE-layer fwd tokens/s on 1 B300 (bf16) and % of roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}-shaped layer d={w.d_model} E={w.n_experts} "
+                               f"k={w.top_k} d_ff={w.d_ff} T={T}",
+                   "tokens_per_rank": T, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: weights larger than L2 stream from HBM every step",
+                   "out_dtype": "bf16"},
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_tc_kernel (up projection)",
+                     "achieved": up_tflops, "peak": peaks["bf16_tflops_sustained"],
+                     "unit": "TFLOP/s", "frac": up_tflops / peaks["bf16_tflops_sustained"],
+                     "frac_of_burst": up_tflops * 1e12 / tc_burst,
+                     "peak_source": f"{src} bf16_tflops_sustained",
+                     "traffic": (tr["dram_bytes_per_launch"] * (T / tr.get("T", T))
+                                 if tr else None)},
+        "layer_roofline": {"flops": flops, "bytes": bytes_, "roofline_ms": roof_s * 1e3,
+                           "frac": roof_s / step_s,
+                           "bound": "tensor" if flops / tc_peak > bytes_ / hbm else "hbm",
+                           "peaks": f"{src}: {peaks['bf16_tflops_sustained']} TF/s sustained, "
+                                    f"{peaks['hbm_gbs']} GB/s"},
+        "stage_ms": {k: v / max(calls, 1) for k, v in stage_ms.items()},
+        "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "clocks": clk,
+        "gpu_launches": launches,
+        "cpu_baseline": cpu,
+        "n_dropped": n_dropped,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral", choices=list(mi.WORKLOADS))
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
+    w = mi.workload(args.workload)
+    T = args.T or max(w.tokens)
+    if args.impl == "reference":
+        run_reference(args, w, T)
+    else:
+        run_ours(args, w, T)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,236 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) forward pass of a token-choice sparse
+ * Mixture-of-Experts FFN layer.
+ *
+ * The layer, for T tokens x[T, d], E experts, top-k, expert width F:
+ *   logits = x W_r^T (+ logit_bias)              router linear, no bias term
+ *   probs  = softmax(logits) over the E experts
+ *   idx    = top-k of (probs + select_bias)       (bias for selection only)
+ *   w      = probs[idx] / sum probs[idx]          renormalised gate weights
+ *   capacity C = ceil(cf * T * k / E); per expert the first C assignments in
+ *   flattened (t*k + j) order are kept, the rest dropped (contribute zero)
+ *   y[t]   = sum_j keep * w[t,j] * FFN_{idx[t,j]}(x[t]) + shared(x[t])
+ *   FFN_e  = W2_e (silu(W1_e x) * W3_e x)  (SwiGLU)  or  W2_e relu(W1_e x)
+ *   f_e = count_e / (T k), p_e = mean_t probs[t,e], aux = E sum_e f_e p_e
+ *
+ * Sources (page title, section):
+ *   "Mixture of Experts", LLM Transformer book (waylandz.com) ch. 30:
+ *     §30.2.3 router, §30.2.4 expert FFN, §30.2.6 load-balancing loss,
+ *     §30.4.5 shared expert, §30.6.1 MoELayer.
+ *   "Mixture of Experts (MoE) memo" (iwashi.co): auxiliary loss worked
+ *     example; DeepSeek-V3 aux-loss-free selection bias; Kimi K3 quantile
+ *     balancing.
+ *   "混合エキスパートモデル（MoE）実践" (deepseekmodel.com): TopKRouter
+ *     (softmax, top-k, renormalise, capacity), capacity factor and token
+ *     dropping, load_balance_loss, BiasBalancedRouter, grouping tokens by
+ *     expert for a grouped GEMM (expert parallelism section).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers, row-major and dense, owned by
+ *     the caller.  The library never allocates or frees device memory and
+ *     never synchronises the stream, except moe_device_status().
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and enqueues kernels only.
+ *   - Arguments are validated on the host before any launch; a call that
+ *     returns an error has enqueued nothing.  Launch failures are reported
+ *     as MOE_ERR_CUDA.
+ *   - Layouts: x [T, d] in cfg->dtype; W_r [E, d] fp32 (nn.Linear
+ *     [out, in]); W1, W3 [E, F, d] and W2 [E, d, F] in cfg->dtype; shared
+ *     expert Ws1, Ws3 [Fs, d], Ws2 [d, Fs]; topk_idx [T, k] int32;
+ *     topk_w [T, k] fp32; probs [T, E] fp32.
+ *   - Results are bitwise reproducible run to run (no floating-point
+ *     atomics; fixed reduction orders).
+ *   - Pointers must be 16-byte aligned (cudaMalloc and torch allocations
+ *     are); d and F must be multiples of 8 for bf16 and of 4 for fp32.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad size */
+    MOE_ERR_UNSUPPORTED = -2,    /* a shape or option this build does not run */
+    MOE_ERR_WORKSPACE = -3,      /* workspace smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = -4,           /* a CUDA runtime/launch error */
+    MOE_ERR_DEVICE_TIMEOUT = -5  /* a kernel gave up a bounded wait (see
+                                    moe_device_status) */
+} moe_status;
+
+enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 };
+enum { MOE_DTYPE_FP32 = 0, MOE_DTYPE_BF16 = 1 };
+enum { MOE_SELECT_PROBS = 0, MOE_SELECT_LOGITS = 1 };
+
+typedef struct {
+    int32_t T;                /* tokens (batch * seq flattened), >= 0 */
+    int32_t d_model;          /* d */
+    int32_t n_experts;        /* E, 1..1024 */
+    int32_t top_k;            /* k, 1..min(E, 16) */
+    int32_t d_ff;             /* F, routed expert width */
+    int32_t act;              /* MOE_ACT_* */
+    int32_t dtype;            /* MOE_DTYPE_* of x and expert weights */
+    float capacity_factor;    /* <= 0: no capacity limit */
+    int32_t d_ff_shared;      /* Fs; 0: no shared expert (SwiGLU when > 0) */
+    int32_t select_space;     /* MOE_SELECT_*: where select_bias is added */
+    int32_t quantile_balance; /* 1: select_bias = -Q_{1-k/E}(probs[:, e]) */
+    int32_t out_dtype;        /* dtype of y: MOE_DTYPE_FP32 or MOE_DTYPE_BF16 */
+} moe_config;
+
+/* Capacity C = ceil(cf * T * k / E), or T*k when cf <= 0 (no limit).
+ * Source: deepseekmodel.com page, section "capacity factor、token dropping". */
+int64_t moe_capacity(const moe_config *cfg);
+
+/* Bytes of device workspace moe_layer_forward() needs for `cfg`; the stage
+ * calls that take a workspace need at most this much.  0 on invalid cfg. */
+size_t moe_workspace_size(const moe_config *cfg);
+
+/* Router: x W_r^T (+ logit_bias), softmax, top-k of (score + select_bias),
+ * renormalisation of the selected unbiased probabilities.
+ * Sources: ch. 30 §30.2.3 steps 1-4; deepseekmodel.com TopKRouter and
+ * BiasBalancedRouter; iwashi.co aux-loss-free and quantile sections.
+ *   x           [T, d] cfg->dtype
+ *   w_r         [E, d] fp32
+ *   logit_bias  [E] fp32 or NULL: added to the logits (part of the router)
+ *   select_bias [E] fp32 or NULL: added to probs (select_space PROBS) or to
+ *               logits (LOGITS) for selection only; ignored when
+ *               cfg->quantile_balance
+ *   topk_idx    [T, k] int32 out: experts by descending selection score,
+ *               exactly equal scores ordered by lower expert index
+ *   topk_w      [T, k] fp32 out: renormalised gate weights
+ *   probs       [T, E] fp32 out or NULL
+ *   p_mean      [E] fp32 out or NULL: p_e = mean_t probs[t, e]
+ *   select_bias_out [E] fp32 out: the quantile bias; required iff
+ *               cfg->quantile_balance, else may be NULL
+ *   ws, ws_bytes: workspace (>= moe_workspace_size(cfg)) */
+int moe_router_topk(const moe_config *cfg, const void *x, const float *w_r,
+                    const float *logit_bias, const float *select_bias,
+                    int32_t *topk_idx, float *topk_w, float *probs,
+                    float *p_mean, float *select_bias_out, void *ws,
+                    size_t ws_bytes, moe_stream_t stream);
+
+/* Dispatch: group the T*k assignments by expert (stable in t*k+j order),
+ * apply capacity.  Source: deepseekmodel.com expert-parallel dispatch
+ * (stable argsort by expert, bincount) and capacity section.
+ *   topk_idx  [T, k] int32 in, values in [0, E)
+ *   counts    [E] int32 out: assignments per expert before drops
+ *   offsets   [E+1] int32 out: exclusive scan of min(counts, C)
+ *   perm      [T*k] int32 out: perm[s] = t*k+j of sorted row s, for
+ *             s < offsets[E]; later entries untouched
+ *   inv       [T*k] int32 out: sorted row of slot t*k+j, or -1 if dropped
+ *   n_dropped [1] int32 out */
+int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx,
+                 int32_t *counts, int32_t *offsets, int32_t *perm,
+                 int32_t *inv, int32_t *n_dropped, void *ws, size_t ws_bytes,
+                 moe_stream_t stream);
+
+/* Per-expert FFN on the grouped rows: out_sorted[s] = FFN_e(x[perm[s] / k])
+ * for offsets[e] <= s < offsets[e+1].  Source: ch. 30 §30.2.4 / §30.6.1.
+ *   x          [T, d]; perm, offsets as produced by moe_dispatch
+ *   w1, w3, w2 expert weights (w3 NULL for ReLU)
+ *   out_sorted [T*k, d] fp32 out (rows >= offsets[E] untouched) */
+int moe_expert_ffn(const moe_config *cfg, const void *x, const int32_t *perm,
+                   const int32_t *offsets, const void *w1, const void *w3,
+                   const void *w2, float *out_sorted, void *ws,
+                   size_t ws_bytes, moe_stream_t stream);
+
+/* Combine: y[t] = sum_j [inv[t*k+j] >= 0] w[t,j] out_sorted[inv[t*k+j]]
+ *               + shared_out[t].   Source: ch. 30 §30.6.1 (weighted
+ * accumulate), §30.4.5 (routed + shared).
+ *   out_sorted [*, d] fp32; inv [T*k]; topk_w [T, k]
+ *   shared_out [T, d] fp32 or NULL;  y [T, d] in cfg->out_dtype */
+int moe_combine(const moe_config *cfg, const float *out_sorted,
+                const int32_t *inv, const float *topk_w,
+                const float *shared_out, void *y, moe_stream_t stream);
+
+/* Load statistics from (probs, indices), the inputs of the pages'
+ * load_balance_loss: f_e = count_e/(T k), p_e = mean_t probs[t,e],
+ * aux = E sum f_e p_e (no coefficient), load_max_over_mean =
+ * max_e count_e / (T k / E).  Sources: ch. 30 §30.2.6; iwashi.co worked
+ * example; deepseekmodel.com load_balance_loss.
+ *   probs [T, E] fp32; topk_idx [T, k]; f, p [E] out; aux, load [1] out;
+ *   counts [E] int32 out or NULL */
+int moe_load_stats(const moe_config *cfg, const int32_t *topk_idx,
+                   const float *probs, int32_t *counts, float *f, float *p,
+                   float *aux, float *load_max_over_mean, void *ws,
+                   size_t ws_bytes, moe_stream_t stream);
+
+/* Weights of one layer (device pointers; see layouts above). */
+typedef struct {
+    const float *w_r;          /* [E, d] fp32 */
+    const float *logit_bias;   /* [E] or NULL */
+    const float *select_bias;  /* [E] or NULL */
+    const void *w1, *w3, *w2;  /* routed experts (w3 NULL for ReLU) */
+    const void *ws1, *ws3, *ws2; /* shared expert, NULL when d_ff_shared = 0 */
+} moe_layer_weights;
+
+/* Outputs of one layer call (device pointers; NULL = not wanted, except y). */
+typedef struct {
+    void *y;                   /* [T, d] cfg->out_dtype, required */
+    int32_t *topk_idx;         /* [T, k] */
+    float *topk_w;             /* [T, k] */
+    int32_t *counts;           /* [E] assignments before drops */
+    int32_t *n_dropped;        /* [1] */
+    float *f;                  /* [E] */
+    float *p;                  /* [E] */
+    float *aux;                /* [1] */
+    float *load_max_over_mean; /* [1] */
+    float *select_bias_out;    /* [E] quantile bias (quantile_balance only) */
+    int32_t *counts_unbiased;  /* [E] counts of the plain top-k, no bias */
+} moe_layer_outputs;
+
+/* The whole forward pass (router, dispatch, experts, shared expert,
+ * combine, statistics) on one stream, with no host synchronisation.
+ * Source: ch. 30 §30.6.1 MoELayer.forward returning (output, aux_loss). */
+int moe_layer_forward(const moe_config *cfg, const void *x,
+                      const moe_layer_weights *wts,
+                      const moe_layer_outputs *out, void *ws,
+                      size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device error word that
+ * kernels set when a bounded wait gave up (MOE_ERR_DEVICE_TIMEOUT), or
+ * MOE_OK.  The only call that blocks the host. */
+int moe_device_status(moe_stream_t stream);
+
+/* Static description of an error code. */
+const char *moe_strerror(int status);
+
+/* Number of kernels this library has launched in this process (all entry
+ * points, all devices); a monotone counter for launch accounting. */
+int64_t moe_kernel_launches(void);
+
+/* Stages of moe_layer_forward that per-stage timing separates. */
+enum {
+    MOE_STAGE_ROUTER = 0,   /* router, softmax, top-k (+ quantile bias) */
+    MOE_STAGE_DISPATCH,     /* histogram, scan, stable scatter */
+    MOE_STAGE_STATS,        /* f, p, aux, load max/mean */
+    MOE_STAGE_GATHER,       /* rows into the grouped layout */
+    MOE_STAGE_UP,           /* grouped up projection + activation */
+    MOE_STAGE_DOWN,         /* grouped down projection */
+    MOE_STAGE_SHARED,       /* shared expert */
+    MOE_STAGE_COMBINE,      /* weighted combine */
+    MOE_NUM_STAGES
+};
+
+/* Optional per-stage timing of moe_layer_forward: while enabled, each call
+ * records a CUDA event on its stream before and after every stage (events
+ * are created on first use; no device memory is allocated).  Disabled by
+ * default; enabling or disabling discards pending records. */
+int moe_stage_timing_enable(int on);
+
+/* Waits for the recorded events, writes the summed milliseconds of each
+ * stage into stage_ms[MOE_NUM_STAGES] and the number of timed calls into
+ * *calls, then discards the records.  Blocks the host. */
+int moe_stage_timing_read(double *stage_ms, int64_t *calls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

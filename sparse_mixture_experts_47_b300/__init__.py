@@ -1,0 +1,305 @@
+"""Token-choice sparse MoE FFN layer forward on B300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``libmoe_b300.so`` (declared in
+``include/moe.h``): every step of the layer runs in the library's CUDA
+kernels.  This module only marshals arguments: it allocates outputs and the
+workspace with torch on the input's device and passes raw device pointers and
+torch's current CUDA stream.  There is no CPU path; the import fails if the
+library has not been built (``python sparse_mixture_experts_47_b300/build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Dict, Optional
+
+import torch
+
+__all__ = [
+    "MoEConfig", "MoEError", "lib", "capacity", "workspace_size", "router_topk", "dispatch",
+    "expert_ffn", "combine", "load_stats", "layer_forward", "device_status", "Workspace",
+    "ACT_RELU", "ACT_SWIGLU", "DTYPE_FP32", "DTYPE_BF16", "SELECT_PROBS", "SELECT_LOGITS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+ACT_RELU, ACT_SWIGLU = 0, 1
+DTYPE_FP32, DTYPE_BF16 = 0, 1
+SELECT_PROBS, SELECT_LOGITS = 0, 1
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
+          -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {status} ({STATUS.get(status, '?')}: "
+                         f"{lib.moe_strerror(status).decode()})")
+        self.status = status
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("d_ff", ctypes.c_int32), ("act", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float), ("d_ff_shared", ctypes.c_int32),
+                ("select_space", ctypes.c_int32), ("quantile_balance", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32)]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_r", "logit_bias", "select_bias", "w1", "w3", "w2", "ws1", "ws3", "ws2")]
+
+
+class _Outputs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("y", "topk_idx", "topk_w", "counts", "n_dropped", "f", "p", "aux",
+                 "load_max_over_mean", "select_bias_out", "counts_unbiased")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python sparse_mixture_experts_47_b300/build.py`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, Z, V = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    C = ctypes.POINTER(_Config)
+    L.moe_capacity.argtypes = [C]; L.moe_capacity.restype = ctypes.c_int64
+    L.moe_workspace_size.argtypes = [C]; L.moe_workspace_size.restype = Z
+    L.moe_router_topk.argtypes = [C] + [P] * 10 + [Z, V]; L.moe_router_topk.restype = I
+    L.moe_dispatch.argtypes = [C] + [P] * 7 + [Z, V]; L.moe_dispatch.restype = I
+    L.moe_expert_ffn.argtypes = [C] + [P] * 8 + [Z, V]; L.moe_expert_ffn.restype = I
+    L.moe_combine.argtypes = [C] + [P] * 5 + [V]; L.moe_combine.restype = I
+    L.moe_load_stats.argtypes = [C] + [P] * 8 + [Z, V]; L.moe_load_stats.restype = I
+    L.moe_layer_forward.argtypes = [C, P, ctypes.POINTER(_Weights), ctypes.POINTER(_Outputs),
+                                    P, Z, V]
+    L.moe_layer_forward.restype = I
+    L.moe_device_status.argtypes = [V]; L.moe_device_status.restype = I
+    L.moe_strerror.argtypes = [I]; L.moe_strerror.restype = ctypes.c_char_p
+    L.moe_kernel_launches.argtypes = []; L.moe_kernel_launches.restype = ctypes.c_int64
+    L.moe_stage_timing_enable.argtypes = [I]; L.moe_stage_timing_enable.restype = I
+    L.moe_stage_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_int64)]
+    L.moe_stage_timing_read.restype = I
+    return L
+
+
+lib = _load()
+
+
+@dataclasses.dataclass
+class MoEConfig:
+    T: int
+    d_model: int
+    n_experts: int
+    top_k: int
+    d_ff: int
+    act: int = ACT_SWIGLU
+    dtype: int = DTYPE_BF16
+    capacity_factor: float = 0.0
+    d_ff_shared: int = 0
+    select_space: int = SELECT_PROBS
+    quantile_balance: int = 0
+    out_dtype: int = DTYPE_FP32
+
+    def c(self) -> _Config:
+        return _Config(*(getattr(self, f.name) for f in dataclasses.fields(self)))
+
+    def with_T(self, T: int) -> "MoEConfig":
+        return dataclasses.replace(self, T=T)
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == DTYPE_FP32 else torch.bfloat16
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != MOE_OK:
+        raise MoEError(fn, rc)
+
+
+def capacity(cfg: MoEConfig) -> int:
+    return int(lib.moe_capacity(ctypes.byref(cfg.c())))
+
+
+def workspace_size(cfg: MoEConfig) -> int:
+    return int(lib.moe_workspace_size(ctypes.byref(cfg.c())))
+
+
+class Workspace:
+    """A device byte buffer reused across calls (grows on demand)."""
+
+    def __init__(self, device):
+        self.device = torch.device(device)
+        self.buf = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def _ws(cfg, device, workspace):
+    n = workspace_size(cfg)
+    buf = (workspace or Workspace(device)).get(n)
+    return buf, buf.numel()
+
+
+def router_topk(cfg: MoEConfig, x, w_r, logit_bias=None, select_bias=None, want_probs=False,
+                want_p=True, workspace: Optional[Workspace] = None) -> Dict[str, torch.Tensor]:
+    dev = x.device
+    T, E, k = cfg.T, cfg.n_experts, cfg.top_k
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    probs = torch.empty((T, E), dtype=torch.float32, device=dev) if want_probs else None
+    p = torch.empty(E, dtype=torch.float32, device=dev) if want_p else None
+    sb = torch.empty(E, dtype=torch.float32, device=dev) if cfg.quantile_balance else None
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_router_topk", lib.moe_router_topk(
+        ctypes.byref(cfg.c()), _ptr(x), _ptr(w_r), _ptr(logit_bias), _ptr(select_bias),
+        _ptr(idx), _ptr(w), _ptr(probs), _ptr(p), _ptr(sb), _ptr(buf), nb, _stream(dev)))
+    return {"idx": idx, "w": w, "probs": probs, "p": p, "select_bias": sb}
+
+
+def dispatch(cfg: MoEConfig, idx, workspace: Optional[Workspace] = None) -> Dict[str, torch.Tensor]:
+    dev = idx.device
+    Tk, E = cfg.T * cfg.top_k, cfg.n_experts
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.full((max(Tk, 1),), -7, dtype=torch.int32, device=dev)
+    inv = torch.full((max(Tk, 1),), -7, dtype=torch.int32, device=dev)
+    nd = torch.empty(1, dtype=torch.int32, device=dev)
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_dispatch", lib.moe_dispatch(
+        ctypes.byref(cfg.c()), _ptr(idx), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+        _ptr(nd), _ptr(buf), nb, _stream(dev)))
+    return {"counts": counts, "offsets": offsets, "perm": perm[:Tk], "inv": inv[:Tk],
+            "n_dropped": nd}
+
+
+def expert_ffn(cfg: MoEConfig, x, perm, offsets, w1, w3, w2,
+               workspace: Optional[Workspace] = None) -> torch.Tensor:
+    dev = x.device
+    out = torch.zeros((max(cfg.T * cfg.top_k, 1), cfg.d_model), dtype=torch.float32, device=dev)
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_expert_ffn", lib.moe_expert_ffn(
+        ctypes.byref(cfg.c()), _ptr(x), _ptr(perm), _ptr(offsets), _ptr(w1), _ptr(w3), _ptr(w2),
+        _ptr(out), _ptr(buf), nb, _stream(dev)))
+    return out
+
+
+def combine(cfg: MoEConfig, out_sorted, inv, topk_w, shared_out=None) -> torch.Tensor:
+    dev = out_sorted.device
+    ydt = torch.float32 if cfg.out_dtype == DTYPE_FP32 else torch.bfloat16
+    y = torch.empty((cfg.T, cfg.d_model), dtype=ydt, device=dev)
+    _check("moe_combine", lib.moe_combine(
+        ctypes.byref(cfg.c()), _ptr(out_sorted), _ptr(inv), _ptr(topk_w), _ptr(shared_out),
+        _ptr(y), _stream(dev)))
+    return y
+
+
+def load_stats(cfg: MoEConfig, idx, probs, workspace: Optional[Workspace] = None):
+    dev = probs.device
+    E = cfg.n_experts
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    f = torch.empty(E, dtype=torch.float32, device=dev)
+    p = torch.empty(E, dtype=torch.float32, device=dev)
+    aux = torch.empty(1, dtype=torch.float32, device=dev)
+    load = torch.empty(1, dtype=torch.float32, device=dev)
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_load_stats", lib.moe_load_stats(
+        ctypes.byref(cfg.c()), _ptr(idx), _ptr(probs), _ptr(counts), _ptr(f), _ptr(p),
+        _ptr(aux), _ptr(load), _ptr(buf), nb, _stream(dev)))
+    return {"counts": counts, "f": f, "p": p, "aux": aux, "load_max_over_mean": load}
+
+
+_WEIGHT_KEYS = ("w_r", "logit_bias", "select_bias", "w1", "w3", "w2", "ws1", "ws3", "ws2")
+
+
+def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
+                  workspace: Optional[Workspace] = None, outputs: Optional[Dict] = None,
+                  want_unbiased_counts: bool = False) -> Dict[str, torch.Tensor]:
+    """The whole layer on torch's current stream.  ``weights`` holds device
+    tensors under the keys w_r, logit_bias, select_bias, w1, w3, w2, ws1,
+    ws3, ws2 (missing or None = absent).  ``outputs`` may pass preallocated
+    output tensors (same keys as the returned dict)."""
+    dev = x.device
+    T, E, k, d = cfg.T, cfg.n_experts, cfg.top_k, cfg.d_model
+    o = dict(outputs or {})
+    ydt = torch.float32 if cfg.out_dtype == DTYPE_FP32 else torch.bfloat16
+
+    def need(key, shape, dtype):
+        if o.get(key) is None:
+            o[key] = torch.empty(shape, dtype=dtype, device=dev)
+
+    need("y", (T, d), ydt)
+    need("idx", (T, k), torch.int32)
+    need("w", (T, k), torch.float32)
+    need("counts", (E,), torch.int32)
+    need("n_dropped", (1,), torch.int32)
+    need("f", (E,), torch.float32)
+    need("p", (E,), torch.float32)
+    need("aux", (1,), torch.float32)
+    need("load_max_over_mean", (1,), torch.float32)
+    if cfg.quantile_balance:
+        need("select_bias", (E,), torch.float32)
+    if want_unbiased_counts:
+        need("counts_unbiased", (E,), torch.int32)
+    W = _Weights(*(_ptr(weights.get(key)) for key in _WEIGHT_KEYS))
+    O = _Outputs(_ptr(o["y"]), _ptr(o["idx"]), _ptr(o["w"]), _ptr(o["counts"]),
+                 _ptr(o["n_dropped"]), _ptr(o["f"]), _ptr(o["p"]), _ptr(o["aux"]),
+                 _ptr(o["load_max_over_mean"]), _ptr(o.get("select_bias")),
+                 _ptr(o.get("counts_unbiased")))
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_layer_forward", lib.moe_layer_forward(
+        ctypes.byref(cfg.c()), _ptr(x), ctypes.byref(W), ctypes.byref(O), _ptr(buf), nb,
+        _stream(dev)))
+    return o
+
+
+STAGES = ("router", "dispatch", "stats", "gather", "up", "down", "shared", "combine")
+
+
+def kernel_launches() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib.moe_kernel_launches())
+
+
+def stage_timing(on: bool) -> None:
+    _check("moe_stage_timing_enable", lib.moe_stage_timing_enable(int(on)))
+
+
+def stage_times():
+    """(summed ms per stage, number of timed layer calls); blocks the host."""
+    ms = (ctypes.c_double * len(STAGES))()
+    calls = ctypes.c_int64(0)
+    _check("moe_stage_timing_read", lib.moe_stage_timing_read(ms, ctypes.byref(calls)))
+    return dict(zip(STAGES, list(ms))), int(calls.value)
+
+
+def device_status(device=None) -> int:
+    return int(lib.moe_device_status(_stream(device or torch.cuda.current_device())))
+
+
+def config_for(workload, T: int, out_dtype: int = DTYPE_FP32) -> MoEConfig:
+    """MoEConfig of a workload description (an object with the fields of
+    ``moe_inputs.MoEWorkload``) at T tokens."""
+    return MoEConfig(
+        T=T, d_model=workload.d_model, n_experts=workload.n_experts, top_k=workload.top_k,
+        d_ff=workload.d_ff, act=ACT_SWIGLU if workload.act == "swiglu" else ACT_RELU,
+        dtype=DTYPE_FP32 if workload.dtype == "fp32" else DTYPE_BF16,
+        capacity_factor=float(workload.capacity_factor), d_ff_shared=workload.d_ff_shared,
+        select_space=SELECT_PROBS, quantile_balance=int(bool(workload.quantile_balance)),
+        out_dtype=out_dtype)

@@ -1,0 +1,156 @@
+// Dispatch: group the T*k (token, slot) assignments by expert, keeping the
+// flattened (t*k + j) order inside each expert, and apply the capacity cap.
+//
+// Sources: "混合エキスパートモデル（MoE）実践" (deepseekmodel.com), expert
+// parallelism section (stable argsort by destination, bincount; the grouped
+// layout is what makes one grouped GEMM over all experts possible) and the
+// capacity section (hard cap C per expert, overflow dropped).
+//
+// Three launches, all integer work and exactly reproducible:
+//   1. per-chunk histograms hist[b][e] (chunks of 1024 slots),
+//   2. one CTA: counts[e] = sum_b hist[b][e], per-chunk bases
+//      base[b][e] = sum_{b'<b} hist[b'][e], offsets = exclusive scan of
+//      min(counts, C), n_dropped,
+//   3. per chunk, one warp walks its slots in order; the rank of a slot in
+//      its expert is base[b][e] + (earlier slots of e in the chunk), found
+//      with __match_any_sync; rank < C keeps the slot at row offsets[e] +
+//      rank.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__global__ void dispatch_hist_kernel(const int32_t *idx, long long n, int E, int32_t *hist) {
+    extern __shared__ int h[];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    const long long base = (long long)blockIdx.x * kDispatchChunk;
+    for (int i = threadIdx.x; i < kDispatchChunk && base + i < n; i += blockDim.x) {
+        const int e = idx[base + i];
+        if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+        else flag_error(kErrBadIndex);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[(size_t)blockIdx.x * E + i] = h[i];
+}
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+__device__ int block_exclusive_scan_1024(int v, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int wt = warp_tot[lane], wi = wt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        warp_tot[lane] = wi - wt;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    return warp_tot[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(
+        const int32_t *hist, int nblk, int E, long long C, int32_t *block_base,
+        int32_t *counts, int32_t *offsets, int32_t *n_dropped) {
+    __shared__ int warp_tot[32];
+    __shared__ int total;
+    const int e = threadIdx.x;
+    int kept = 0, run = 0;
+    if (e < E) {
+        for (int b = 0; b < nblk; ++b) {
+            const size_t o = (size_t)b * E + e;
+            if (block_base) block_base[o] = run;
+            run += hist[o];
+        }
+        if (counts) counts[e] = run;
+        kept = (long long)run < C ? run : (int)C;
+    }
+    block_exclusive_scan_1024(run, warp_tot, &total);
+    const int all_total = total;
+    __syncthreads();
+    const int ex = block_exclusive_scan_1024(kept, warp_tot, &total);
+    if (offsets && e < E) offsets[e] = ex;
+    if (e == 0) {
+        if (offsets) offsets[E] = total;
+        if (n_dropped) *n_dropped = all_total - total;
+    }
+}
+
+__global__ void dispatch_scatter_kernel(const int32_t *idx, long long n, int E, long long C,
+                                        const int32_t *block_base, const int32_t *offsets,
+                                        int32_t *perm, int32_t *inv) {
+    extern __shared__ int run[];
+    const int lane = threadIdx.x;
+    for (int i = lane; i < E; i += 32) run[i] = block_base[(size_t)blockIdx.x * E + i];
+    __syncwarp();
+    const long long base = (long long)blockIdx.x * kDispatchChunk;
+    for (int i0 = 0; i0 < kDispatchChunk && base + i0 < n; i0 += 32) {
+        const long long f = base + i0 + lane;
+        int e = -1;
+        if (f < n) {
+            e = idx[f];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int rank = 0;
+        if (e >= 0) rank = run[e] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (e >= 0 && lane == 31 - __clz(peers)) run[e] += __popc(peers);
+        __syncwarp();
+        if (f < n) {
+            if (e >= 0 && rank < C) {
+                const int s = offsets[e] + rank;
+                perm[s] = (int32_t)f;
+                inv[f] = s;
+            } else {
+                inv[f] = -1;
+            }
+        }
+    }
+}
+
+cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long long C,
+                            int32_t *hist, int32_t *block_base, int32_t *counts,
+                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *n_dropped,
+                            cudaStream_t st) {
+    (void)k;
+    const int nblk = dispatch_blocks(n);
+    if (nblk > 0) {
+        dispatch_hist_kernel<<<nblk, 256, sizeof(int) * E, st>>>(idx, n, E, hist);
+        note_launch();
+    }
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(hist, nblk, E, C, block_base, counts, offsets,
+                                             n_dropped);
+    note_launch();
+    if (nblk > 0) {
+        dispatch_scatter_kernel<<<nblk, 32, sizeof(int) * E, st>>>(idx, n, E, C, block_base,
+                                                                   offsets, perm, inv);
+        note_launch();
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_histogram(const int32_t *idx, long long n, int E, int32_t *hist,
+                             int32_t *counts, cudaStream_t st) {
+    const int nblk = dispatch_blocks(n);
+    if (nblk > 0) {
+        dispatch_hist_kernel<<<nblk, 256, sizeof(int) * E, st>>>(idx, n, E, hist);
+        note_launch();
+    }
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(hist, nblk, E, (long long)1 << 40, nullptr, counts,
+                                             nullptr, nullptr);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace moe

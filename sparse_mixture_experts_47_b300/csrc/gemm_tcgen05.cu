@@ -1,0 +1,487 @@
+// Grouped expert GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA, for the bf16 layer.
+//
+// Expert FFN ("Mixture of Experts", waylandz.com ch. 30, §30.2.4 / §30.6.1),
+// on the rows grouped by expert ("混合エキスパートモデル（MoE）実践",
+// deepseekmodel.com: contiguous per-expert rows make one grouped GEMM over
+// all experts possible):
+//   up   SwiGLU: H = silu(A W1_e^T) * (A W3_e^T)    ReLU: H = relu(A W1_e^T)
+//   down O = H W2_e^T  (fp32 out)
+// A [rows, K] and all weights [E*N, K] are K-major bf16, exactly the
+// nn.Linear layout, so both operands are "K-major" for tcgen05.mma.
+//
+// One CTA per SM, persistent over output tiles of 128 rows.  Tile order:
+// experts in order; inside an expert, N-tiles outer and M-tiles inner, so the
+// CTAs running at the same time share one expert's weight tiles through L2
+// and each expert's weights stream from HBM about once.
+//   warp 0     TMA producer: A tile [128 x 64] + B tile [256 x 64] per stage
+//              (SwiGLU: 128 rows of W1 and the same 128 rows of W3),
+//              128-byte swizzle, 4 stages in shared memory
+//   warp 1     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128, N=256,
+//              K=16 per instruction, fp32 accumulator in TMEM
+//   warp 2     TMEM allocator (512 columns: two 256-column accumulators)
+//   warps 4-7  epilogue: tcgen05.ld of 32 TMEM lanes each, activation,
+//              bf16 (up) or fp32 (down) stores
+// Every mbarrier wait is bounded (about 2 s of no progress); on expiry the
+// kernel sets the device error word, stops issuing, lets its own copies and
+// MMAs land, frees TMEM and returns.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <cuda.h>
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;              // rows per tile (UMMA M)
+constexpr int BNM = 256;             // UMMA N (B rows per stage)
+constexpr int BK = 64;               // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BYTES = BNM * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int TMEM_COLS = 512;
+constexpr int ACC_COLS = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
+
+struct Args {
+    int mode;          // GEMM_UP_SWIGLU, GEMM_UP_RELU, GEMM_DOWN
+    int N;             // output columns
+    int K;
+    int n_ntiles;      // N-tiles of the output (128 cols for SwiGLU, 256 otherwise)
+    int b_rows;        // weight rows per expert (F for up, d for down)
+    const int32_t *tile_e, *tile_start, *n_mtiles, *offsets;
+    void *C;
+    int ldc;
+};
+
+__host__ __device__ constexpr size_t smem_bytes() {
+    return (size_t)STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256 /* barriers */;
+}
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait; false when the limit expired or another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            flag_error(kErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// 32 TMEM lanes x 16 consecutive 32-bit columns; thread i reads lane base+i.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 8-row (1024-byte) atoms.  Fields: start address >> 4 (bits
+// 0-13), leading byte offset >> 4 (16-29; unused for this layout), stride
+// byte offset >> 4 = 1024 >> 4 (32-45), descriptor version 1 (bits 46-47),
+// swizzle mode 2 = 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+struct TileCoord {
+    int e, m0, mend, n0;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const Args &g, int L) {
+    const int gm = L / g.n_ntiles;
+    const int e = g.tile_e[gm];
+    const int st = g.tile_start[e];
+    const int mt_e = g.tile_start[e + 1] - st;
+    const int local = L - st * g.n_ntiles;
+    const int nt = local / mt_e, mt = local - nt * mt_e;
+    TileCoord c;
+    c.e = e;
+    c.m0 = g.offsets[e] + mt * BM;
+    c.mend = g.offsets[e + 1];
+    c.n0 = nt * (g.mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM);
+    return c;
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
+    uint4 u;
+    uint32_t *w = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    return u;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256, 1)
+grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmB1, Args g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done[1]
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 4);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total = (*g.n_mtiles) * g.n_ntiles;
+    const int nk = (g.K + BK - 1) / BK;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0;   // stages with a load in flight or unconsumed
+        bool ok = true;
+        for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+            const TileCoord c = decode_tile(g, L);
+            int b0, b1;
+            if (MODE == GEMM_UP_SWIGLU) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
+            else { b0 = c.e * g.b_rows + c.n0; b1 = b0 + BNM / 2; }
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+                const uint32_t fb = full0 + 8 * stage;
+                mbar_expect_tx(fb, STAGE_BYTES);
+                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+                tma_load_2d(sa, &tmA, kb * BK, c.m0, fb);
+                tma_load_2d(sb, &tmB0, kb * BK, b0, fb);
+                tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b1, fb);
+                issued |= 1u << stage;
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok) {
+            // Let the copies already issued land before the CTA can exit.
+            for (int s = 0; s < STAGES; ++s) {
+                if (!(issued >> s & 1u)) continue;
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(full0 + 8 * s, 0) && !mbar_try_wait(full0 + 8 * s, 1) &&
+                       globaltimer() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_bf16(BM, BNM);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
+                           (kb | kk) != 0);
+                tc_commit(empty0 + 8 * stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            tc_commit(tfull0 + 8 * acc);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+        // All MMAs of this thread complete before TMEM can be freed.
+        tc_commit(done_bar);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(done_bar, 0) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        const int quarter = warp - 4;                     // TMEM lanes 32*quarter..
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int L = blockIdx.x; L < total; L += gridDim.x) {
+            const TileCoord c = decode_tile(g, L);
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const int row = c.m0 + quarter * 32 + lane;
+            const bool vrow = row < c.mend;
+            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+            if (MODE == GEMM_UP_SWIGLU) {
+                __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+#pragma unroll 1
+                for (int cc = 0; cc < BNM / 2; cc += 16) {
+                    float gt[16], up[16];
+                    tmem_ld16(tbase + cc, gt);
+                    tmem_ld16(tbase + BNM / 2 + cc, up);
+                    tmem_ld_wait();
+                    float h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) h[i] = silu(gt[i]) * up[i];
+                    const int col = c.n0 + cc;
+                    if (vrow) {
+                        __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                        if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(h);
+                        if (col + 8 < g.N) *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(h + 8);
+                    }
+                }
+            } else if (MODE == GEMM_UP_RELU) {
+                __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+#pragma unroll 1
+                for (int cc = 0; cc < BNM; cc += 16) {
+                    float v[16];
+                    tmem_ld16(tbase + cc, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
+                    const int col = c.n0 + cc;
+                    if (vrow) {
+                        __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                        if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
+                        if (col + 8 < g.N) *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
+                    }
+                }
+            } else {
+                float *O = static_cast<float *>(g.C);
+#pragma unroll 1
+                for (int cc = 0; cc < BNM; cc += 16) {
+                    float v[16];
+                    tmem_ld16(tbase + cc, v);
+                    tmem_ld_wait();
+                    const int col = c.n0 + cc;
+                    if (vrow) {
+                        float *dst = O + (size_t)row * g.ldc + col;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (col + 4 * q < g.N)
+                                *reinterpret_cast<float4 *>(dst + 4 * q) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, K] (K contiguous), box [box_rows, 64], 128-B swizzle.
+static bool make_map(CUtensorMap *m, const void *base, long long rows, long long K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+static int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace tc
+
+// A [a_rows, K], weights B0/B1 [E*b_rows, K]; tile table from
+// launch_build_tiles with BM = 128.
+cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, const void *B0,
+                           const void *B1, int E, int b_rows, int N, int K,
+                           const int32_t *tile_e, const int32_t *tile_start,
+                           const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
+                           cudaStream_t st) {
+    using namespace tc;
+    if (a_rows == 0) return cudaSuccess;
+    CUtensorMap mA, mB0, mB1;
+    if (!make_map(&mA, A, a_rows, K, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mB0, B0, (long long)E * b_rows, K, BNM / 2)) return cudaErrorInvalidValue;
+    if (!make_map(&mB1, B1 ? B1 : B0, (long long)E * b_rows, K, BNM / 2))
+        return cudaErrorInvalidValue;
+    Args g;
+    g.mode = mode;
+    g.N = N;
+    g.K = K;
+    g.n_ntiles = (N + (mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM) - 1) /
+                 (mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM);
+    g.b_rows = b_rows;
+    g.tile_e = tile_e;
+    g.tile_start = tile_start;
+    g.n_mtiles = n_mtiles;
+    g.offsets = offsets;
+    g.C = C;
+    g.ldc = ldc;
+    const size_t smem = smem_bytes();
+    cudaError_t err;
+    if (mode == GEMM_UP_SWIGLU) {
+        err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<GEMM_UP_SWIGLU>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        grouped_gemm_tc_kernel<GEMM_UP_SWIGLU><<<num_sms(), 256, smem, st>>>(mA, mB0, mB1, g);
+        note_launch();
+    } else if (mode == GEMM_UP_RELU) {
+        err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<GEMM_UP_RELU>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        grouped_gemm_tc_kernel<GEMM_UP_RELU><<<num_sms(), 256, smem, st>>>(mA, mB0, mB1, g);
+        note_launch();
+    } else {
+        err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<GEMM_DOWN>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        grouped_gemm_tc_kernel<GEMM_DOWN><<<num_sms(), 256, smem, st>>>(mA, mB0, mB1, g);
+        note_launch();
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,93 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry
+point include/moe.h declares, and its host-only logic (capacity, workspace
+sizing, argument validation, error strings) behaves; no kernel is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import sparse_mixture_experts_47_b300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert "moe_layer_forward" in names and len(names) >= 10
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (moe_[a-z_0-9]+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert getattr(moe.lib, n) is not None
+
+
+def test_built_for_sm_103a():
+    out = subprocess.run(["/usr/local/cuda/bin/cuobjdump", "--list-elf", moe.LIB_PATH],
+                         capture_output=True, text=True).stdout
+    assert "sm_103a" in out
+
+
+def mixtral(T=16384):
+    return moe.MoEConfig(T=T, d_model=4096, n_experts=8, top_k=2, d_ff=14336)
+
+
+def test_capacity_host_logic():
+    sw = moe.MoEConfig(T=8192, d_model=1024, n_experts=8, top_k=1, d_ff=4096, act=moe.ACT_RELU,
+                       capacity_factor=1.25)
+    assert moe.capacity(sw) == 1280
+    assert moe.capacity(mixtral(100)) == 200          # no limit: T*k
+    odd = moe.MoEConfig(T=4, d_model=8, n_experts=3, top_k=2, d_ff=8, capacity_factor=0.75)
+    assert moe.capacity(odd) == 2
+
+
+def test_workspace_size_scales():
+    a = moe.workspace_size(mixtral(4096))
+    b = moe.workspace_size(mixtral(16384))
+    assert 0 < a < b
+    # the grouped intermediates dominate: x_sorted + h (bf16) + out_sorted (fp32)
+    Tk = 16384 * 2
+    assert b >= Tk * (4096 * 2 + 14336 * 2 + 4096 * 4)
+    assert moe.workspace_size(moe.MoEConfig(T=0, d_model=64, n_experts=4, top_k=2, d_ff=128)) > 0
+
+
+@pytest.mark.parametrize("field,value", [
+    ("n_experts", 0), ("n_experts", 1025), ("top_k", 0), ("top_k", 17), ("d_model", 12),
+    ("d_ff", 0), ("act", 5), ("dtype", 3), ("T", -1), ("select_space", 2), ("out_dtype", 7)])
+def test_invalid_config_rejected_without_launch(field, value):
+    cfg = mixtral(16)
+    setattr(cfg, field, value)
+    assert moe.workspace_size(cfg) == 0
+    rc = moe.lib.moe_router_topk(ctypes.byref(cfg.c()), *([None] * 10), 0, None)
+    assert rc == -1
+
+
+def test_null_pointers_and_small_workspace_rejected():
+    cfg = mixtral(16)
+    c = ctypes.byref(cfg.c())
+    fake = ctypes.c_void_p(1 << 20)                       # never dereferenced on the host
+    assert moe.lib.moe_router_topk(c, None, fake, None, None, fake, fake, None, None, None,
+                                   fake, 1 << 40, None) == -1
+    assert moe.lib.moe_router_topk(c, fake, fake, None, None, fake, fake, None, None, None,
+                                   fake, 16, None) == -3
+    misaligned = ctypes.c_void_p((1 << 20) + 4)
+    assert moe.lib.moe_combine(c, misaligned, fake, fake, None, fake, None) == -1
+    qcfg = moe.MoEConfig(T=16, d_model=64, n_experts=32, top_k=2, d_ff=64, quantile_balance=1,
+                         select_space=moe.SELECT_LOGITS)
+    assert moe.lib.moe_router_topk(ctypes.byref(qcfg.c()), *([fake] * 10), 1 << 40, None) == -2
+
+
+def test_strerror():
+    for s in (0, -1, -2, -3, -4, -5):
+        assert moe.lib.moe_strerror(s)
+    assert moe.lib.moe_strerror(-99) == b"unknown status"
