@@ -70,7 +70,11 @@ def algorithmic(w, T, n_kept, counts_nonzero):
     flops = 2.0 * d * E * T + 2.0 * m * d * F * n_kept + 6.0 * d * Fs * T
     bytes_ = (m * d * F * eb) * counts_nonzero + 3 * d * Fs * eb + 4 * d * E + 2 * T * d * eb
     up_flops = 2.0 * d * F * n_kept * (2 if w.act == "swiglu" else 1)
-    return flops, bytes_, up_flops
+    # up projection alone: its weights (W1, W3) of the active experts, its
+    # input rows and its output h
+    up_bytes = ((2 if w.act == "swiglu" else 1) * d * F * eb * counts_nonzero
+                + n_kept * d * eb + n_kept * F * eb)
+    return flops, bytes_, up_flops, up_bytes
 
 
 class ClockSampler:
@@ -133,13 +137,19 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """The slowest rank's time (the job's time)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, steps, ms):
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms / 1e3)
 
 
 # --------------------------------------------------------------------------- oracle timing
@@ -302,7 +312,7 @@ def run_ours(args, w, T):
     counts = outs["counts"].cpu().numpy()
     n_kept = T * w.top_k - n_dropped
     nz = int((counts > 0).sum()) if w.capacity_factor <= 0 else int((counts > 0).sum())
-    flops, bytes_, up_flops = algorithmic(w, T, n_kept, nz)
+    flops, bytes_, up_flops, up_bytes = algorithmic(w, T, n_kept, nz)
     peaks, src = load_peaks()
     step_s = ms / 1e3 / args.steps
     tc_peak = peaks["bf16_tflops_sustained"] * 1e12
@@ -311,7 +321,22 @@ def run_ours(args, w, T):
     roof_s = max(flops / tc_peak, bytes_ / hbm)
     up_ms = stage_ms["up"] / max(calls, 1)
     up_tflops = up_flops / (up_ms / 1e3) / 1e12
+    up_gbs = up_bytes / (up_ms / 1e3) / 1e9
     tr = traffic_record("gemm_tcgen05.cu")
+    up_tensor_bound = up_flops / tc_peak >= up_bytes / hbm
+    if up_tensor_bound:
+        roof = {"bound": "tensor", "achieved": up_tflops, "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": up_tflops / peaks["bf16_tflops_sustained"],
+                "frac_of_burst": up_tflops * 1e12 / tc_burst,
+                "peak_source": f"{src} bf16_tflops_sustained"}
+    else:
+        roof = {"bound": "hbm", "achieved": up_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": up_gbs / peaks["hbm_gbs"], "peak_source": f"{src} hbm_gbs"}
+    roof["kernel"] = "grouped_gemm_tc_kernel (up projection)"
+    roof["algorithmic_per_launch"] = {"flops": up_flops, "bytes": up_bytes}
+    roof["ms_per_launch"] = up_ms
+    roof["traffic"] = (tr["dram_bytes_per_launch"] * (T / tr.get("T", T))
+                       if tr and tr.get("workload") == w.name else None)
 
     if rank != 0:
         return
@@ -323,7 +348,7 @@ def run_ours(args, w, T):
         cpu = {"value": S / t, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"first {S} of the {T} tokens as one batch (routing, dispatch, "
                          "stats, FFN, combine), fp64 numpy, one run"}
-    value = world * T * args.steps / (ms / 1e3)
+    value = job_throughput(world, T, args.steps, ms)
     line = {
         "metric": "MoE-layer fwd tokens/s on 1 B300 (bf16) and % of roofline",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -334,20 +359,14 @@ def run_ours(args, w, T):
                    "tokens_per_rank": T, "parallelism": f"replicas x{world}",
                    "l2": "no flush: weights larger than L2 stream from HBM every step",
                    "out_dtype": "bf16"},
-        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_tc_kernel (up projection)",
-                     "achieved": up_tflops, "peak": peaks["bf16_tflops_sustained"],
-                     "unit": "TFLOP/s", "frac": up_tflops / peaks["bf16_tflops_sustained"],
-                     "frac_of_burst": up_tflops * 1e12 / tc_burst,
-                     "peak_source": f"{src} bf16_tflops_sustained",
-                     "traffic": (tr["dram_bytes_per_launch"] * (T / tr.get("T", T))
-                                 if tr else None)},
+        "roofline": roof,
         "layer_roofline": {"flops": flops, "bytes": bytes_, "roofline_ms": roof_s * 1e3,
                            "frac": roof_s / step_s,
                            "bound": "tensor" if flops / tc_peak > bytes_ / hbm else "hbm",
                            "peaks": f"{src}: {peaks['bf16_tflops_sustained']} TF/s sustained, "
                                     f"{peaks['hbm_gbs']} GB/s"},
         "stage_ms": {k: v / max(calls, 1) for k, v in stage_ms.items()},
-        "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(world, T, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
         "clocks": clk,
