@@ -61,8 +61,10 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = -2,    /* a shape or option this build does not run */
     MOE_ERR_WORKSPACE = -3,      /* workspace smaller than moe_workspace_size() */
     MOE_ERR_CUDA = -4,           /* a CUDA runtime/launch error */
-    MOE_ERR_DEVICE_TIMEOUT = -5  /* a kernel gave up a bounded wait (see
+    MOE_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up a bounded wait (see
                                     moe_device_status) */
+    MOE_ERR_TOO_LARGE = -6       /* problem needs more than the fixed scratch
+                                    of moe_dispatch_static */
 } moe_status;
 
 enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 };
@@ -130,6 +132,30 @@ int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx,
                  int32_t *counts, int32_t *offsets, int32_t *perm,
                  int32_t *inv, int32_t *n_dropped, void *ws, size_t ws_bytes,
                  moe_stream_t stream);
+
+/* Same results as moe_dispatch, for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a deployment variant.
+ * Some callers have no way to get a workspace: code running inside a host
+ * framework that hands it only its inputs and outputs, or a service that
+ * forbids device allocations after start-up so that its memory footprint
+ * stays fixed.  For them this call takes no workspace and allocates nothing:
+ * its scratch (per-chunk histograms and bases) is a fixed
+ * MOE_DISPATCH_STATIC_SCRATCH_BYTES array compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Limit: 2 * ceil(T*k / 1024) * E * 4 bytes must fit in the scratch;
+ *     larger problems return MOE_ERR_TOO_LARGE before any launch.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture on the device.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (every entry a call reads is written by that call first), so calls
+ *     that overlap on the GPU (other streams, other host threads) race:
+ *     serialise them.
+ * Arguments, layouts and results are those of moe_dispatch. */
+#define MOE_DISPATCH_STATIC_SCRATCH_BYTES (2u << 20)
+int moe_dispatch_static(const moe_config *cfg, const int32_t *topk_idx,
+                        int32_t *counts, int32_t *offsets, int32_t *perm,
+                        int32_t *inv, int32_t *n_dropped, moe_stream_t stream);
 
 /* Per-expert FFN on the grouped rows: out_sorted[s] = FFN_e(x[perm[s] / k])
  * for offsets[e] <= s < offsets[e+1].  Source: ch. 30 §30.2.4 / §30.6.1.

@@ -31,7 +31,8 @@ SELECT_PROBS, SELECT_LOGITS = 0, 1
 
 MOE_OK = 0
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
-          -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT"}
+          -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT",
+          -6: "MOE_ERR_TOO_LARGE"}
 
 
 class MoEError(RuntimeError):
@@ -72,6 +73,7 @@ def _load():
     L.moe_workspace_size.argtypes = [C]; L.moe_workspace_size.restype = Z
     L.moe_router_topk.argtypes = [C] + [P] * 10 + [Z, V]; L.moe_router_topk.restype = I
     L.moe_dispatch.argtypes = [C] + [P] * 7 + [Z, V]; L.moe_dispatch.restype = I
+    L.moe_dispatch_static.argtypes = [C] + [P] * 6 + [V]; L.moe_dispatch_static.restype = I
     L.moe_expert_ffn.argtypes = [C] + [P] * 8 + [Z, V]; L.moe_expert_ffn.restype = I
     L.moe_combine.argtypes = [C] + [P] * 5 + [V]; L.moe_combine.restype = I
     L.moe_load_stats.argtypes = [C] + [P] * 8 + [Z, V]; L.moe_load_stats.restype = I

@@ -16,6 +16,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 using namespace moe;
@@ -277,6 +278,30 @@ int run_shared(const moe_config *c, const void *x, const void *ws1, const void *
     return MOE_OK;
 }
 
+// Fixed scratch of moe_dispatch_static (no workspace, no allocation).  In host
+// code g_dispatch_scratch only names the symbol; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+__device__ __align__(256) unsigned char g_dispatch_scratch[MOE_DISPATCH_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+int dispatch_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p)
+            return MOE_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -320,6 +345,26 @@ int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, int32_t *counts
     MOE_CUDA(launch_dispatch(topk_idx, s.Tk, (int)s.E, (int)s.k, capacity_of(cfg),
                              at<int32_t>(ws, L.hist), at<int32_t>(ws, L.block_base), counts,
                              offsets, perm, inv, n_dropped, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int moe_dispatch_static(const moe_config *cfg, const int32_t *topk_idx, int32_t *counts,
+                        int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *n_dropped,
+                        moe_stream_t stream) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    MOE_PTR(counts); MOE_PTR(offsets); MOE_PTR(n_dropped);
+    if (cfg->T > 0) { MOE_PTR(topk_idx); MOE_PTR(perm); MOE_PTR(inv); }
+    const Sizes s = sizes(cfg);
+    const size_t half = sizeof(int32_t) * (size_t)dispatch_blocks(s.Tk) * (size_t)s.E;
+    if (2 * half > MOE_DISPATCH_STATIC_SCRATCH_BYTES) return MOE_ERR_TOO_LARGE;
+    void *scratch = nullptr;
+    rc = dispatch_scratch(&scratch);
+    if (rc != MOE_OK) return rc;
+    int32_t *hist = static_cast<int32_t *>(scratch);
+    int32_t *base = reinterpret_cast<int32_t *>(static_cast<char *>(scratch) + half);
+    MOE_CUDA(launch_dispatch(topk_idx, s.Tk, (int)s.E, (int)s.k, capacity_of(cfg), hist, base,
+                             counts, offsets, perm, inv, n_dropped, (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -503,6 +548,8 @@ const char *moe_strerror(int status) {
         case MOE_ERR_WORKSPACE: return "workspace too small";
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait timed out";
+        case MOE_ERR_TOO_LARGE:
+            return "problem exceeds the fixed scratch of moe_dispatch_static";
         default: return "unknown status";
     }
 }
