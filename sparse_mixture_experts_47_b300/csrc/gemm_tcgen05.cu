@@ -47,9 +47,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 struct Args {
     int mode;          // GEMM_UP_SWIGLU, GEMM_UP_RELU, GEMM_DOWN
     int N;             // output columns
-    int K;
+    int K;             // reduction length (B's columns)
+    int a_k_period;    // A's column of reduction index k is k mod a_k_period
     int n_ntiles;      // N-tiles of the output (128 cols for SwiGLU, 256 otherwise)
     int b_rows;        // weight rows per expert (F for up, d for down)
+    int k_splits;      // work items per output tile along K (GEMM_DOWN only)
+    int kb_per_split;  // K blocks of one split
+    long long split_stride;   // output elements between the partial results of splits
     const int32_t *tile_e, *tile_start, *n_mtiles, *offsets;
     void *C;
     int ldc;
@@ -166,10 +170,14 @@ constexpr uint32_t idesc_bf16(int M, int N) {
 }
 
 struct TileCoord {
-    int e, m0, mend, n0;
+    int e, m0, mend, n0, split, kb0, kb1;
 };
 
-__device__ __forceinline__ TileCoord decode_tile(const Args &g, int L) {
+// Work item L -> (split, expert, M-tile, N-tile, K-block range).  Splits are
+// outermost so that the CTAs in flight work on the same K slice.
+__device__ __forceinline__ TileCoord decode_tile(const Args &g, int L, int tiles, int nk) {
+    const int split = L / tiles;
+    L -= split * tiles;
     const int gm = L / g.n_ntiles;
     const int e = g.tile_e[gm];
     const int st = g.tile_start[e];
@@ -181,6 +189,9 @@ __device__ __forceinline__ TileCoord decode_tile(const Args &g, int L) {
     c.m0 = g.offsets[e] + mt * BM;
     c.mend = g.offsets[e + 1];
     c.n0 = nt * (g.mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM);
+    c.split = split;
+    c.kb0 = split * g.kb_per_split;
+    c.kb1 = min(nk, c.kb0 + g.kb_per_split);
     return c;
 }
 
@@ -237,7 +248,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int total = (*g.n_mtiles) * g.n_ntiles;
+    const int tiles = (*g.n_mtiles) * g.n_ntiles;
+    const int total = tiles * g.k_splits;
     const int nk = (g.K + BK - 1) / BK;
 
     if (warp == 0 && lane == 0) {
@@ -247,17 +259,17 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t issued = 0;   // stages with a load in flight or unconsumed
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
-            const TileCoord c = decode_tile(g, L);
+            const TileCoord c = decode_tile(g, L, tiles, nk);
             int b0, b1;
             if (MODE == GEMM_UP_SWIGLU) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
             else { b0 = c.e * g.b_rows + c.n0; b1 = b0 + BNM / 2; }
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb = c.kb0; kb < c.kb1; ++kb) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
                 mbar_expect_tx(fb, STAGE_BYTES);
                 const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                 const uint32_t sb = sa + A_BYTES;
-                tma_load_2d(sa, &tmA, kb * BK, c.m0, fb);
+                tma_load_2d(sa, &tmA, (kb * BK) % g.a_k_period, c.m0, fb);
                 tma_load_2d(sb, &tmB0, kb * BK, b0, fb);
                 tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b1, fb);
                 issued |= 1u << stage;
@@ -283,10 +295,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+            // Only the K range is needed here; it depends on the split alone,
+            // so the issuing thread never waits on the tile table.
+            const int kb0 = (L / tiles) * g.kb_per_split;
+            const int kb1 = min(nk, kb0 + g.kb_per_split);
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
@@ -294,7 +310,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
-                           (kb | kk) != 0);
+                           (kb > kb0 || kk > 0) ? 1u : 0u);
                 tc_commit(empty0 + 8 * stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
@@ -313,7 +329,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int L = blockIdx.x; L < total; L += gridDim.x) {
-            const TileCoord c = decode_tile(g, L);
+            const TileCoord c = decode_tile(g, L, tiles, nk);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
             tc_fence_after();
             const int row = c.m0 + quarter * 32 + lane;
@@ -354,7 +370,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                 }
             } else {
-                float *O = static_cast<float *>(g.C);
+                float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
 #pragma unroll 1
                 for (int cc = 0; cc < BNM; cc += 16) {
                     float v[16];
@@ -433,17 +449,25 @@ static int num_sms() {
 
 }  // namespace tc
 
-// A [a_rows, K], weights B0/B1 [E*b_rows, K]; tile table from
-// launch_build_tiles with BM = 128.
-cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, const void *B0,
-                           const void *B1, int E, int b_rows, int N, int K,
-                           const int32_t *tile_e, const int32_t *tile_start,
-                           const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           cudaStream_t st) {
+// A [a_rows, a_cols], weights B0/B1 [E*b_rows, K]; tile table from
+// launch_build_tiles with BM = 128.  A's column for reduction index k is
+// k mod a_k_period (a_k_period = K: no wrap).  With k_splits > 1 (GEMM_DOWN
+// only) split s of every tile writes its partial sum to C + s * split_stride.
+cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, int a_cols, const void *B0,
+                           const void *B1, int E, int b_rows, int N, int K, int a_k_period,
+                           int k_splits, long long split_stride, const int32_t *tile_e,
+                           const int32_t *tile_start, const int32_t *n_mtiles,
+                           const int32_t *offsets, void *C, int ldc, cudaStream_t st) {
     using namespace tc;
     if (a_rows == 0) return cudaSuccess;
+    const int nk = (K + BK - 1) / BK;
+    if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN) ||
+        (a_k_period % BK != 0 && a_k_period != K))
+        return cudaErrorInvalidValue;
+    const int kbps = (nk + k_splits - 1) / k_splits;
+    k_splits = (nk + kbps - 1) / kbps;          // every split gets at least one K block
     CUtensorMap mA, mB0, mB1;
-    if (!make_map(&mA, A, a_rows, K, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mA, A, a_rows, a_cols, BM)) return cudaErrorInvalidValue;
     if (!make_map(&mB0, B0, (long long)E * b_rows, K, BNM / 2)) return cudaErrorInvalidValue;
     if (!make_map(&mB1, B1 ? B1 : B0, (long long)E * b_rows, K, BNM / 2))
         return cudaErrorInvalidValue;
@@ -451,9 +475,13 @@ cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, const void
     g.mode = mode;
     g.N = N;
     g.K = K;
+    g.a_k_period = a_k_period;
     g.n_ntiles = (N + (mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM) - 1) /
                  (mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM);
     g.b_rows = b_rows;
+    g.k_splits = k_splits;
+    g.kb_per_split = kbps;
+    g.split_stride = split_stride;
     g.tile_e = tile_e;
     g.tile_start = tile_start;
     g.n_mtiles = n_mtiles;

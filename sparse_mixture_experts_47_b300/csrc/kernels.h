@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <cuda_bf16.h>
 
 namespace moe {
 
@@ -21,6 +22,10 @@ struct RouterArgs {
 int router_blocks(int T, int E);
 size_t router_smem_bytes(int E, int dtype);
 cudaError_t launch_router(const RouterArgs &a, int dtype, cudaStream_t st);
+cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp,
+                                       __nv_bfloat16 *out, cudaStream_t st);
+cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, int S,
+                                      cudaStream_t st);
 cudaError_t launch_select_from_probsT(const float *probsT, const float *bias, int T, int E,
                                       int k, int32_t *idx, float *w, cudaStream_t st);
 cudaError_t launch_quantile_bias(const float *probsT, int T, int E, long long lo, float frac,
@@ -74,10 +79,10 @@ cudaError_t launch_simt_gemm(const GroupedGemmArgs &g, int mode, int dtype, cuda
 
 // gemm_tcgen05.cu: tcgen05/TMEM grouped GEMM for the bf16 workloads.
 constexpr int kTcBM = 128;
-cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, const void *B0,
-                           const void *B1, int E, int b_rows, int N, int K,
-                           const int32_t *tile_e, const int32_t *tile_start,
-                           const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           cudaStream_t st);
+cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, int a_cols, const void *B0,
+                           const void *B1, int E, int b_rows, int N, int K, int a_k_period,
+                           int k_splits, long long split_stride, const int32_t *tile_e,
+                           const int32_t *tile_start, const int32_t *n_mtiles,
+                           const int32_t *offsets, void *C, int ldc, cudaStream_t st);
 
 }  // namespace moe

@@ -13,18 +13,34 @@
 
 namespace moe {
 
-// p_e = (sum over blocks b, in order, of p_partial[b][e]) / T, summed in fp64.
-__global__ void p_finalize_kernel(const float *p_partial, int nblk, int E, int T, float *p) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
+// Fixed-order tree reduction of one double per thread over a 256-thread block;
+// the result is valid in thread 0.
+__device__ double block_sum_256(double v, double *red) {
+    red[threadIdx.x] = v;
+    __syncthreads();
+#pragma unroll
+    for (int off = 128; off >= 1; off >>= 1) {
+        if (threadIdx.x < off) red[threadIdx.x] += red[threadIdx.x + off];
+        __syncthreads();
+    }
+    return red[0];
+}
+
+// p_e = (sum over blocks b of p_partial[b][e]) / T in fp64: one CTA per expert,
+// thread i sums blocks i, i+256, ... in order, then a fixed tree.
+__global__ void __launch_bounds__(256) p_finalize_kernel(const float *p_partial, int nblk, int E,
+                                                         int T, float *p) {
+    __shared__ double red[256];
+    const int e = blockIdx.x;
     double s = 0.0;
-    for (int b = 0; b < nblk; ++b) s += (double)p_partial[(size_t)b * E + e];
-    p[e] = T > 0 ? (float)(s / (double)T) : 0.f;
+    for (int b = threadIdx.x; b < nblk; b += 256) s += (double)p_partial[(size_t)b * E + e];
+    s = block_sum_256(s, red);
+    if (threadIdx.x == 0) p[e] = T > 0 ? (float)(s / (double)T) : 0.f;
 }
 
 cudaError_t launch_p_finalize(const float *p_partial, int nblk, int E, int T, float *p,
                               cudaStream_t st) {
-    p_finalize_kernel<<<(E + 255) / 256, 256, 0, st>>>(p_partial, nblk, E, T, p);
+    p_finalize_kernel<<<E, 256, 0, st>>>(p_partial, nblk, E, T, p);
     note_launch();
     return cudaGetLastError();
 }
@@ -48,11 +64,12 @@ cudaError_t launch_prob_partials(const float *probs, int T, int E, float *p_part
     return cudaGetLastError();
 }
 
-// f_e = count_e / (T k); aux = E * sum_e f_e p_e (fp64 sum in expert order);
-// load = max_e count_e / (T k / E).
-__global__ void stats_finalize_kernel(const int32_t *counts, const float *p, int T, int E,
-                                      int k, float *f, float *p_out, float *aux,
-                                      float *load) {
+// f_e = count_e / (T k); aux = E * sum_e f_e p_e (fp64, fixed tree order);
+// load = max_e count_e / (T k / E).  One CTA of 1024 threads, E <= 1024.
+__global__ void __launch_bounds__(1024) stats_finalize_kernel(const int32_t *counts,
+                                                              const float *p, int T, int E,
+                                                              int k, float *f, float *p_out,
+                                                              float *aux, float *load) {
     __shared__ double red[1024];
     __shared__ int redmax[1024];
     const int e = threadIdx.x;
@@ -69,12 +86,17 @@ __global__ void stats_finalize_kernel(const int32_t *counts, const float *p, int
     red[e] = fp;
     redmax[e] = c;
     __syncthreads();
+#pragma unroll
+    for (int off = 512; off >= 1; off >>= 1) {
+        if (e < off) {
+            red[e] += red[e + off];
+            redmax[e] = max(redmax[e], redmax[e + off]);
+        }
+        __syncthreads();
+    }
     if (e == 0) {
-        double s = 0.0;
-        int mx = 0;
-        for (int i = 0; i < E; ++i) { s += red[i]; mx = max(mx, redmax[i]); }
-        if (aux) *aux = (float)((double)E * s);
-        if (load) *load = tk > 0 ? (float)((double)mx / (tk / (double)E)) : 0.f;
+        if (aux) *aux = (float)((double)E * red[0]);
+        if (load) *load = tk > 0 ? (float)((double)redmax[0] / (tk / (double)E)) : 0.f;
     }
 }
 

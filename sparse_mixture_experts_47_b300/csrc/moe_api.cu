@@ -16,6 +16,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -33,7 +34,8 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 struct Layout {
     size_t p_partial, probsT, hist, block_base, idx, w, counts, offsets, perm, inv, ndrop,
         pvec, sbias, idx_unb, tile_e, tile_m0, tile_start, ntiles, sh_offsets, sh_tile_e,
-        sh_tile_m0, sh_tile_start, sh_ntiles, xs, h, out_sorted, sh_h, sh_out, total;
+        sh_tile_m0, sh_tile_start, sh_ntiles, xs, h, out_sorted, sh_h, sh_out, rt_wsplit,
+        rt_logits, rt_offsets, rt_tile_e, rt_tile_start, rt_ntiles, total;
 };
 
 struct Sizes {
@@ -45,6 +47,29 @@ Sizes sizes(const moe_config *c) {
     s.T = c->T; s.d = c->d_model; s.E = c->n_experts; s.k = c->top_k; s.F = c->d_ff;
     s.Fs = c->d_ff_shared; s.Tk = s.T * s.k;
     return s;
+}
+
+// Router logits on the tensor cores (bf16 x, E > 32, E % 4 == 0): W_r split
+// into three bf16 parts over a 3*dp reduction.  The tensor core's fp32
+// accumulation loses a little with every step of a long chain (measured on
+// B300: logit error up to 1.3e-4 over one 192-block chain, 1e-5 over chains of
+// about 20 blocks, where the fp32 CUDA-core router reaches 1.4e-5), so the
+// reduction is cut into S chains of at most 16 K blocks, each written as an
+// fp32 partial plane and summed in fixed order by the softmax kernel.  Small T
+// uses more, shorter chains to fill the SMs.
+bool tc_router(const moe_config *c) {
+    return c->dtype == MOE_DTYPE_BF16 && c->n_experts > 32 && c->n_experts % 4 == 0;
+}
+long long router_dp(const moe_config *c) { return (c->d_model + 63) / 64 * 64; }
+constexpr int kRouterChainBlocks = 16;
+int router_splits(const moe_config *c) {
+    const long long tiles = ((long long)c->T + 127) / 128 * ((c->n_experts + 255) / 256);
+    const long long nk = 3 * router_dp(c) / 64;
+    long long S = (nk + kRouterChainBlocks - 1) / kRouterChainBlocks;
+    if (tiles > 0) S = std::max<long long>(S, std::min<long long>((296 + tiles - 1) / tiles,
+                                                                    std::max<long long>(1, nk / 4)));
+    const long long kbps = (nk + S - 1) / S;
+    return (int)((nk + kbps - 1) / kbps);
 }
 
 Layout layout(const moe_config *c) {
@@ -85,6 +110,13 @@ Layout layout(const moe_config *c) {
     L.out_sorted = take(sizeof(float) * s.Tk * s.d);
     L.sh_h = take(eb * s.T * s.Fs);
     L.sh_out = take(sizeof(float) * s.T * s.d);
+    const bool rt = tc_router(c);
+    L.rt_wsplit = take(rt ? 2 * s.E * 3 * router_dp(c) : 0);
+    L.rt_logits = take(rt ? sizeof(float) * router_splits(c) * s.T * s.E : 0);
+    L.rt_offsets = take(sizeof(int32_t) * 2);
+    L.rt_tile_e = take(sizeof(int32_t) * max_tiles(s.T, 1, kTcBM));
+    L.rt_tile_start = take(sizeof(int32_t) * 2);
+    L.rt_ntiles = take(sizeof(int32_t));
     L.total = o;
     return L;
 }
@@ -174,7 +206,25 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
     a.idx = idx; a.w = w; a.probs = probs;
     a.probsT = (c->quantile_balance || want_probsT) ? at<float>(ws, L.probsT) : nullptr;
     a.p_partial = at<float>(ws, L.p_partial);
-    MOE_CUDA(launch_router(a, c->dtype, st));
+    if (tc_router(c)) {
+        const int dp = (int)router_dp(c);
+        const int S = router_splits(c);
+        __nv_bfloat16 *wsplit = at<__nv_bfloat16>(ws, L.rt_wsplit);
+        float *part = at<float>(ws, L.rt_logits);
+        int32_t *off = at<int32_t>(ws, L.rt_offsets);
+        int32_t *te = at<int32_t>(ws, L.rt_tile_e), *ts = at<int32_t>(ws, L.rt_tile_start);
+        int32_t *nt = at<int32_t>(ws, L.rt_ntiles);
+        MOE_CUDA(launch_split_router_weight(w_r, a.E, a.d, dp, wsplit, st));
+        set_pair_kernel<<<1, 1, 0, st>>>(off, 0, a.T);
+        note_launch();
+        MOE_CUDA(cudaGetLastError());
+        MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
+        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E, 3 * dp, dp,
+                                S, s.T * s.E, te, ts, nt, off, part, a.E, st));
+        MOE_CUDA(launch_router_from_logits(a, part, S, st));
+    } else {
+        MOE_CUDA(launch_router(a, c->dtype, st));
+    }
     if (p_out && s.T > 0)
         MOE_CUDA(launch_p_finalize(a.p_partial, router_blocks(a.T, a.E), a.E, a.T, p_out, st));
     if (c->quantile_balance && s.T > 0) {
@@ -209,13 +259,14 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
                                     st));
         stage_end(MOE_STAGE_GATHER, ev, st);
         ev = stage_begin(st);
-        MOE_CUDA(launch_tc_gemm(up_mode, xs, s.Tk, w1, w3, (int)s.E, (int)s.F, (int)s.F,
-                                (int)s.d, tile_e, tile_start, ntiles, offsets, h, (int)s.F, st));
+        MOE_CUDA(launch_tc_gemm(up_mode, xs, s.Tk, (int)s.d, w1, w3, (int)s.E, (int)s.F,
+                                (int)s.F, (int)s.d, (int)s.d, 1, 0, tile_e, tile_start, ntiles,
+                                offsets, h, (int)s.F, st));
         stage_end(MOE_STAGE_UP, ev, st);
         ev = stage_begin(st);
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, h, s.Tk, w2, nullptr, (int)s.E, (int)s.d, (int)s.d,
-                                (int)s.F, tile_e, tile_start, ntiles, offsets, out_sorted,
-                                (int)s.d, st));
+        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, h, s.Tk, (int)s.F, w2, nullptr, (int)s.E, (int)s.d,
+                                (int)s.d, (int)s.F, (int)s.F, 1, 0, tile_e, tile_start, ntiles,
+                                offsets, out_sorted, (int)s.d, st));
         stage_end(MOE_STAGE_DOWN, ev, st);
         return MOE_OK;
     }
@@ -257,10 +308,12 @@ int run_shared(const moe_config *c, const void *x, const void *ws1, const void *
     float *o = at<float>(ws, L.sh_out);
     if (c->dtype == MOE_DTYPE_BF16) {
         MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_UP_SWIGLU, x, s.T, ws1, ws3, 1, (int)s.Fs, (int)s.Fs,
-                                (int)s.d, te, ts, nt, off, h, (int)s.Fs, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, h, s.T, ws2, nullptr, 1, (int)s.d, (int)s.d,
-                                (int)s.Fs, te, ts, nt, off, o, (int)s.d, st));
+        MOE_CUDA(launch_tc_gemm(GEMM_UP_SWIGLU, x, s.T, (int)s.d, ws1, ws3, 1, (int)s.Fs,
+                                (int)s.Fs, (int)s.d, (int)s.d, 1, 0, te, ts, nt, off, h,
+                                (int)s.Fs, st));
+        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, h, s.T, (int)s.Fs, ws2, nullptr, 1, (int)s.d,
+                                (int)s.d, (int)s.Fs, (int)s.Fs, 1, 0, te, ts, nt, off, o,
+                                (int)s.d, st));
         return MOE_OK;
     }
     MOE_CUDA(launch_build_tiles(off, 1, kSimtBM, te, tm, nullptr, nt, st));

@@ -18,6 +18,8 @@
 
 #include <math_constants.h>
 
+#include <algorithm>
+
 namespace moe {
 
 // --------------------------------------------------------------------------
@@ -190,68 +192,13 @@ __device__ __forceinline__ void load4_f32(const __nv_bfloat16 *p, float *v) {
     v[2] = __uint_as_float(a.y << 16); v[3] = __uint_as_float(a.y & 0xffff0000u);
 }
 
-template <typename TX>
-__global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
-    extern __shared__ __align__(16) float smem[];
-    const int E = a.E, d = a.d;
-    float *lg = smem;                         // [kTB][E]
-    float *xs = lg + kTB * E;                 // [kDK][kTB]
-    float *wsh = xs + kDK * kTB;              // [kDK][kEC + 4]
-    float *st_m = wsh + kDK * (kEC + 4);      // [kTB]
-    float *st_s = st_m + kTB;                 // [kTB]
-
+// Softmax, load-statistics partial sums, optional probs/probsT and top-k with
+// renormalisation for a tile of kTB tokens whose logits (logit offset included)
+// are in shared memory lg[kTB][E].  256 threads; warp w owns tokens 4w..4w+3.
+__device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m, float *st_s,
+                                     int t0) {
+    const int E = a.E;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = blockIdx.x * kTB;
-    const TX *x = static_cast<const TX *>(a.x);
-
-    for (int e0 = 0; e0 < E; e0 += kEC) {
-        float acc[4][4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[r][i] = 0.f;
-        for (int k0 = 0; k0 < d; k0 += kDK) {
-            __syncthreads();
-            {
-                const int tt = tid >> 3, kk = (tid & 7) * 4, t = t0 + tt;
-                float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (t < a.T && k0 + kk < d) load4_f32(x + (size_t)t * d + k0 + kk, v);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) xs[(kk + i) * kTB + tt] = v[i];
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int id = tid + q * 256, ee = id >> 3, kk = (id & 7) * 4, e = e0 + ee;
-                float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (e < E && k0 + kk < d) load4_f32(a.w_r + (size_t)e * d + k0 + kk, v);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) wsh[(kk + i) * (kEC + 4) + ee] = v[i];
-            }
-            __syncthreads();
-#pragma unroll 8
-            for (int kk = 0; kk < kDK; ++kk) {
-                const float4 xv = *reinterpret_cast<const float4 *>(xs + kk * kTB + 4 * warp);
-                const float xr[4] = {xv.x, xv.y, xv.z, xv.w};
-                float wv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) wv[i] = wsh[kk * (kEC + 4) + lane + 32 * i];
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[r][i] = fmaf(xr[r], wv[i], acc[r][i]);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = e0 + lane + 32 * i;
-            if (e < E) {
-                const float lb = a.logit_bias ? a.logit_bias[e] : 0.f;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) lg[(4 * warp + r) * E + e] = acc[r][i] + lb;
-            }
-        }
-    }
-    __syncthreads();
 
     // Softmax statistics per token (warp per 4 tokens), optional probs rows.
     for (int r = 0; r < 4; ++r) {
@@ -321,6 +268,122 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
             a.w[(size_t)t * a.k + lane] = my_p / psum;
         }
     }
+}
+
+template <typename TX>
+__global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    const int E = a.E, d = a.d;
+    float *lg = smem;                         // [kTB][E]
+    float *xs = lg + kTB * E;                 // [kDK][kTB]
+    float *wsh = xs + kDK * kTB;              // [kDK][kEC + 4]
+    float *st_m = wsh + kDK * (kEC + 4);      // [kTB]
+    float *st_s = st_m + kTB;                 // [kTB]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * kTB;
+    const TX *x = static_cast<const TX *>(a.x);
+
+    for (int e0 = 0; e0 < E; e0 += kEC) {
+        float acc[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[r][i] = 0.f;
+        for (int k0 = 0; k0 < d; k0 += kDK) {
+            __syncthreads();
+            {
+                const int tt = tid >> 3, kk = (tid & 7) * 4, t = t0 + tt;
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (t < a.T && k0 + kk < d) load4_f32(x + (size_t)t * d + k0 + kk, v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xs[(kk + i) * kTB + tt] = v[i];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int id = tid + q * 256, ee = id >> 3, kk = (id & 7) * 4, e = e0 + ee;
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (e < E && k0 + kk < d) load4_f32(a.w_r + (size_t)e * d + k0 + kk, v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) wsh[(kk + i) * (kEC + 4) + ee] = v[i];
+            }
+            __syncthreads();
+#pragma unroll 8
+            for (int kk = 0; kk < kDK; ++kk) {
+                const float4 xv = *reinterpret_cast<const float4 *>(xs + kk * kTB + 4 * warp);
+                const float xr[4] = {xv.x, xv.y, xv.z, xv.w};
+                float wv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) wv[i] = wsh[kk * (kEC + 4) + lane + 32 * i];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[r][i] = fmaf(xr[r], wv[i], acc[r][i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = e0 + lane + 32 * i;
+            if (e < E) {
+                const float lb = a.logit_bias ? a.logit_bias[e] : 0.f;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) lg[(4 * warp + r) * E + e] = acc[r][i] + lb;
+            }
+        }
+    }
+    __syncthreads();
+    router_rows_epilogue(a, lg, st_m, st_s, t0);
+}
+
+// --------------------------------------------------------------------------
+// Tensor-core router support.  W_r (fp32) is split exactly into three bf16
+// parts, w = hi + mid + lo (8 + 8 + 8 significant bits, residual at most
+// 2^-24 |w|), laid out as one [E, 3*dp] bf16 matrix (dp = d rounded up to 64,
+// zero padded), so that x W_r^T = x [hi|mid|lo]^T over a 3*dp reduction with
+// x's column taken mod dp.  bf16 x bf16 products are exact in fp32.
+// --------------------------------------------------------------------------
+__global__ void split_router_weight_kernel(const float *w_r, int E, int d, int dp,
+                                           __nv_bfloat16 *out) {
+    const long long n = (long long)E * dp;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int e = (int)(i / dp), c = (int)(i % dp);
+        const float w = c < d ? w_r[(size_t)e * d + c] : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+        __nv_bfloat16 *row = out + (size_t)e * 3 * dp;
+        row[c] = hi;
+        row[dp + c] = mid;
+        row[2 * dp + c] = lo;
+    }
+}
+
+// Logits = sum of S partial products (fixed order) + logit offset, then the
+// same per-token epilogue as the SIMT router.
+__global__ void __launch_bounds__(256) router_from_logits_kernel(RouterArgs a,
+                                                                 const float *part, int S) {
+    extern __shared__ __align__(16) float smem[];
+    const int E = a.E;
+    float *lg = smem;
+    float *st_m = lg + kTB * E;
+    float *st_s = st_m + kTB;
+    const int t0 = blockIdx.x * kTB;
+    const size_t plane = (size_t)a.T * E;
+    for (int i = threadIdx.x; i < kTB * E; i += blockDim.x) {
+        const int tt = i / E, e = i - tt * E, t = t0 + tt;
+        float v = 0.f;
+        if (t < a.T) {
+            const size_t o = (size_t)t * E + e;
+            for (int sp = 0; sp < S; ++sp) v += part[sp * plane + o];
+            if (a.logit_bias) v += a.logit_bias[e];
+        }
+        lg[i] = v;
+    }
+    __syncthreads();
+    router_rows_epilogue(a, lg, st_m, st_s, t0);
 }
 
 // --------------------------------------------------------------------------
@@ -476,6 +539,27 @@ cudaError_t launch_router(const RouterArgs &a, int dtype, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     return dtype == MOE_DTYPE_FP32 ? launch_router_t<float>(a, st)
                                    : launch_router_t<__nv_bfloat16>(a, st);
+}
+
+cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp,
+                                       __nv_bfloat16 *out, cudaStream_t st) {
+    const long long n = (long long)E * dp;
+    const int grid = (int)std::min<long long>((n + 255) / 256, 148 * 8);
+    split_router_weight_kernel<<<grid, 256, 0, st>>>(w_r, E, d, dp, out);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, int S,
+                                      cudaStream_t st) {
+    if (a.T == 0) return cudaSuccess;
+    const size_t smem = sizeof(float) * ((size_t)kTB * a.E + 2 * kTB);
+    cudaError_t err = cudaFuncSetAttribute(router_from_logits_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    router_from_logits_kernel<<<(a.T + kTB - 1) / kTB, 256, smem, st>>>(a, part, S);
+    note_launch();
+    return cudaGetLastError();
 }
 
 cudaError_t launch_select_from_probsT(const float *probsT, const float *bias, int T, int E,
