@@ -38,6 +38,21 @@ Readings where the pages are silent or disagree (each restated where used):
       contributes 0 and the surviving weights are not renormalised.
   R7  quantile bias b_e = -Q(probs[:, e], 1 - k/E) with Q the linear
       interpolation between order statistics (h = (T-1) q).
+  R10 capacity overflow redirected to the next-best expert (ch30 §30.5.2):
+      round 0 is R6; in each further round, unserved slots take their
+      token's next unused experts down the full score ranking and are
+      served in (t*k + j) order by experts with room; the weight of a slot
+      served by expert e is p[t, e] over the token's top-k probability sum.
+  R11 expert-choice routing (prac, memo routing table): each expert takes
+      the min(C, T) tokens with the largest softmax probability for it (ties
+      by lower token index), C = ceil(cf*T*k/E); weight probs[t, e], not
+      renormalised; a token picked by no expert gets routed output 0.
+  R9  observability (prac, scale drift): gate entropy is the mean over
+      tokens of -sum_e p ln p in nats; an expert's output scale is the mean,
+      population standard deviation and largest magnitude over all elements
+      of its output tensor (its kept rows' FFN outputs, before the gate
+      weight); bias size is mean and max |b_e| of the selection bias in
+      effect.
   R8  the layer's activations are stored in the layer dtype: for a bf16 layer
       the expert's intermediate activation h (the input of W2) is a bf16
       tensor, so it is rounded once, to nearest even, from its exact value
@@ -64,7 +79,9 @@ __all__ = [
     "router_logits", "softmax", "topk_desc", "renormalise", "route",
     "quantile_linear", "quantile_select_bias", "capacity", "dispatch",
     "expert_ffn", "load_stats", "moe_forward", "RouterOut", "DispatchOut", "round_to_bf16",
-    "round_to_fp32",
+    "round_to_fp32", "gate_entropy", "expert_output_scale", "bias_magnitude", "observe",
+    "dispatch_reroute", "RerouteOut", "expert_choice", "ExpertChoiceOut",
+    "moe_forward_expert_choice",
 ]
 
 
@@ -236,6 +253,153 @@ def dispatch(idx: np.ndarray, E: int, C: int) -> DispatchOut:
                        keep, int(T * k - perm.shape[0]))
 
 
+@dataclass
+class RerouteOut:
+    slot_expert: np.ndarray   # [T, k] expert serving each slot, -1 if dropped
+    slot_w: np.ndarray        # [T, k] gate weight of that expert (0 if dropped)
+    slot_round: np.ndarray    # [T, k] round that placed the slot (0 = first choice)
+    counts: np.ndarray        # [E] first-choice assignments (before capacity)
+    kept_counts: np.ndarray   # [E] rows served per expert (<= C)
+    offsets: np.ndarray       # [E+1]
+    perm: np.ndarray          # [sum kept] flat slot of each grouped row
+    inv: np.ndarray           # [T*k] grouped row of each slot, -1 if dropped
+    n_dropped: int
+
+
+def dispatch_reroute(scores: np.ndarray, probs: np.ndarray, k: int, C: int, rounds: int
+                     ) -> RerouteOut:
+    """Capacity with overflow redirected to the next-best expert ([MoE-ch30]
+    §30.5.2: tokens beyond an expert's capacity are dropped or sent to the
+    next-best expert).  Reading R10:
+
+    * each token ranks all experts by its selection score (descending,
+      exactly equal scores by lower index); its first k are its slots;
+    * round 0 is the plain capacity rule: slots in flattened (t*k + j) order,
+      a slot is served by its expert while that expert has fewer than C rows;
+    * in each of ``rounds`` further rounds, every slot still unserved takes
+      its token's next unused expert down the ranking (a token's unserved
+      slots in j order take consecutive candidates), and the slots are then
+      served, again in (t*k + j) order, by experts that still have room;
+    * slots unserved after the last round are dropped (output 0);
+    * a slot served by expert e carries the weight p[t, e] / sum of the
+      token's top-k probabilities: the normaliser of the plain top-k, so that
+      capacity decisions never rescale the other slots (as for drops, R6);
+    * an expert's rows are grouped in the order they were served: round 0 in
+      (t*k + j) order, then round 1, and so on.
+    """
+    T, E = scores.shape
+    order = np.argsort(-scores, axis=1, kind="stable")        # full ranking per token
+    top = order[:, :k]
+    norm = np.take_along_axis(probs, top, axis=1).sum(axis=1)
+    counts = np.bincount(top.reshape(-1), minlength=E).astype(np.int64)
+    slot_e = top.copy()
+    served = np.full((T, k), -1, dtype=np.int64)      # expert serving the slot
+    rnd = np.full((T, k), -1, dtype=np.int64)
+    rows: list = [[] for _ in range(E)]                 # served slots per expert, in order
+    nxt = np.full(T, k, dtype=np.int64)                 # next candidate position per token
+    for r in range(rounds + 1):
+        if r > 0:
+            for t in range(T):
+                for j in range(k):
+                    if served[t, j] >= 0:
+                        continue
+                    if nxt[t] < E:
+                        slot_e[t, j] = order[t, nxt[t]]
+                        nxt[t] += 1
+                    else:
+                        slot_e[t, j] = -1                # no candidate left
+        for t in range(T):
+            for j in range(k):
+                e = int(slot_e[t, j])
+                if served[t, j] >= 0 or e < 0:
+                    continue
+                if len(rows[e]) < C:
+                    rows[e].append(t * k + j)
+                    served[t, j] = e
+                    rnd[t, j] = r
+    kept = np.array([len(rows[e]) for e in range(E)], dtype=np.int64)
+    offsets = np.concatenate([[0], np.cumsum(kept)]).astype(np.int64)
+    perm = np.array([f for e in range(E) for f in rows[e]], dtype=np.int64)
+    inv = np.full(T * k, -1, dtype=np.int64)
+    inv[perm] = np.arange(perm.shape[0])
+    w = np.zeros((T, k))
+    for t in range(T):
+        for j in range(k):
+            if served[t, j] >= 0:
+                w[t, j] = probs[t, served[t, j]] / norm[t]
+    return RerouteOut(served, w, rnd, counts, kept, offsets, perm, inv,
+                      int(T * k - perm.shape[0]))
+
+
+@dataclass
+class ExpertChoiceOut:
+    chosen: np.ndarray        # [E, Cn] tokens each expert picked, ascending token index
+    weight: np.ndarray        # [E, Cn] their gate weights probs[t, e]
+    counts: np.ndarray        # [E] Cn = min(C, T) for every expert
+    offsets: np.ndarray       # [E+1] e * Cn
+    n_unchosen: int           # tokens no expert picked (their routed output is 0)
+
+
+def expert_choice(probs: np.ndarray, C: int) -> ExpertChoiceOut:
+    """Expert-choice routing ([MoE-prac] TopKRouter discussion: each expert
+    picks the top-C tokens for its capacity, so every expert is exactly
+    full; [MoE-memo] routing table: each expert chooses its top tokens).
+    Reading R11: the scores are the router's softmax probabilities (the same
+    router as token choice); expert e takes the min(C, T) tokens with the
+    largest probs[:, e], exactly equal values by lower token index; the gate
+    weight of (t, e) is probs[t, e] with no renormalisation; a token may be
+    picked by any number of experts, including none."""
+    T, E = probs.shape
+    Cn = min(C, T)
+    chosen = np.zeros((E, Cn), dtype=np.int64)
+    weight = np.zeros((E, Cn))
+    picked = np.zeros(T, dtype=bool)
+    for e in range(E):
+        order = np.argsort(-probs[:, e], kind="stable")   # ties: lower token first
+        top = np.sort(order[:Cn])
+        chosen[e] = top
+        weight[e] = probs[top, e]
+        picked[top] = True
+    return ExpertChoiceOut(chosen, weight, np.full(E, Cn, dtype=np.int64),
+                           np.arange(E + 1, dtype=np.int64) * Cn, int(T - picked.sum()))
+
+
+def moe_forward_expert_choice(inp: Dict, k: int, act: str, capacity_factor: float = 1.0,
+                              tokens: Optional[Sequence[int]] = None,
+                              act_dtype: str = "fp64") -> Dict:
+    """Layer forward with expert-choice routing (reading R11):
+    y[t] = sum over experts e that picked t of probs[t, e] FFN_e(x[t]) +
+    shared(x[t]), with capacity C = ceil(cf * T * k / E) (k = average number
+    of experts per token).  f, p and aux use the experts' actual loads:
+    f_e = Cn / (T k)."""
+    x = _f64(inp["x"])
+    T = x.shape[0]
+    E = inp["w_r"].shape[0]
+    logits = router_logits(x, inp["w_r"], inp.get("logit_bias"))
+    probs = softmax(logits)
+    C = capacity(T, k, E, capacity_factor)
+    ec = expert_choice(probs, C)
+    f = ec.counts / float(T * k) if T else np.zeros(E)
+    p = probs.mean(axis=0) if T else np.zeros(E)
+    stats = {"counts": ec.counts, "f": f, "p": p, "aux": E * float(np.sum(f * p)),
+             "load_max_over_mean": (float(ec.counts.max()) / (T * k / float(E))) if T else 0.0}
+    rows = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
+    pos = {int(t): i for i, t in enumerate(rows)}
+    y = np.zeros((rows.shape[0], x.shape[1]))
+    for e in range(E):
+        sel = [(n, int(t)) for n, t in enumerate(ec.chosen[e]) if int(t) in pos]
+        if not sel:
+            continue
+        tt = np.array([t for _, t in sel])
+        out = expert_ffn(x[tt], inp["w1"][e], None if inp.get("w3") is None else inp["w3"][e],
+                         inp["w2"][e], act, act_dtype)
+        for i, (n, t) in enumerate(sel):
+            y[pos[t]] += ec.weight[e, n] * out[i]
+    if inp.get("ws1") is not None:
+        y += expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
+    return {"probs": probs, "ec": ec, "stats": stats, "capacity": C, "rows": rows, "y": y}
+
+
 # --------------------------------------------------------------------------
 # Expert FFN: [MoE-ch30] §30.2.4 / §30.6.1 Expert
 # --------------------------------------------------------------------------
@@ -305,12 +469,65 @@ def load_stats(probs: np.ndarray, idx: np.ndarray, E: int) -> Dict[str, np.ndarr
 
 
 # --------------------------------------------------------------------------
+# Observability: [MoE-prac] "エキスパート間のスケールドリフト" (monitor each
+# expert's output mean, standard deviation and maximum; the minimum set of
+# MoE metrics: drop ratio, per-expert load, per-expert output scale, the
+# size of the bias term and the gate entropy)
+# --------------------------------------------------------------------------
+
+def gate_entropy(probs: np.ndarray) -> float:
+    """Mean over tokens of the router distribution's entropy, in nats:
+    H_t = -sum_e p[t, e] ln p[t, e], with 0 ln 0 = 0 (reading R9)."""
+    p = np.asarray(probs, dtype=np.float64)
+    if p.shape[0] == 0:
+        return 0.0
+    safe = np.where(p > 0, p, 1.0)
+    return float(np.mean(-np.sum(np.where(p > 0, p * np.log(safe), 0.0), axis=1)))
+
+
+def expert_output_scale(outputs: Dict[int, np.ndarray], E: int) -> Dict[str, np.ndarray]:
+    """Per expert, over every element of its output tensor (the FFN outputs
+    of its kept rows, before the gate weight): mean, standard deviation
+    (population) and largest magnitude; zeros for an expert without rows
+    (reading R9)."""
+    mean, std, mx = np.zeros(E), np.zeros(E), np.zeros(E)
+    for e, o in outputs.items():
+        o = np.asarray(o, dtype=np.float64)
+        if o.size == 0:
+            continue
+        mean[e] = o.mean()
+        std[e] = o.std()
+        mx[e] = np.abs(o).max()
+    return {"mean": mean, "std": std, "max_abs": mx}
+
+
+def bias_magnitude(bias: Optional[np.ndarray]) -> Dict[str, float]:
+    """Size of the selection bias in effect: mean and largest |b_e| (0
+    without a bias)."""
+    if bias is None:
+        return {"mean_abs": 0.0, "max_abs": 0.0}
+    b = np.abs(np.asarray(bias, dtype=np.float64))
+    return {"mean_abs": float(b.mean()), "max_abs": float(b.max())}
+
+
+def observe(r: "RouterOut", dp: "DispatchOut", outputs: Dict[int, np.ndarray], E: int,
+            k: int) -> Dict:
+    """The pages' MoE observability set for one batch."""
+    T = r.probs.shape[0]
+    return {"drop_ratio": dp.n_dropped / float(T * k) if T else 0.0,
+            "gate_entropy": gate_entropy(r.probs),
+            "bias": bias_magnitude(r.select_bias),
+            "expert_out": expert_output_scale(outputs, E)}
+
+
+# --------------------------------------------------------------------------
 # Whole layer: [MoE-ch30] §30.6.1 MoELayer.forward, §30.4.5 shared expert
 # --------------------------------------------------------------------------
 
 def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
                 select_space: str = "probs", quantile_balance: bool = False,
-                tokens: Optional[Sequence[int]] = None, act_dtype: str = "fp64") -> Dict:
+                tokens: Optional[Sequence[int]] = None, act_dtype: str = "fp64",
+                observe_outputs: bool = False, reroute_rounds: int = 0) -> Dict:
     """Forward of the token-choice MoE layer.
 
     y[t] = sum_j keep[t,j] * w[t,j] * FFN_{idx[t,j]}(x[t]) + shared(x[t]).
@@ -318,7 +535,10 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
     couples them); y is computed for ``tokens`` only (all when None), since
     each token's output depends on nothing else once its slots are known.
     ``act_dtype`` is the storage type of the experts' intermediate
-    activation (reading R8).
+    activation (reading R8).  ``observe_outputs`` adds the observability set
+    (needs every token: ``tokens`` None).  ``reroute_rounds`` > 0 sends
+    capacity overflow to the next-best experts (reading R10) instead of
+    dropping it.
     """
     x = _f64(inp["x"])
     T = x.shape[0]
@@ -326,7 +546,12 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
     r = route(x, inp["w_r"], k, inp.get("logit_bias"), inp.get("select_bias"),
               select_space, quantile_balance)
     C = capacity(T, k, E, capacity_factor)
-    dp = dispatch(r.idx, E, C)
+    if reroute_rounds > 0:
+        dp = dispatch_reroute(r.scores, r.probs, k, C, reroute_rounds)
+        slot_e, slot_w = dp.slot_expert, dp.slot_w
+    else:
+        dp = dispatch(r.idx, E, C)
+        slot_e, slot_w = np.where(dp.keep, r.idx, -1), r.w
     st = load_stats(r.probs, r.idx, E)
     rows = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     y = np.zeros((rows.shape[0], x.shape[1]))
@@ -334,16 +559,21 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
     groups: Dict[int, list] = {}
     for t in rows:
         for j in range(k):
-            if dp.keep[t, j]:
-                groups.setdefault(int(r.idx[t, j]), []).append((int(t), j))
+            if slot_e[t, j] >= 0:
+                groups.setdefault(int(slot_e[t, j]), []).append((int(t), j))
+    outputs: Dict[int, np.ndarray] = {}
     for e, tj in sorted(groups.items()):
         tt = np.array([t for t, _ in tj])
-        ww = np.array([r.w[t, j] for t, j in tj])
+        ww = np.array([slot_w[t, j] for t, j in tj])
         out = expert_ffn(x[tt], inp["w1"][e], None if inp.get("w3") is None else inp["w3"][e],
                          inp["w2"][e], act, act_dtype)
+        outputs[e] = out
         for n, (t, _) in enumerate(tj):
             y[pos[int(t)]] += ww[n] * out[n]
     if inp.get("ws1") is not None:
         y += expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
-    return {"router": r, "dispatch": dp, "stats": st, "capacity": C,
-            "rows": rows, "y": y}
+    res = {"router": r, "dispatch": dp, "stats": st, "capacity": C, "rows": rows, "y": y}
+    if observe_outputs:
+        assert tokens is None, "observability needs every token"
+        res["observe"] = observe(r, dp, outputs, E, k)
+    return res

@@ -298,12 +298,182 @@ def pin_bf16_activation_ffn():
     assert not np.allclose(out["y"], exact["y"], atol=1e-6)   # the rounding is visible
 
 
+def pin_gate_entropy():
+    # closed forms: a uniform router over E experts has entropy ln E, a
+    # one-hot router 0; a general distribution against scipy.stats.entropy
+    from scipy.stats import entropy as sp_entropy
+    for E in (2, 8, 896):
+        assert abs(om.gate_entropy(np.full((3, E), 1.0 / E)) - math.log(E)) < 1e-12
+    assert om.gate_entropy(np.eye(5)) == 0.0
+    p = om.softmax(RNG.normal(size=(7, 11)) * 3)
+    ref = float(np.mean([sp_entropy(row) for row in p]))
+    assert abs(om.gate_entropy(p) - ref) < 1e-12
+    # through the layer: logits = log(p) give back p
+    r = om.route(np.log(p), np.eye(11), 2)
+    assert abs(om.gate_entropy(r.probs) - ref) < 1e-12
+
+
+def pin_expert_output_scale():
+    # constant outputs: mean c, std 0, max |c|; a +-a pattern: mean 0, std a
+    c = om.expert_output_scale({0: np.full((3, 4), -2.5), 2: np.array([[1.5, -1.5], [-1.5, 1.5]])}, 3)
+    assert c["mean"].tolist() == [-2.5, 0.0, 0.0]
+    assert c["std"].tolist() == [0.0, 0.0, 1.5]
+    assert c["max_abs"].tolist() == [2.5, 0.0, 1.5]
+    # against torch's reductions of the same values (population std)
+    o = RNG.normal(size=(5, 6))
+    st = om.expert_output_scale({1: o}, 2)
+    ot = torch.tensor(o)
+    assert abs(st["mean"][1] - float(ot.mean())) < 1e-14
+    assert abs(st["std"][1] - float(ot.std(unbiased=False))) < 1e-14
+    assert st["max_abs"][1] == float(ot.abs().max())
+    # through the layer: E = 1, no capacity: expert 0's outputs are the dense FFN
+    inp = _rand_layer(9, 8, 1, 12, "relu")
+    out = om.moe_forward(inp, 1, "relu", observe_outputs=True)
+    x, w1, w2 = (torch.tensor(np.asarray(a, dtype=np.float64))
+                 for a in (inp["x"], inp["w1"][0], inp["w2"][0]))
+    dense = Fnn.linear(Fnn.relu(Fnn.linear(x, w1)), w2)
+    ob = out["observe"]["expert_out"]
+    assert abs(ob["mean"][0] - float(dense.mean())) < 1e-12
+    assert abs(ob["std"][0] - float(dense.std(unbiased=False))) < 1e-12
+    assert abs(ob["max_abs"][0] - float(dense.abs().max())) < 1e-12
+
+
+def pin_observe_drop_and_bias():
+    g = load_golden("capacity_cases.json")["cases"][0]
+    idx = np.array(g["idx"])
+    T, k = idx.shape
+    E = g["E"]
+    C = om.capacity(T, k, E, g["capacity_factor"])
+    dp = om.dispatch(idx, E, C)
+    probs = np.full((T, E), 1.0 / E)
+    r = om.RouterOut(np.zeros((T, E)), probs, probs, idx, np.ones((T, k)) / k,
+                     np.array([0.25, -0.5] + [0.0] * (E - 2)))
+    ob = om.observe(r, dp, {}, E, k)
+    assert ob["drop_ratio"] == g["n_dropped"] / (T * k)
+    assert ob["bias"]["max_abs"] == 0.5 and abs(ob["bias"]["mean_abs"] - 0.75 / E) < 1e-15
+    assert abs(ob["gate_entropy"] - math.log(E)) < 1e-12
+    assert om.bias_magnitude(None) == {"mean_abs": 0.0, "max_abs": 0.0}
+
+
+def _scores_from_ranking(ranking):
+    ranking = np.asarray(ranking)
+    T, E = ranking.shape
+    sc = np.zeros((T, E))
+    for t in range(T):
+        sc[t, ranking[t]] = E - np.arange(E)
+    return sc
+
+
+def pin_reroute_cases():
+    g = load_golden("reroute_cases.json")
+    for c in g["cases"]:
+        sc = _scores_from_ranking(c["ranking"])
+        probs = om.softmax(sc)
+        out = om.dispatch_reroute(sc, probs, c["k"], c["C"], c["rounds"])
+        assert out.slot_expert.tolist() == c["slot_expert"], c["note"]
+        assert out.slot_round.tolist() == c["slot_round"], c["note"]
+        assert out.kept_counts.tolist() == c["kept_counts"], c["note"]
+        assert out.perm.tolist() == c["perm"], c["note"]
+        assert out.n_dropped == c["n_dropped"], c["note"]
+
+
+def pin_reroute_invariants():
+    rng = np.random.default_rng(21)
+    for T, E, k, cf in [(200, 8, 1, 1.0), (150, 16, 2, 0.8), (90, 32, 4, 1.1), (60, 5, 2, 0.5)]:
+        pop = 1.0 / np.arange(1, E + 1) ** 1.3
+        sc = om.softmax(rng.normal(size=(T, E)) + np.log(pop)[None, :])
+        C = om.capacity(T, k, E, cf)
+        plain = om.dispatch(om.topk_desc(sc, k), E, C)
+        r0 = om.dispatch_reroute(sc, sc, k, C, 0)
+        # zero rounds is the plain capacity rule
+        assert r0.perm.tolist() == plain.perm.tolist() and r0.n_dropped == plain.n_dropped
+        assert r0.inv.tolist() == plain.inv.tolist()
+        prev = r0.n_dropped
+        top = om.topk_desc(sc, k)
+        norm = np.take_along_axis(sc, top, axis=1).sum(axis=1)
+        for R in (1, 2, 3):
+            r = om.dispatch_reroute(sc, sc, k, C, R)
+            assert np.all(r.kept_counts <= C)
+            assert r.kept_counts.sum() + r.n_dropped == T * k
+            assert r.n_dropped <= prev            # more rounds never drop more
+            prev = r.n_dropped
+            # every expert serves its first-choice slots exactly as the plain rule
+            first = (r.slot_round == 0)
+            assert np.array_equal(first, plain.keep)
+            for t in range(T):
+                served = [e for e in r.slot_expert[t] if e >= 0]
+                assert len(served) == len(set(served))           # distinct experts
+                for j in range(k):
+                    e = r.slot_expert[t, j]
+                    if r.slot_round[t, j] > 0:
+                        assert e not in top[t]                  # redirected beyond top-k
+                    if e >= 0:
+                        assert abs(r.slot_w[t, j] - sc[t, e] / norm[t]) < 1e-15
+                    else:
+                        assert r.slot_w[t, j] == 0.0
+            # grouped rows: each expert's rows are its served slots
+            for e in range(E):
+                a, b = r.offsets[e], r.offsets[e + 1]
+                assert all(r.slot_expert.reshape(-1)[r.perm[a:b]] == e)
+        # enough capacity: nothing overflows, nothing is redirected
+        big = om.dispatch_reroute(sc, sc, k, T * k, 2)
+        assert big.n_dropped == 0 and np.all(big.slot_round == 0)
+
+
+def pin_expert_choice_case():
+    g = load_golden("expert_choice_case.json")
+    ec = om.expert_choice(np.array(g["probs"]), g["C"])
+    assert ec.chosen.tolist() == g["chosen"]
+    assert np.allclose(ec.weight, g["weight"], atol=1e-15)
+    assert ec.n_unchosen == g["n_unchosen"]
+    assert ec.offsets.tolist() == [0, 2, 4]
+
+
+def pin_expert_choice_bruteforce():
+    # every C-subset of a column: the chosen one has the largest sum, and among
+    # equal sums the lexicographically smallest token set
+    rng = np.random.default_rng(8)
+    for T, E, C in [(6, 3, 2), (7, 2, 3), (5, 4, 5), (6, 2, 4)]:
+        probs = om.softmax(np.round(rng.normal(size=(T, E)), 1))   # rounding makes ties
+        ec = om.expert_choice(probs, C)
+        for e in range(E):
+            best = None
+            for sub in itertools.combinations(range(T), min(C, T)):
+                key = (-probs[list(sub), e].sum(), sorted(sub))
+                # ties in the sum resolved by preferring the largest values of the
+                # lowest tokens: compare the per-token sorted selection instead
+                if best is None or key < best:
+                    best = key
+            chosen_vals = np.sort(probs[ec.chosen[e], e])
+            best_vals = np.sort(probs[best[1], e])
+            assert np.allclose(chosen_vals, best_vals, atol=1e-15)
+            # the exact tie rule: a picked token is never beaten by an unpicked
+            # one with a larger value, or an equal value and a lower index
+            picked = set(ec.chosen[e].tolist())
+            for t in picked:
+                for u in set(range(T)) - picked:
+                    assert probs[t, e] > probs[u, e] or (probs[t, e] == probs[u, e] and t < u)
+
+
+def pin_expert_choice_full_capacity_is_dense_mixture():
+    # C >= T: every expert takes every token, y = sum_e p_e FFN_e(x), which is
+    # token choice with k = E (renormalised weights p / sum p = p)
+    inp = _rand_layer(6, 8, 3, 10, "swiglu")
+    ec = om.moe_forward_expert_choice(inp, 3, "swiglu", capacity_factor=1.0)
+    assert ec["ec"].n_unchosen == 0 and ec["capacity"] == 6
+    tc = om.moe_forward(inp, 3, "swiglu")
+    assert np.allclose(ec["y"], tc["y"], atol=1e-12)
+
+
 PINS = [pin_top2_example, pin_aux_worked_example, pin_selection_bias_example,
         pin_uniform_aux_is_one, pin_topk_bruteforce, pin_softmax_closed_forms,
         pin_router_logits_layout, pin_single_expert_is_dense_ffn, pin_identical_experts,
         pin_all_experts_is_dense_mixture, pin_shared_expert_added, pin_capacity_cases,
         pin_capacity_switch_workload, pin_dispatch_invariants, pin_quantile_vs_numpy,
-        pin_quantile_balance_share, pin_round_to_bf16, pin_bf16_activation_ffn]
+        pin_quantile_balance_share, pin_round_to_bf16, pin_bf16_activation_ffn,
+        pin_gate_entropy, pin_expert_output_scale, pin_observe_drop_and_bias,
+        pin_reroute_cases, pin_reroute_invariants, pin_expert_choice_case,
+        pin_expert_choice_bruteforce, pin_expert_choice_full_capacity_is_dense_mixture]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -400,7 +570,92 @@ def _mut_capacity_floor(T, k, E, cf):
     return T * k if cf <= 0 else int(cf * T / E)    # drops k (one of the page variants)
 
 
+def _mut_entropy_log2(probs):
+    p = np.asarray(probs, dtype=np.float64)
+    safe = np.where(p > 0, p, 1.0)
+    return float(np.mean(-np.sum(np.where(p > 0, p * np.log2(safe), 0.0), axis=1)))   # bits
+
+
+def _mut_scale_sample_std(outputs, E):
+    mean, std, mx = np.zeros(E), np.zeros(E), np.zeros(E)
+    for e, o in outputs.items():
+        mean[e], std[e], mx[e] = o.mean(), o.std(ddof=1), o.max()   # sample std, signed max
+    return {"mean": mean, "std": std, "max_abs": mx}
+
+
+_ORIG_REROUTE = om.dispatch_reroute
+
+
+def _mut_reroute_same_candidate(scores, probs, k, C, rounds):
+    # every unserved slot of a token takes the SAME next candidate
+    T, E = scores.shape
+    order = np.argsort(-scores, axis=1, kind="stable")
+    top = order[:, :k]
+    norm = np.take_along_axis(probs, top, axis=1).sum(axis=1)
+    slot_e = top.copy()
+    served = np.full((T, k), -1)
+    rnd = np.full((T, k), -1)
+    rows = [[] for _ in range(E)]
+    nxt = np.full(T, k)
+    for r in range(rounds + 1):
+        if r > 0:
+            for t in range(T):
+                if nxt[t] < E and (served[t] < 0).any():
+                    slot_e[t, served[t] < 0] = order[t, nxt[t]]
+                    nxt[t] += 1
+        for t in range(T):
+            for j in range(k):
+                e = int(slot_e[t, j])
+                if served[t, j] < 0 and len(rows[e]) < C:
+                    rows[e].append(t * k + j)
+                    served[t, j], rnd[t, j] = e, r
+    kept = np.array([len(x) for x in rows])
+    perm = np.array([f for x in rows for f in x], dtype=np.int64)
+    inv = np.full(T * k, -1)
+    inv[perm] = np.arange(perm.shape[0])
+    w = np.where(served >= 0, np.take_along_axis(probs, np.maximum(served, 0), axis=1)
+                 / norm[:, None], 0.0)
+    return om.RerouteOut(served, w, rnd, np.bincount(top.reshape(-1), minlength=E), kept,
+                         np.concatenate([[0], np.cumsum(kept)]), perm, inv,
+                         int(T * k - perm.shape[0]))
+
+
+def _mut_reroute_renormalised(scores, probs, k, C, rounds):
+    out = _ORIG_REROUTE(scores, probs, k, C, rounds)
+    tot = out.slot_w.sum(axis=1, keepdims=True)
+    out.slot_w = np.where(tot > 0, out.slot_w / np.where(tot > 0, tot, 1), 0)
+    return out
+
+
+def _mut_ec_ties_high(probs, C):
+    T, E = probs.shape
+    Cn = min(C, T)
+    chosen = np.zeros((E, Cn), dtype=np.int64)
+    weight = np.zeros((E, Cn))
+    picked = np.zeros(T, dtype=bool)
+    for e in range(E):
+        order = (T - 1 - np.argsort(-probs[::-1, e], kind="stable"))   # ties: HIGHER token
+        top = np.sort(order[:Cn])
+        chosen[e], weight[e], picked[top] = top, probs[top, e], True
+    return om.ExpertChoiceOut(chosen, weight, np.full(E, Cn), np.arange(E + 1) * Cn,
+                              int(T - picked.sum()))
+
+
+def _mut_ec_renormalised(probs, C):
+    out = _ORIG_EC(probs, C)
+    out.weight = out.weight / out.weight.sum(axis=1, keepdims=True)
+    return out
+
+
+_ORIG_EC = om.expert_choice
+
 MUTATIONS = [
+    ("gate_entropy", _mut_entropy_log2),
+    ("expert_choice", _mut_ec_ties_high),
+    ("expert_choice", _mut_ec_renormalised),
+    ("dispatch_reroute", _mut_reroute_same_candidate),
+    ("dispatch_reroute", _mut_reroute_renormalised),
+    ("expert_output_scale", _mut_scale_sample_std),
     ("renormalise", _mut_no_renorm),
     ("load_stats", _mut_f_over_T),
     ("topk_desc", _mut_topk_ascending),
