@@ -9,7 +9,9 @@ and down projections, shared expert when present, combine) over one batch of
 T synthetic tokens of the named workload (default: the Mixtral-8x7B-shaped
 layer, d=4096, E=8, k=2, SwiGLU d_ff=14336, bf16, T=16384), inputs resident
 in HBM.  The weights (2.8 GB) are larger than L2, so every step streams them
-from HBM; no L2 flush is needed.
+from HBM; no L2 flush is needed.  By default each step is one replay of a
+CUDA graph holding one captured moe_layer_forward (--launch eager calls the
+C ABI directly instead); the graph removes host launch gaps, not work.
 
 Metric: tokens/s over the whole job (all ranks).  Under torchrun each rank
 runs its own batch on its own GPU (weak scaling, no collective on the data
@@ -160,8 +162,11 @@ def oracle_sample_run(w, inp_cpu64, S):
     sub = dict(inp_cpu64)
     sub["x"] = inp_cpu64["x"][:S]
     t0 = time.perf_counter()
-    om.moe_forward(sub, w.top_k, w.act, w.capacity_factor, "probs", w.quantile_balance,
-                   None, w.dtype)
+    if w.routing == "expert":
+        om.moe_forward_expert_choice(sub, w.top_k, w.act, w.capacity_factor, None, w.dtype)
+    else:
+        om.moe_forward(sub, w.top_k, w.act, w.capacity_factor, "probs", w.quantile_balance,
+                       None, w.dtype, reroute_rounds=w.reroute_rounds)
     return time.perf_counter() - t0
 
 
@@ -244,6 +249,36 @@ def traffic_record(kernel_file):
     return rec
 
 
+def stage_pass(moe, cfg, inp, weights, ws, outs, args, use_graph, dev, reps=None):
+    """Summed per-stage milliseconds over `reps` layer calls, and the number
+    of calls.  Graph mode captures one call with stage events on and reads
+    the events after each replay; eager mode times `reps` eager calls."""
+    reps = reps or max(3, min(args.steps, 10))
+    if use_graph:
+        moe.stage_timing(True)
+        try:
+            g = moe.LayerGraph(cfg, inp["x"], weights, workspace=ws, outputs=outs, warm=False)
+            tot = {k: 0.0 for k in moe.STAGES}
+            for _ in range(reps):
+                g.replay()
+                ms, _ = moe.stage_times()
+                for k in tot:
+                    tot[k] += ms[k]
+            del g
+            return tot, reps
+        except moe.MoEError:
+            pass        # event timing inside graphs unavailable: time eager calls
+        finally:
+            moe.stage_timing(False)
+    moe.stage_timing(True)
+    for _ in range(reps):
+        moe.layer_forward(cfg, inp["x"], weights, workspace=ws, outputs=outs)
+    torch.cuda.synchronize(dev)
+    res = moe.stage_times()
+    moe.stage_timing(False)
+    return res
+
+
 def run_ours(args, w, T):
     import sparse_mixture_experts_47_b300 as moe
 
@@ -265,53 +300,84 @@ def run_ours(args, w, T):
         moe.layer_forward(cfg, inp["x"], weights, workspace=ws, outputs=outs)
     torch.cuda.synchronize(dev)
     assert moe.device_status(dev) == 0
+    l0 = moe.kernel_launches()
+    moe.layer_forward(cfg, inp["x"], weights, workspace=ws, outputs=outs)
+    launches_per_step = moe.kernel_launches() - l0
+
+    graph = None
+    if args.launch == "graph":
+        graph = moe.LayerGraph(cfg, inp["x"], weights, workspace=ws, outputs=outs, warm=False)
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            moe.layer_forward(cfg, inp["x"], weights, workspace=ws, outputs=outs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert moe.device_status(dev) == 0
 
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
-    moe.stage_timing(True)
-    l0 = moe.kernel_launches()
     barrier(world)
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        moe.layer_forward(cfg, inp["x"], weights, workspace=ws, outputs=outs)
+        step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    launches = moe.kernel_launches() - l0
-    stage_ms, calls = moe.stage_times()
-    moe.stage_timing(False)
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world)
     assert moe.device_status(dev) == 0
+    launches = launches_per_step * args.steps
 
-    # end to end through the same C ABI call with host buffers
+    # Per-stage times (CUDA events the library records around each stage on
+    # the launching stream), in a separate pass so that recording them does
+    # not perturb the timed region above.
+    stage_ms, calls = stage_pass(moe, cfg, inp, weights, ws, outs, args, graph is not None, dev)
+
+    # end to end through the same public call with host buffers
     x_host = inp["x"].cpu().pin_memory()
     y_host = torch.empty(outs["y"].shape, dtype=outs["y"].dtype).pin_memory()
-    x_dev = torch.empty_like(inp["x"])
-    for _ in range(2):
+    x_dev = inp["x"] if graph is not None else torch.empty_like(inp["x"])
+
+    def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
-        moe.layer_forward(cfg, x_dev, weights, workspace=ws, outputs=outs)
+        if graph is not None:
+            graph.replay()
+        else:
+            moe.layer_forward(cfg, x_dev, weights, workspace=ws, outputs=outs)
         y_host.copy_(outs["y"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.layer_forward(cfg, x_dev, weights, workspace=ws, outputs=outs)
-        y_host.copy_(outs["y"], non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
 
     n_dropped = int(outs["n_dropped"][0])
     counts = outs["counts"].cpu().numpy()
-    n_kept = T * w.top_k - n_dropped
-    nz = int((counts > 0).sum()) if w.capacity_factor <= 0 else int((counts > 0).sum())
+    if w.routing == "expert":
+        # every expert serves exactly its counts[e] rows; n_dropped counts the
+        # tokens no expert took
+        n_kept = int(counts.sum())
+        nz = int((counts > 0).sum())
+    else:
+        # counts are assignments before capacity; served rows = T*k - dropped
+        n_kept = T * w.top_k - n_dropped
+        nz = int((counts > 0).sum())
     flops, bytes_, up_flops, up_bytes = algorithmic(w, T, n_kept, nz)
     peaks, src = load_peaks()
     step_s = ms / 1e3 / args.steps
@@ -358,7 +424,9 @@ def run_ours(args, w, T):
                                f"k={w.top_k} d_ff={w.d_ff} T={T}",
                    "tokens_per_rank": T, "parallelism": f"replicas x{world}",
                    "l2": "no flush: weights larger than L2 stream from HBM every step",
-                   "out_dtype": "bf16"},
+                   "out_dtype": "bf16",
+                   "launch": ("one CUDA graph replay of moe_layer_forward per step"
+                              if args.launch == "graph" else "eager moe_layer_forward calls")},
         "roofline": roof,
         "layer_roofline": {"flops": flops, "bytes": bytes_, "roofline_ms": roof_s * 1e3,
                            "frac": roof_s / step_s,
@@ -386,6 +454,9 @@ def main():
     ap.add_argument("--workload", default="mixtral", choices=list(mi.WORKLOADS))
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
+                    help="replay one captured CUDA graph of the layer per step (default) "
+                         "or call the layer eagerly")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     w = mi.workload(args.workload)

@@ -70,6 +70,11 @@ typedef enum {
 enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 };
 enum { MOE_DTYPE_FP32 = 0, MOE_DTYPE_BF16 = 1 };
 enum { MOE_SELECT_PROBS = 0, MOE_SELECT_LOGITS = 1 };
+/* Token choice: each token picks its top-k experts (the layer above).
+ * Expert choice: each expert picks its top-C tokens by router probability,
+ * C = capacity (cf * T * k / E, k the average experts per token); see
+ * moe_layer_forward. */
+enum { MOE_ROUTING_TOKEN_CHOICE = 0, MOE_ROUTING_EXPERT_CHOICE = 1 };
 
 typedef struct {
     int32_t T;                /* tokens (batch * seq flattened), >= 0 */
@@ -84,6 +89,11 @@ typedef struct {
     int32_t select_space;     /* MOE_SELECT_*: where select_bias is added */
     int32_t quantile_balance; /* 1: select_bias = -Q_{1-k/E}(probs[:, e]) */
     int32_t out_dtype;        /* dtype of y: MOE_DTYPE_FP32 or MOE_DTYPE_BF16 */
+    int32_t reroute_rounds;   /* capacity overflow: 0 = dropped; R > 0 = sent to
+                                 the next-best experts in up to R rounds (see
+                                 moe_dispatch_reroute); needs capacity_factor > 0
+                                 and k * (1 + R) <= 32 */
+    int32_t routing;          /* MOE_ROUTING_*: who chooses */
 } moe_config;
 
 /* Capacity C = ceil(cf * T * k / E), or T*k when cf <= 0 (no limit).
@@ -133,6 +143,70 @@ int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx,
                  int32_t *inv, int32_t *n_dropped, void *ws, size_t ws_bytes,
                  moe_stream_t stream);
 
+/* Dispatch with capacity overflow redirected to the next-best experts
+ * (cfg->reroute_rounds = R > 0).  Source: ch. 30 §30.5.2 (tokens beyond an
+ * expert's capacity are dropped or sent to the next best expert).
+ *   Round 0 is the rule of moe_dispatch: slots in flattened (t*k + j) order
+ *   are served by their expert while it has fewer than C rows.  In each of
+ *   the R further rounds every unserved slot takes its token's next unused
+ *   expert down the token's ranking (the token's unserved slots, in j order,
+ *   take consecutive candidates) and the slots are served in (t*k + j)
+ *   order by experts that still have room.  Slots unserved after round R
+ *   are dropped.  An expert's rows are grouped in the order served.
+ *   topk_idx, topk_w [T, k]: the router's top-k and renormalised weights
+ *   cand_idx  [T, nc] int32: each token's experts ranked after its top k,
+ *             best first, nc = moe_reroute_candidates(cfg)
+ *             = min(E - k, k * R)
+ *   cand_w    [T, nc] fp32: their gate weights, p[t, e] over the token's
+ *             top-k probability sum (capacity never rescales other slots)
+ *   counts [E] (first-choice assignments before capacity), offsets [E+1],
+ *   perm [T*k], inv [T*k], n_dropped [1]: as moe_dispatch
+ *   slot_expert [T, k] int32, slot_w [T, k] fp32 (or NULL): the expert that
+ *             serves each slot and its weight (-1 and 0 when dropped) */
+int moe_dispatch_reroute(const moe_config *cfg, const int32_t *topk_idx,
+                         const float *topk_w, const int32_t *cand_idx,
+                         const float *cand_w, int32_t *counts, int32_t *offsets,
+                         int32_t *perm, int32_t *inv, int32_t *slot_expert,
+                         float *slot_w, int32_t *n_dropped, void *ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
+/* Number of candidate experts per token that redirection uses (see
+ * moe_dispatch_reroute), or -1 on an invalid cfg. */
+int64_t moe_reroute_candidates(const moe_config *cfg);
+
+/* Expert-choice routing (cfg->routing = MOE_ROUTING_EXPERT_CHOICE).
+ * Sources: deepseekmodel.com TopKRouter discussion (each expert picks the
+ * top-C tokens for its capacity, so every expert is exactly full);
+ * iwashi.co routing table (expert choice).  Expert e takes the
+ * Cn = moe_expert_choice_rows(cfg) = min(C, T) tokens with the largest
+ * router probability probs[t, e], exactly equal values by lower token
+ * index; the gate weight is probs[t, e] (not renormalised); a token may be
+ * taken by any number of experts, including none.  In moe_layer_forward the
+ * router's probabilities are used (selection bias and topk_idx/topk_w do
+ * not apply and are not written); counts = Cn per expert; n_dropped = the
+ * tokens no expert took (their routed output is 0).
+ *   probs_t   [E, T] fp32 expert-major router probabilities
+ *   perm      [E*Cn] int32 out: token of grouped row e*Cn + i, ascending in t
+ *   row_w     [E*Cn] fp32 out: its gate weight
+ *   counts [E], offsets [E+1] (e*Cn) out
+ *   tok_start [T+1], tok_rows [E*Cn] int32 out: the rows of token t are
+ *             tok_rows[tok_start[t] .. tok_start[t+1]), experts ascending
+ *   n_unchosen [1] int32 out */
+int64_t moe_expert_choice_rows(const moe_config *cfg);
+int moe_expert_choice(const moe_config *cfg, const float *probs_t,
+                      int32_t *perm, float *row_w, int32_t *counts,
+                      int32_t *offsets, int32_t *tok_start, int32_t *tok_rows,
+                      int32_t *n_unchosen, void *ws, size_t ws_bytes,
+                      moe_stream_t stream);
+
+/* Combine over per-token row lists (expert choice):
+ * y[t] = sum_{i in [tok_start[t], tok_start[t+1])} row_w[r_i] out_sorted[r_i]
+ *        + shared_out[t], in list order.  out_sorted [rows, d] fp32. */
+int moe_combine_rows(const moe_config *cfg, const float *out_sorted,
+                     const float *row_w, const int32_t *tok_start,
+                     const int32_t *tok_rows, const float *shared_out, void *y,
+                     moe_stream_t stream);
+
 /* Same results as moe_dispatch, for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a deployment variant.
  * Some callers have no way to get a workspace: code running inside a host
@@ -158,10 +232,13 @@ int moe_dispatch_static(const moe_config *cfg, const int32_t *topk_idx,
                         int32_t *inv, int32_t *n_dropped, moe_stream_t stream);
 
 /* Per-expert FFN on the grouped rows: out_sorted[s] = FFN_e(x[perm[s] / k])
- * for offsets[e] <= s < offsets[e+1].  Source: ch. 30 §30.2.4 / §30.6.1.
- *   x          [T, d]; perm, offsets as produced by moe_dispatch
+ * for offsets[e] <= s < offsets[e+1] (expert choice: x[perm[s]]).
+ * Source: ch. 30 §30.2.4 / §30.6.1.
+ *   x          [T, d]; perm, offsets as produced by moe_dispatch (or
+ *              moe_dispatch_reroute, moe_expert_choice)
  *   w1, w3, w2 expert weights (w3 NULL for ReLU)
- *   out_sorted [T*k, d] fp32 out (rows >= offsets[E] untouched) */
+ *   out_sorted [rows, d] fp32 out, rows = T*k (expert choice: E * Cn);
+ *              rows >= offsets[E] untouched */
 int moe_expert_ffn(const moe_config *cfg, const void *x, const int32_t *perm,
                    const int32_t *offsets, const void *w1, const void *w3,
                    const void *w2, float *out_sorted, void *ws,
@@ -210,6 +287,9 @@ typedef struct {
     float *load_max_over_mean; /* [1] */
     float *select_bias_out;    /* [E] quantile bias (quantile_balance only) */
     int32_t *counts_unbiased;  /* [E] counts of the plain top-k, no bias */
+    int32_t *slot_expert;      /* [T, k] expert that served each slot after
+                                  capacity (and redirection), -1 if dropped */
+    float *slot_w;             /* [T, k] gate weight the combine used for it */
 } moe_layer_outputs;
 
 /* The whole forward pass (router, dispatch, experts, shared expert,
@@ -219,6 +299,45 @@ int moe_layer_forward(const moe_config *cfg, const void *x,
                       const moe_layer_weights *wts,
                       const moe_layer_outputs *out, void *ws,
                       size_t ws_bytes, moe_stream_t stream);
+
+/* The monitoring set the deepseekmodel.com page asks every MoE deployment
+ * to log ("エキスパート間のスケールドリフト": drop ratio, per-expert load,
+ * per-expert output scale, size of the bias term, gate entropy).  Device
+ * pointers; NULL = not wanted.  Per-expert load is moe_layer_outputs.counts. */
+typedef struct {
+    float *drop_ratio;          /* [1] n_dropped / (T k) */
+    float *gate_entropy;        /* [1] mean over tokens of -sum_e p ln p (nats) */
+    float *bias_mean_abs;       /* [1] mean |b_e| of the selection bias in effect
+                                       (the caller's or the quantile bias; 0 without) */
+    float *bias_max_abs;        /* [1] max |b_e| */
+    float *expert_out_mean;     /* [E] mean over all elements of expert e's output
+                                       rows (its kept rows' FFN outputs, before the
+                                       gate weight); 0 for an expert without rows */
+    float *expert_out_std;      /* [E] population standard deviation of the same */
+    float *expert_out_max_abs;  /* [E] largest magnitude of the same */
+} moe_observability;
+
+/* moe_layer_forward plus the observability set `obs` (may be NULL, which is
+ * exactly moe_layer_forward).  The entropy is summed inside the router
+ * kernels; the expert output scale costs one extra read of the expert
+ * outputs (T*k*d fp32). */
+int moe_layer_forward_observed(const moe_config *cfg, const void *x,
+                               const moe_layer_weights *wts,
+                               const moe_layer_outputs *out,
+                               const moe_observability *obs, void *ws,
+                               size_t ws_bytes, moe_stream_t stream);
+
+/* The observability set from stored tensors (the stage form):
+ *   probs      [T, E] fp32 router probabilities, or NULL (no entropy)
+ *   out_sorted [rows, d] fp32 expert outputs grouped by expert and
+ *   offsets    [E+1] int32 their row ranges, or both NULL (no output scale)
+ *   select_bias [E] fp32 or NULL; n_dropped [1] int32 or NULL
+ * Fields of `obs` whose inputs are NULL are set to 0. */
+int moe_observe(const moe_config *cfg, const float *probs,
+                const float *out_sorted, const int32_t *offsets,
+                const float *select_bias, const int32_t *n_dropped,
+                const moe_observability *obs, void *ws, size_t ws_bytes,
+                moe_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device error word that
  * kernels set when a bounded wait gave up (MOE_ERR_DEVICE_TIMEOUT), or
@@ -253,7 +372,10 @@ int moe_stage_timing_enable(int on);
 
 /* Waits for the recorded events, writes the summed milliseconds of each
  * stage into stage_ms[MOE_NUM_STAGES] and the number of timed calls into
- * *calls, then discards the records.  Blocks the host. */
+ * *calls.  The records are kept until the next moe_stage_timing_enable().
+ * A call captured into a CUDA graph while timing is on captures its event
+ * records; every replay records those events again, so a read after a
+ * replay returns the times of that replay.  Blocks the host. */
 int moe_stage_timing_read(double *stage_ms, int64_t *calls);
 
 #ifdef __cplusplus

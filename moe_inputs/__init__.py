@@ -18,6 +18,15 @@ Workloads (the model shapes the pages discuss; no dataset is involved):
 * ``e896``     very sparse: bf16, T=16384, d=4096, E=896, k=8, SwiGLU d_ff=512,
                Zipf(1.1) popularity via logit offsets -1.1*ln(e+1),
                per-batch quantile selection bias.
+* ``switch_reroute`` the Switch workload with capacity overflow sent to the
+               next-best expert (one round) instead of being dropped.
+* ``mixtral_ec`` the Mixtral-shaped layer with expert-choice routing: every
+               expert takes its C = T k / E top tokens (capacity factor 1.0).
+* ``mixtral_cap``, ``deepseek_cap``  the Mixtral- and DeepSeek-shaped layers
+               (same seeds, so the same weights and tokens) with a capacity
+               factor of 1.0, the value the capacity section gives for k = 2
+               and for fine-grained experts: overflow beyond
+               C = ceil(T k / E) per expert is dropped in (t, j) order.
 
 Value recipe: x ~ N(0,1); router weight W_r ~ N(0, 1/d) in fp32; expert
 weights ~ N(0, 1/fan_in), drawn in fp32 and rounded to bf16 (round to nearest
@@ -61,6 +70,8 @@ class MoEWorkload:
     logit_offset: str = "none"    # "none" | "expert0" | "zipf"
     select_bias: str = "none"     # "none" | "uniform"
     quantile_balance: bool = False
+    reroute_rounds: int = 0       # capacity overflow: 0 dropped, R > 0 redirected
+    routing: str = "token"        # "token" (token choice) | "expert" (expert choice)
 
     def with_sizes(self, **kw) -> "MoEWorkload":
         """A reduced copy (same recipe, smaller shapes) for small test cases."""
@@ -81,6 +92,16 @@ WORKLOADS: Dict[str, MoEWorkload] = {
                             (128, 8192), d_ff_shared=2048, select_bias="uniform"),
     "e896": MoEWorkload("e896", 4, 4096, 896, 8, 512, "swiglu", "bf16", (16384,),
                         logit_offset="zipf", quantile_balance=True),
+    "mixtral_cap": MoEWorkload("mixtral_cap", 2, 4096, 8, 2, 14336, "swiglu", "bf16",
+                               (4096, 16384), capacity_factor=1.0),
+    "deepseek_cap": MoEWorkload("deepseek_cap", 3, 7168, 256, 8, 2048, "swiglu", "bf16",
+                                (8192,), capacity_factor=1.0, d_ff_shared=2048,
+                                select_bias="uniform"),
+    "switch_reroute": MoEWorkload("switch_reroute", 1, 1024, 8, 1, 4096, "relu", "bf16",
+                                  (8192,), capacity_factor=1.25, logit_offset="expert0",
+                                  reroute_rounds=1),
+    "mixtral_ec": MoEWorkload("mixtral_ec", 2, 4096, 8, 2, 14336, "swiglu", "bf16",
+                              (4096, 16384), capacity_factor=1.0, routing="expert"),
 }
 
 

@@ -19,6 +19,9 @@ import torch
 __all__ = [
     "MoEConfig", "MoEError", "lib", "capacity", "workspace_size", "router_topk", "dispatch",
     "expert_ffn", "combine", "load_stats", "layer_forward", "device_status", "Workspace",
+    "LayerGraph", "observe", "OBS_KEYS", "dispatch_reroute", "reroute_candidates",
+    "ROUTING_TOKEN_CHOICE", "ROUTING_EXPERT_CHOICE", "expert_choice", "expert_choice_rows",
+    "combine_rows",
     "ACT_RELU", "ACT_SWIGLU", "DTYPE_FP32", "DTYPE_BF16", "SELECT_PROBS", "SELECT_LOGITS",
 ]
 
@@ -28,6 +31,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 ACT_RELU, ACT_SWIGLU = 0, 1
 DTYPE_FP32, DTYPE_BF16 = 0, 1
 SELECT_PROBS, SELECT_LOGITS = 0, 1
+ROUTING_TOKEN_CHOICE, ROUTING_EXPERT_CHOICE = 0, 1
 
 MOE_OK = 0
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
@@ -48,7 +52,8 @@ class _Config(ctypes.Structure):
                 ("d_ff", ctypes.c_int32), ("act", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("d_ff_shared", ctypes.c_int32),
                 ("select_space", ctypes.c_int32), ("quantile_balance", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("reroute_rounds", ctypes.c_int32),
+                ("routing", ctypes.c_int32)]
 
 
 class _Weights(ctypes.Structure):
@@ -59,7 +64,16 @@ class _Weights(ctypes.Structure):
 class _Outputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("y", "topk_idx", "topk_w", "counts", "n_dropped", "f", "p", "aux",
-                 "load_max_over_mean", "select_bias_out", "counts_unbiased")]
+                 "load_max_over_mean", "select_bias_out", "counts_unbiased", "slot_expert",
+                 "slot_w")]
+
+
+OBS_KEYS = ("drop_ratio", "gate_entropy", "bias_mean_abs", "bias_max_abs", "expert_out_mean",
+            "expert_out_std", "expert_out_max_abs")
+
+
+class _Observability(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in OBS_KEYS]
 
 
 def _load():
@@ -74,12 +88,24 @@ def _load():
     L.moe_router_topk.argtypes = [C] + [P] * 10 + [Z, V]; L.moe_router_topk.restype = I
     L.moe_dispatch.argtypes = [C] + [P] * 7 + [Z, V]; L.moe_dispatch.restype = I
     L.moe_dispatch_static.argtypes = [C] + [P] * 6 + [V]; L.moe_dispatch_static.restype = I
+    L.moe_dispatch_reroute.argtypes = [C] + [P] * 12 + [Z, V]
+    L.moe_dispatch_reroute.restype = I
+    L.moe_reroute_candidates.argtypes = [C]; L.moe_reroute_candidates.restype = ctypes.c_int64
+    L.moe_expert_choice_rows.argtypes = [C]; L.moe_expert_choice_rows.restype = ctypes.c_int64
+    L.moe_expert_choice.argtypes = [C] + [P] * 9 + [Z, V]; L.moe_expert_choice.restype = I
+    L.moe_combine_rows.argtypes = [C] + [P] * 6 + [V]; L.moe_combine_rows.restype = I
     L.moe_expert_ffn.argtypes = [C] + [P] * 8 + [Z, V]; L.moe_expert_ffn.restype = I
     L.moe_combine.argtypes = [C] + [P] * 5 + [V]; L.moe_combine.restype = I
     L.moe_load_stats.argtypes = [C] + [P] * 8 + [Z, V]; L.moe_load_stats.restype = I
     L.moe_layer_forward.argtypes = [C, P, ctypes.POINTER(_Weights), ctypes.POINTER(_Outputs),
                                     P, Z, V]
     L.moe_layer_forward.restype = I
+    L.moe_layer_forward_observed.argtypes = [C, P, ctypes.POINTER(_Weights),
+                                             ctypes.POINTER(_Outputs),
+                                             ctypes.POINTER(_Observability), P, Z, V]
+    L.moe_layer_forward_observed.restype = I
+    L.moe_observe.argtypes = [C] + [P] * 5 + [ctypes.POINTER(_Observability), P, Z, V]
+    L.moe_observe.restype = I
     L.moe_device_status.argtypes = [V]; L.moe_device_status.restype = I
     L.moe_strerror.argtypes = [I]; L.moe_strerror.restype = ctypes.c_char_p
     L.moe_kernel_launches.argtypes = []; L.moe_kernel_launches.restype = ctypes.c_int64
@@ -107,6 +133,8 @@ class MoEConfig:
     select_space: int = SELECT_PROBS
     quantile_balance: int = 0
     out_dtype: int = DTYPE_FP32
+    reroute_rounds: int = 0
+    routing: int = 0
 
     def c(self) -> _Config:
         return _Config(*(getattr(self, f.name) for f in dataclasses.fields(self)))
@@ -191,10 +219,80 @@ def dispatch(cfg: MoEConfig, idx, workspace: Optional[Workspace] = None) -> Dict
             "n_dropped": nd}
 
 
+def reroute_candidates(cfg: MoEConfig) -> int:
+    """Candidates per token that redirection of capacity overflow uses."""
+    return int(lib.moe_reroute_candidates(ctypes.byref(cfg.c())))
+
+
+def dispatch_reroute(cfg: MoEConfig, idx, w, cand_idx, cand_w,
+                     workspace: Optional[Workspace] = None) -> Dict[str, torch.Tensor]:
+    """Dispatch with capacity overflow sent to the next-best experts
+    (``cfg.reroute_rounds`` rounds); ``cand_idx``/``cand_w`` [T, nc] are each
+    token's experts after its top k and their weights."""
+    dev = idx.device
+    T, k, E = cfg.T, cfg.top_k, cfg.n_experts
+    Tk = T * k
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.full((max(Tk, 1),), -7, dtype=torch.int32, device=dev)
+    inv = torch.full((max(Tk, 1),), -7, dtype=torch.int32, device=dev)
+    se = torch.empty((max(T, 1), k), dtype=torch.int32, device=dev)
+    sw = torch.empty((max(T, 1), k), dtype=torch.float32, device=dev)
+    nd = torch.empty(1, dtype=torch.int32, device=dev)
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_dispatch_reroute", lib.moe_dispatch_reroute(
+        ctypes.byref(cfg.c()), _ptr(idx), _ptr(w), _ptr(cand_idx), _ptr(cand_w), _ptr(counts),
+        _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(se), _ptr(sw), _ptr(nd), _ptr(buf), nb,
+        _stream(dev)))
+    return {"counts": counts, "offsets": offsets, "perm": perm[:Tk], "inv": inv[:Tk],
+            "slot_expert": se[:T], "slot_w": sw[:T], "n_dropped": nd}
+
+
+def expert_choice_rows(cfg: MoEConfig) -> int:
+    """Rows each expert takes under expert choice, min(C, T)."""
+    return int(lib.moe_expert_choice_rows(ctypes.byref(cfg.c())))
+
+
+def expert_choice(cfg: MoEConfig, probs_t, workspace: Optional[Workspace] = None
+                  ) -> Dict[str, torch.Tensor]:
+    """Expert-choice selection from expert-major probabilities ``probs_t``
+    [E, T]: every expert takes its top ``expert_choice_rows(cfg)`` tokens."""
+    dev = probs_t.device
+    T, E = cfg.T, cfg.n_experts
+    R = E * expert_choice_rows(cfg)
+    perm = torch.full((max(R, 1),), -7, dtype=torch.int32, device=dev)
+    row_w = torch.zeros(max(R, 1), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    tok_start = torch.empty(T + 1, dtype=torch.int32, device=dev)
+    tok_rows = torch.full((max(R, 1),), -7, dtype=torch.int32, device=dev)
+    nu = torch.empty(1, dtype=torch.int32, device=dev)
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_expert_choice", lib.moe_expert_choice(
+        ctypes.byref(cfg.c()), _ptr(probs_t), _ptr(perm), _ptr(row_w), _ptr(counts),
+        _ptr(offsets), _ptr(tok_start), _ptr(tok_rows), _ptr(nu), _ptr(buf), nb, _stream(dev)))
+    return {"perm": perm[:R], "row_w": row_w[:R], "counts": counts, "offsets": offsets,
+            "tok_start": tok_start, "tok_rows": tok_rows[:R], "n_unchosen": nu}
+
+
+def combine_rows(cfg: MoEConfig, out_sorted, row_w, tok_start, tok_rows,
+                 shared_out=None) -> torch.Tensor:
+    """y[t] = sum over token t's rows r of row_w[r] out_sorted[r] (+ shared)."""
+    dev = out_sorted.device
+    ydt = torch.float32 if cfg.out_dtype == DTYPE_FP32 else torch.bfloat16
+    y = torch.empty((cfg.T, cfg.d_model), dtype=ydt, device=dev)
+    _check("moe_combine_rows", lib.moe_combine_rows(
+        ctypes.byref(cfg.c()), _ptr(out_sorted), _ptr(row_w), _ptr(tok_start), _ptr(tok_rows),
+        _ptr(shared_out), _ptr(y), _stream(dev)))
+    return y
+
+
 def expert_ffn(cfg: MoEConfig, x, perm, offsets, w1, w3, w2,
                workspace: Optional[Workspace] = None) -> torch.Tensor:
     dev = x.device
-    out = torch.zeros((max(cfg.T * cfg.top_k, 1), cfg.d_model), dtype=torch.float32, device=dev)
+    rows = (cfg.n_experts * expert_choice_rows(cfg) if cfg.routing == ROUTING_EXPERT_CHOICE
+            else cfg.T * cfg.top_k)
+    out = torch.zeros((max(rows, 1), cfg.d_model), dtype=torch.float32, device=dev)
     buf, nb = _ws(cfg, dev, workspace)
     _check("moe_expert_ffn", lib.moe_expert_ffn(
         ctypes.byref(cfg.c()), _ptr(x), _ptr(perm), _ptr(offsets), _ptr(w1), _ptr(w3), _ptr(w2),
@@ -230,13 +328,27 @@ def load_stats(cfg: MoEConfig, idx, probs, workspace: Optional[Workspace] = None
 _WEIGHT_KEYS = ("w_r", "logit_bias", "select_bias", "w1", "w3", "w2", "ws1", "ws3", "ws2")
 
 
+def _obs_tensors(cfg: MoEConfig, dev, obs: Optional[Dict]) -> Dict[str, torch.Tensor]:
+    o = dict(obs or {})
+    for key in OBS_KEYS:
+        if o.get(key) is None:
+            n = cfg.n_experts if key.startswith("expert_out") else 1
+            o[key] = torch.empty(n, dtype=torch.float32, device=dev)
+    return o
+
+
 def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
                   workspace: Optional[Workspace] = None, outputs: Optional[Dict] = None,
-                  want_unbiased_counts: bool = False) -> Dict[str, torch.Tensor]:
+                  want_unbiased_counts: bool = False, observe: bool = False,
+                  observed: Optional[Dict] = None,
+                  want_slots: bool = False) -> Dict[str, torch.Tensor]:
     """The whole layer on torch's current stream.  ``weights`` holds device
     tensors under the keys w_r, logit_bias, select_bias, w1, w3, w2, ws1,
     ws3, ws2 (missing or None = absent).  ``outputs`` may pass preallocated
-    output tensors (same keys as the returned dict)."""
+    output tensors (same keys as the returned dict).  ``observe`` adds the
+    monitoring set (``OBS_KEYS``: drop ratio, gate entropy, bias size,
+    per-expert output mean/std/max) under the key "observe"; ``observed``
+    may pass its preallocated tensors."""
     dev = x.device
     T, E, k, d = cfg.T, cfg.n_experts, cfg.top_k, cfg.d_model
     o = dict(outputs or {})
@@ -259,16 +371,80 @@ def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
         need("select_bias", (E,), torch.float32)
     if want_unbiased_counts:
         need("counts_unbiased", (E,), torch.int32)
+    if want_slots:
+        need("slot_expert", (T, k), torch.int32)
+        need("slot_w", (T, k), torch.float32)
     W = _Weights(*(_ptr(weights.get(key)) for key in _WEIGHT_KEYS))
     O = _Outputs(_ptr(o["y"]), _ptr(o["idx"]), _ptr(o["w"]), _ptr(o["counts"]),
                  _ptr(o["n_dropped"]), _ptr(o["f"]), _ptr(o["p"]), _ptr(o["aux"]),
                  _ptr(o["load_max_over_mean"]), _ptr(o.get("select_bias")),
-                 _ptr(o.get("counts_unbiased")))
+                 _ptr(o.get("counts_unbiased")), _ptr(o.get("slot_expert")),
+                 _ptr(o.get("slot_w")))
     buf, nb = _ws(cfg, dev, workspace)
+    if observe or observed is not None:
+        ob = _obs_tensors(cfg, dev, observed)
+        OB = _Observability(*(_ptr(ob[key]) for key in OBS_KEYS))
+        _check("moe_layer_forward_observed", lib.moe_layer_forward_observed(
+            ctypes.byref(cfg.c()), _ptr(x), ctypes.byref(W), ctypes.byref(O), ctypes.byref(OB),
+            _ptr(buf), nb, _stream(dev)))
+        o["observe"] = ob
+        return o
     _check("moe_layer_forward", lib.moe_layer_forward(
         ctypes.byref(cfg.c()), _ptr(x), ctypes.byref(W), ctypes.byref(O), _ptr(buf), nb,
         _stream(dev)))
     return o
+
+
+def observe(cfg: MoEConfig, probs=None, out_sorted=None, offsets=None, select_bias=None,
+            n_dropped=None, workspace: Optional[Workspace] = None) -> Dict[str, torch.Tensor]:
+    """The monitoring set from stored tensors (stage form of the layer's
+    ``observe``): gate entropy from ``probs`` [T, E], per-expert output
+    scale from ``out_sorted`` [rows, d] fp32 grouped by ``offsets`` [E+1],
+    bias size from ``select_bias``, drop ratio from ``n_dropped``."""
+    dev = next(t.device for t in (probs, out_sorted, select_bias, n_dropped) if t is not None)
+    ob = _obs_tensors(cfg, dev, None)
+    OB = _Observability(*(_ptr(ob[key]) for key in OBS_KEYS))
+    buf, nb = _ws(cfg, dev, workspace)
+    _check("moe_observe", lib.moe_observe(
+        ctypes.byref(cfg.c()), _ptr(probs), _ptr(out_sorted), _ptr(offsets), _ptr(select_bias),
+        _ptr(n_dropped), ctypes.byref(OB), _ptr(buf), nb, _stream(dev)))
+    return ob
+
+
+class LayerGraph:
+    """One ``layer_forward`` captured into a CUDA graph on fixed buffers.
+
+    An eager ``layer_forward`` costs host time for argument checks,
+    tensor-map encoding and about fifteen kernel launches; for small batches
+    that host time is longer than the kernels themselves.  A graph replays
+    the same kernels with a single launch.  The graph reads ``x`` and the
+    weights from the tensors given here and writes the same output tensors on
+    every replay: copy a new batch into ``self.x`` (same shape) before
+    ``replay()``.  The capture itself runs no kernels; a first eager call
+    made before it initialises the outputs and the kernels' attributes."""
+
+    def __init__(self, cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
+                 workspace: Optional[Workspace] = None, outputs: Optional[Dict] = None,
+                 warm: bool = True):
+        """``warm=False`` skips the eager call; ``outputs`` must then hold
+        every output tensor of an earlier ``layer_forward`` of this ``cfg``
+        on the same workspace."""
+        self.cfg, self.x, self.weights = cfg, x, dict(weights)
+        self.workspace = workspace or Workspace(x.device)
+        if warm or outputs is None:
+            self.outputs = layer_forward(cfg, x, self.weights, workspace=self.workspace,
+                                         outputs=outputs)
+        else:
+            self.outputs = outputs
+        torch.cuda.synchronize(x.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="relaxed"):
+            layer_forward(cfg, x, self.weights, workspace=self.workspace, outputs=self.outputs)
+
+    def replay(self) -> Dict[str, torch.Tensor]:
+        """Enqueue the captured layer on torch's current stream."""
+        self.graph.replay()
+        return self.outputs
 
 
 STAGES = ("router", "dispatch", "stats", "gather", "up", "down", "shared", "combine")
@@ -304,4 +480,6 @@ def config_for(workload, T: int, out_dtype: int = DTYPE_FP32) -> MoEConfig:
         dtype=DTYPE_FP32 if workload.dtype == "fp32" else DTYPE_BF16,
         capacity_factor=float(workload.capacity_factor), d_ff_shared=workload.d_ff_shared,
         select_space=SELECT_PROBS, quantile_balance=int(bool(workload.quantile_balance)),
-        out_dtype=out_dtype)
+        out_dtype=out_dtype, reroute_rounds=int(getattr(workload, "reroute_rounds", 0)),
+        routing=ROUTING_EXPERT_CHOICE if getattr(workload, "routing", "token") == "expert"
+        else ROUTING_TOKEN_CHOICE)

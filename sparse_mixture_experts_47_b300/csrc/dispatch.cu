@@ -67,10 +67,17 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
     const int e = threadIdx.x;
     int kept = 0, run = 0;
     if (e < E) {
-        for (int b = 0; b < nblk; ++b) {
-            const size_t o = (size_t)b * E + e;
-            if (block_base) block_base[o] = run;
-            run += hist[o];
+        // 8 histogram loads in flight per step; the running sum stays in order
+        for (int b0 = 0; b0 < nblk; b0 += 8) {
+            int hv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                hv[u] = b0 + u < nblk ? hist[(size_t)(b0 + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (b0 + u < nblk && block_base) block_base[(size_t)(b0 + u) * E + e] = run;
+                run += hv[u];
+            }
         }
         if (counts) counts[e] = run;
         kept = (long long)run < C ? run : (int)C;
@@ -86,21 +93,38 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
     }
 }
 
+// One warp per chunk.  The chunk's expert indices are loaded up front (32
+// per lane, coalesced) and the expert offsets staged in shared memory, so
+// the in-order walk below touches only registers and shared memory.
 __global__ void dispatch_scatter_kernel(const int32_t *idx, long long n, int E, long long C,
                                         const int32_t *block_base, const int32_t *offsets,
                                         int32_t *perm, int32_t *inv) {
-    extern __shared__ int run[];
+    extern __shared__ int run[];          // [E] running rank, then [E] offsets
+    int *off = run + E;
     const int lane = threadIdx.x;
-    for (int i = lane; i < E; i += 32) run[i] = block_base[(size_t)blockIdx.x * E + i];
-    __syncwarp();
+    for (int i = lane; i < E; i += 32) {
+        run[i] = block_base[(size_t)blockIdx.x * E + i];
+        off[i] = offsets[i];
+    }
     const long long base = (long long)blockIdx.x * kDispatchChunk;
-    for (int i0 = 0; i0 < kDispatchChunk && base + i0 < n; i0 += 32) {
-        const long long f = base + i0 + lane;
+    constexpr int kIter = kDispatchChunk / 32;
+    int ev[kIter];
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+        const long long f = base + it * 32 + lane;
         int e = -1;
         if (f < n) {
             e = idx[f];
             if (e < 0 || e >= E) e = -1;
         }
+        ev[it] = e;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+        const long long f = base + it * 32 + lane;
+        if (base + it * 32 >= n) break;
+        const int e = ev[it];
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         int rank = 0;
         if (e >= 0) rank = run[e] + __popc(peers & lanemask_lt());
@@ -109,7 +133,7 @@ __global__ void dispatch_scatter_kernel(const int32_t *idx, long long n, int E, 
         __syncwarp();
         if (f < n) {
             if (e >= 0 && rank < C) {
-                const int s = offsets[e] + rank;
+                const int s = off[e] + rank;
                 perm[s] = (int32_t)f;
                 inv[f] = s;
             } else {
@@ -133,8 +157,8 @@ cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long 
                                              n_dropped);
     note_launch();
     if (nblk > 0) {
-        dispatch_scatter_kernel<<<nblk, 32, sizeof(int) * E, st>>>(idx, n, E, C, block_base,
-                                                                   offsets, perm, inv);
+        dispatch_scatter_kernel<<<nblk, 32, 2 * sizeof(int) * E, st>>>(idx, n, E, C, block_base,
+                                                                       offsets, perm, inv);
         note_launch();
     }
     return cudaGetLastError();

@@ -22,6 +22,12 @@
 //   warp 2     TMEM allocator (512 columns: two 256-column accumulators)
 //   warps 4-7  epilogue: tcgen05.ld of 32 TMEM lanes each, activation,
 //              bf16 (up) or fp32 (down) stores
+// Small batches (a few rows per expert) run the same pipeline with the
+// operands swapped (NT > 0): 128 weight rows are the MMA's M side and NT = 16,
+// 32 or 64 token rows its N side, so a tile streams 128 rows of W1 (and W3)
+// against a narrow token tile instead of padding 128 token rows.  The
+// reduction can then be split over CTAs (k_splits): each split writes fp32
+// partial sums that a later kernel adds in split order.
 // Every mbarrier wait is bounded (about 2 s of no progress); on expiry the
 // kernel sets the device error word, stops issuing, lets its own copies and
 // MMAs land, frees TMEM and returns.
@@ -36,13 +42,33 @@ namespace tc {
 constexpr int BM = 128;              // rows per tile (UMMA M)
 constexpr int BNM = 256;             // UMMA N (B rows per stage)
 constexpr int BK = 64;               // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;             // 16 KB
-constexpr int B_BYTES = BNM * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int WROWS = 128;           // weight rows of one TMA box
 constexpr int TMEM_COLS = 512;
-constexpr int ACC_COLS = 256;
+constexpr int ACC_COLS = 256;        // columns of one of the two accumulators
+constexpr int kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KB)
+constexpr int kSmemExtra = 1024 /* alignment slack */ + 256 /* barriers */;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
+
+// Tile geometry of one kernel instantiation.  NT = 0: token rows on the M
+// side (A = 128 activation rows, B = 256 weight rows).  NT > 0: weight rows on
+// the M side (A = 128 rows of W1, plus 128 rows of W3 for SwiGLU), token rows
+// on the N side (NT rows).  A stage holds the activation tile first, then the
+// weight tile(s); every tile is a multiple of 1024 bytes.
+template <int MODE, int NT, int BN> struct Geo {
+    static constexpr bool SWAP = NT > 0;
+    static constexpr int ROWS = SWAP ? NT : BM;                  // activation rows per tile
+    static constexpr int WT = (SWAP && MODE == GEMM_UP_SWIGLU) ? 2 : 1;
+    // rows of one weight TMA box: 128 (NT > 0), BN / 2 (NT = 0: two boxes)
+    static constexpr int BOX = SWAP ? WROWS : BN / 2;
+    static constexpr int ACT_BYTES = ROWS * BK * 2;
+    static constexpr int W_BYTES = SWAP ? WT * WROWS * BK * 2 : BN * BK * 2;
+    static constexpr int STAGE_BYTES = ACT_BYTES + W_BYTES;
+    static constexpr int FIT = (kSmemLimit - kSmemExtra) / STAGE_BYTES;
+    static constexpr int STAGES = SWAP ? (FIT < 8 ? FIT : 8) : (BN == BNM ? 4 : 6);
+    // output columns (features) of one tile
+    static constexpr int OUTC = SWAP ? WROWS : (MODE == GEMM_UP_SWIGLU ? BN / 2 : BN);
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + kSmemExtra;
+};
 
 struct Args {
     int mode;          // GEMM_UP_SWIGLU, GEMM_UP_RELU, GEMM_DOWN
@@ -51,17 +77,13 @@ struct Args {
     int a_k_period;    // A's column of reduction index k is k mod a_k_period
     int n_ntiles;      // N-tiles of the output (128 cols for SwiGLU, 256 otherwise)
     int b_rows;        // weight rows per expert (F for up, d for down)
-    int k_splits;      // work items per output tile along K (GEMM_DOWN only)
+    int k_splits;      // work items per output tile along K
     int kb_per_split;  // K blocks of one split
     long long split_stride;   // output elements between the partial results of splits
     const int32_t *tile_e, *tile_start, *n_mtiles, *offsets;
     void *C;
     int ldc;
 };
-
-__host__ __device__ constexpr size_t smem_bytes() {
-    return (size_t)STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256 /* barriers */;
-}
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -173,8 +195,10 @@ struct TileCoord {
     int e, m0, mend, n0, split, kb0, kb1;
 };
 
-// Work item L -> (split, expert, M-tile, N-tile, K-block range).  Splits are
-// outermost so that the CTAs in flight work on the same K slice.
+// Work item L -> (split, expert, row tile, output-column tile, K-block
+// range).  Splits are outermost so that the CTAs in flight work on the same K
+// slice.  ROWS = activation rows per tile, OUTC = output columns per tile.
+template <int ROWS, int OUTC>
 __device__ __forceinline__ TileCoord decode_tile(const Args &g, int L, int tiles, int nk) {
     const int split = L / tiles;
     L -= split * tiles;
@@ -186,9 +210,9 @@ __device__ __forceinline__ TileCoord decode_tile(const Args &g, int L, int tiles
     const int nt = local / mt_e, mt = local - nt * mt_e;
     TileCoord c;
     c.e = e;
-    c.m0 = g.offsets[e] + mt * BM;
+    c.m0 = g.offsets[e] + mt * ROWS;
     c.mend = g.offsets[e + 1];
-    c.n0 = nt * (g.mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM);
+    c.n0 = nt * OUTC;
     c.split = split;
     c.kb0 = split * g.kb_per_split;
     c.kb1 = min(nk, c.kb0 + g.kb_per_split);
@@ -206,15 +230,17 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
     return u;
 }
 
-template <int MODE>
+template <int MODE, int NT, int BN>
 __global__ void __launch_bounds__(256, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, Args g) {
+    using G = Geo<MODE, NT, BN>;
+    constexpr int STAGES = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * G::STAGE_BYTES);
     // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done[1]
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
@@ -259,19 +285,21 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t issued = 0;   // stages with a load in flight or unconsumed
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
-            const TileCoord c = decode_tile(g, L, tiles, nk);
+            const TileCoord c = decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk);
             int b0, b1;
-            if (MODE == GEMM_UP_SWIGLU) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
-            else { b0 = c.e * g.b_rows + c.n0; b1 = b0 + BNM / 2; }
+            if (G::SWAP) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
+            else if (MODE == GEMM_UP_SWIGLU) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
+            else { b0 = c.e * g.b_rows + c.n0; b1 = b0 + BN / 2; }
             for (int kb = c.kb0; kb < c.kb1; ++kb) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
-                mbar_expect_tx(fb, STAGE_BYTES);
-                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                const uint32_t sb = sa + A_BYTES;
+                mbar_expect_tx(fb, G::STAGE_BYTES);
+                const uint32_t sa = smem_u32(smem + stage * G::STAGE_BYTES);
+                const uint32_t sb = sa + G::ACT_BYTES;
                 tma_load_2d(sa, &tmA, (kb * BK) % g.a_k_period, c.m0, fb);
                 tma_load_2d(sb, &tmB0, kb * BK, b0, fb);
-                tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b1, fb);
+                if (!G::SWAP || MODE == GEMM_UP_SWIGLU)
+                    tma_load_2d(sb + G::BOX * BK * 2, &tmB1, kb * BK, b1, fb);
                 issued |= 1u << stage;
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
@@ -288,7 +316,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_bf16(BM, BNM);
+        constexpr uint32_t idesc = G::SWAP ? idesc_bf16(WROWS, NT) : idesc_bf16(BM, BN);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -305,12 +333,23 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                const uint32_t sb = sa + A_BYTES;
+                const uint32_t sa = smem_u32(smem + stage * G::STAGE_BYTES);
+                const uint32_t sb = sa + G::ACT_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
-                           (kb > kb0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+                    if (G::SWAP) {
+                        // weights (M side) x tokens (N side)
+                        tc_mma(d_tmem, desc_sw128(sb + kk * 32), desc_sw128(sa + kk * 32), idesc,
+                               accum);
+                        if (MODE == GEMM_UP_SWIGLU)
+                            tc_mma(d_tmem + NT, desc_sw128(sb + WROWS * BK * 2 + kk * 32),
+                                   desc_sw128(sa + kk * 32), idesc, accum);
+                    } else {
+                        tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
+                               accum);
+                    }
+                }
                 tc_commit(empty0 + 8 * stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
@@ -329,61 +368,93 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int L = blockIdx.x; L < total; L += gridDim.x) {
-            const TileCoord c = decode_tile(g, L, tiles, nk);
+            const TileCoord c = decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
             tc_fence_after();
-            const int row = c.m0 + quarter * 32 + lane;
-            const bool vrow = row < c.mend;
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
-            if (MODE == GEMM_UP_SWIGLU) {
+            if (G::SWAP) {
+                // TMEM lane = output feature f, column = token row m0 + j.
+                const int f = c.n0 + quarter * 32 + lane;
+                const bool vf = f < g.N;
+                const bool raw = MODE == GEMM_DOWN || g.k_splits > 1;
+                float *P = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
                 __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
 #pragma unroll 1
-                for (int cc = 0; cc < BNM / 2; cc += 16) {
-                    float gt[16], up[16];
-                    tmem_ld16(tbase + cc, gt);
-                    tmem_ld16(tbase + BNM / 2 + cc, up);
-                    tmem_ld_wait();
-                    float h[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) h[i] = silu(gt[i]) * up[i];
-                    const int col = c.n0 + cc;
-                    if (vrow) {
-                        __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
-                        if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(h);
-                        if (col + 8 < g.N) *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(h + 8);
-                    }
-                }
-            } else if (MODE == GEMM_UP_RELU) {
-                __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
-#pragma unroll 1
-                for (int cc = 0; cc < BNM; cc += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + cc, v);
+                for (int j0 = 0; j0 < NT; j0 += 16) {
+                    float a[16], b[16];
+                    tmem_ld16(tbase + j0, a);
+                    if (MODE == GEMM_UP_SWIGLU) tmem_ld16(tbase + NT + j0, b);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
-                    const int col = c.n0 + cc;
-                    if (vrow) {
-                        __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
-                        if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
-                        if (col + 8 < g.N) *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
+                    for (int i = 0; i < 16; ++i) {
+                        const int row = c.m0 + j0 + i;
+                        if (!vf || row >= c.mend) continue;
+                        if (raw) {
+                            float *dst = P + (size_t)row * g.ldc + f;
+                            dst[0] = a[i];
+                            if (MODE == GEMM_UP_SWIGLU) dst[g.N] = b[i];
+                        } else if (MODE == GEMM_UP_SWIGLU) {
+                            H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(silu(a[i]) * b[i]);
+                        } else {
+                            H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(fmaxf(a[i], 0.f));
+                        }
                     }
                 }
             } else {
-                float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
+                const int row = c.m0 + quarter * 32 + lane;
+                const bool vrow = row < c.mend;
+                if (MODE == GEMM_UP_SWIGLU) {
+                    __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
 #pragma unroll 1
-                for (int cc = 0; cc < BNM; cc += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + cc, v);
-                    tmem_ld_wait();
-                    const int col = c.n0 + cc;
-                    if (vrow) {
-                        float *dst = O + (size_t)row * g.ldc + col;
+                    for (int cc = 0; cc < BN / 2; cc += 16) {
+                        float gt[16], up[16];
+                        tmem_ld16(tbase + cc, gt);
+                        tmem_ld16(tbase + BN / 2 + cc, up);
+                        tmem_ld_wait();
+                        float h[16];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (col + 4 * q < g.N)
-                                *reinterpret_cast<float4 *>(dst + 4 * q) =
-                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        for (int i = 0; i < 16; ++i) h[i] = silu(gt[i]) * up[i];
+                        const int col = c.n0 + cc;
+                        if (vrow) {
+                            __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                            if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(h);
+                            if (col + 8 < g.N)
+                                *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(h + 8);
+                        }
+                    }
+                } else if (MODE == GEMM_UP_RELU) {
+                    __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+#pragma unroll 1
+                    for (int cc = 0; cc < BN; cc += 16) {
+                        float v[16];
+                        tmem_ld16(tbase + cc, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
+                        const int col = c.n0 + cc;
+                        if (vrow) {
+                            __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                            if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
+                            if (col + 8 < g.N)
+                                *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
+                        }
+                    }
+                } else {
+                    float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
+#pragma unroll 1
+                    for (int cc = 0; cc < BN; cc += 16) {
+                        float v[16];
+                        tmem_ld16(tbase + cc, v);
+                        tmem_ld_wait();
+                        const int col = c.n0 + cc;
+                        if (vrow) {
+                            float *dst = O + (size_t)row * g.ldc + col;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (col + 4 * q < g.N)
+                                    *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(
+                                        v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        }
                     }
                 }
             }
@@ -447,37 +518,75 @@ static int num_sms() {
     return n;
 }
 
+template <int MODE, int NT, int BN>
+static cudaError_t launch_geo(const CUtensorMap &mA, const CUtensorMap &mB0,
+                              const CUtensorMap &mB1, const Args &g, cudaStream_t st) {
+    using G = Geo<MODE, NT, BN>;
+    static_assert(G::SMEM <= (size_t)kSmemLimit, "shared memory");
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, NT, BN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)G::SMEM);
+    if (err != cudaSuccess) return err;
+    grouped_gemm_tc_kernel<MODE, NT, BN><<<num_sms(), 256, G::SMEM, st>>>(mA, mB0, mB1, g);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t launch_mode(int nt, int bn, const CUtensorMap &mA, const CUtensorMap &mB0,
+                               const CUtensorMap &mB1, const Args &g, cudaStream_t st) {
+    switch (nt) {
+        case 0:
+            return bn == BNM ? launch_geo<MODE, 0, BNM>(mA, mB0, mB1, g, st)
+                             : launch_geo<MODE, 0, BNM / 2>(mA, mB0, mB1, g, st);
+        case 16: return launch_geo<MODE, 16, BNM>(mA, mB0, mB1, g, st);
+        case 32: return launch_geo<MODE, 32, BNM>(mA, mB0, mB1, g, st);
+        case 64: return launch_geo<MODE, 64, BNM>(mA, mB0, mB1, g, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace tc
 
 // A [a_rows, a_cols], weights B0/B1 [E*b_rows, K]; tile table from
-// launch_build_tiles with BM = 128.  A's column for reduction index k is
-// k mod a_k_period (a_k_period = K: no wrap).  With k_splits > 1 (GEMM_DOWN
-// only) split s of every tile writes its partial sum to C + s * split_stride.
-cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, int a_cols, const void *B0,
-                           const void *B1, int E, int b_rows, int N, int K, int a_k_period,
-                           int k_splits, long long split_stride, const int32_t *tile_e,
-                           const int32_t *tile_start, const int32_t *n_mtiles,
-                           const int32_t *offsets, void *C, int ldc, cudaStream_t st) {
+// launch_build_tiles with row tiles of 128 (nt = 0) or nt rows (nt = 16, 32,
+// 64: weights on the MMA's M side).  bn (nt = 0 only): MMA N of 256 or 128;
+// 128 doubles the output tiles when there are too few to fill the SMs.  A's column for reduction index k is
+// k mod a_k_period (a_k_period = K: no wrap).  With k_splits > 1 split s of
+// every tile writes fp32 partial sums to C + s * split_stride: GEMM_DOWN
+// always (row-major [rows, ldc]); the up modes only with nt > 0, writing the
+// pre-activation sums (SwiGLU: W1 part at column f, W3 part at N + f).
+// k_splits = 1 up modes write the activation in bf16.
+cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_rows, int a_cols,
+                           const void *B0, const void *B1, int E, int b_rows, int N, int K,
+                           int a_k_period, int k_splits, long long split_stride,
+                           const int32_t *tile_e, const int32_t *tile_start,
+                           const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
+                           cudaStream_t st) {
     using namespace tc;
     if (a_rows == 0) return cudaSuccess;
     const int nk = (K + BK - 1) / BK;
-    if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN) ||
+    if (nt != 0 && nt != 16 && nt != 32 && nt != 64) return cudaErrorInvalidValue;
+    if (bn != BNM && bn != BNM / 2) return cudaErrorInvalidValue;
+    if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN && nt == 0) ||
         (a_k_period % BK != 0 && a_k_period != K))
         return cudaErrorInvalidValue;
     const int kbps = (nk + k_splits - 1) / k_splits;
     k_splits = (nk + kbps - 1) / kbps;          // every split gets at least one K block
+    const int rows = nt ? nt : BM;
     CUtensorMap mA, mB0, mB1;
-    if (!make_map(&mA, A, a_rows, a_cols, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&mB0, B0, (long long)E * b_rows, K, BNM / 2)) return cudaErrorInvalidValue;
-    if (!make_map(&mB1, B1 ? B1 : B0, (long long)E * b_rows, K, BNM / 2))
+    if (!make_map(&mA, A, a_rows, a_cols, rows)) return cudaErrorInvalidValue;
+    const int box = nt ? WROWS : bn / 2;
+    if (!make_map(&mB0, B0, (long long)E * b_rows, K, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mB1, B1 ? B1 : B0, (long long)E * b_rows, K, box))
         return cudaErrorInvalidValue;
+    const int outc = nt ? WROWS : (mode == GEMM_UP_SWIGLU ? bn / 2 : bn);
     Args g;
     g.mode = mode;
     g.N = N;
     g.K = K;
     g.a_k_period = a_k_period;
-    g.n_ntiles = (N + (mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM) - 1) /
-                 (mode == GEMM_UP_SWIGLU ? BNM / 2 : BNM);
+    g.n_ntiles = (N + outc - 1) / outc;
     g.b_rows = b_rows;
     g.k_splits = k_splits;
     g.kb_per_split = kbps;
@@ -488,28 +597,9 @@ cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, int a_cols
     g.offsets = offsets;
     g.C = C;
     g.ldc = ldc;
-    const size_t smem = smem_bytes();
-    cudaError_t err;
-    if (mode == GEMM_UP_SWIGLU) {
-        err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<GEMM_UP_SWIGLU>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        grouped_gemm_tc_kernel<GEMM_UP_SWIGLU><<<num_sms(), 256, smem, st>>>(mA, mB0, mB1, g);
-        note_launch();
-    } else if (mode == GEMM_UP_RELU) {
-        err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<GEMM_UP_RELU>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        grouped_gemm_tc_kernel<GEMM_UP_RELU><<<num_sms(), 256, smem, st>>>(mA, mB0, mB1, g);
-        note_launch();
-    } else {
-        err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<GEMM_DOWN>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        grouped_gemm_tc_kernel<GEMM_DOWN><<<num_sms(), 256, smem, st>>>(mA, mB0, mB1, g);
-        note_launch();
-    }
-    return cudaGetLastError();
+    if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, mA, mB0, mB1, g, st);
+    if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, mA, mB0, mB1, g, st);
+    return launch_mode<GEMM_DOWN>(nt, bn, mA, mB0, mB1, g, st);
 }
 
 }  // namespace moe

@@ -16,18 +16,28 @@ struct RouterArgs {
     int T, d, E, k, select_space, do_select;
     int32_t *idx;
     float *w, *probs, *probsT, *p_partial;
+    float *ent_partial;   // per-block sums of the tokens' gate entropies, or NULL
+    int n_cand;           // experts ranked after the top k to report (0: none)
+    int32_t *cand_idx;    // [T, n_cand] next-best experts, descending score
+    float *cand_w;        // [T, n_cand] their probability over the top-k sum
 };
 
 // router.cu
-int router_blocks(int T, int E);
+// E <= 32: the logits are computed in slices of kRouterSlice columns of d,
+// written as partial planes [slices][T][E] (caller's buffer) and added in
+// slice order by the softmax kernel.
+constexpr int kRouterSlice = 512;
+inline int router_slices(int d) { return (d + kRouterSlice - 1) / kRouterSlice; }
+int router_blocks(int T, int E, int dtype);
 size_t router_smem_bytes(int E, int dtype);
-cudaError_t launch_router(const RouterArgs &a, int dtype, cudaStream_t st);
+cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStream_t st);
 cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp,
                                        __nv_bfloat16 *out, cudaStream_t st);
 cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, int S,
                                       cudaStream_t st);
-cudaError_t launch_select_from_probsT(const float *probsT, const float *bias, int T, int E,
-                                      int k, int32_t *idx, float *w, cudaStream_t st);
+cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int E, int k,
+                               int32_t *idx, float *w, cudaStream_t st, int n_cand = 0,
+                               int32_t *cand_idx = nullptr, float *cand_w = nullptr);
 cudaError_t launch_quantile_bias(const float *probsT, int T, int E, long long lo, float frac,
                                  float *bias_out, cudaStream_t st);
 
@@ -41,20 +51,78 @@ cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long 
 cudaError_t launch_histogram(const int32_t *idx, long long n, int E, int32_t *hist,
                              int32_t *counts, cudaStream_t st);
 
+// reroute.cu: capacity overflow redirected to the next-best experts.
+struct RerouteWork {             // device scratch
+    int32_t *slot_e;             // [T*k] current target expert of each slot (-1: none)
+    float *slot_w;               // [T*k] its gate weight
+    int32_t *served;             // [T*k] rank in the serving expert's rows, -1 if unserved
+    int32_t *nxt;                // [T] next unused candidate of each token
+    int32_t *filled, *filled_before;   // [E]
+    int32_t *hist, *block_base;  // [chunks][E]
+};
+cudaError_t launch_dispatch_reroute(const int32_t *topk_idx, const float *topk_w,
+                                    const int32_t *cand_idx, const float *cand_w, int n_cand,
+                                    long long T, int k, int E, long long C, int rounds,
+                                    const RerouteWork &w, int32_t *counts, int32_t *offsets,
+                                    int32_t *perm, int32_t *inv, int32_t *slot_expert,
+                                    float *slot_w_out, int32_t *n_dropped, cudaStream_t st);
+
 // misc.cu
 cudaError_t launch_p_finalize(const float *p_partial, int nblk, int E, int T, float *p,
                               cudaStream_t st);
 cudaError_t launch_prob_partials(const float *probs, int T, int E, float *p_partial,
                                  cudaStream_t st);
+// Optional observability outputs of stats_finalize (any pointer may be NULL).
+struct ObsArgs {
+    const int32_t *n_dropped;   // in: dropped assignments
+    const float *bias;          // in: selection bias in effect [E]
+    float *drop_ratio, *bias_mean_abs, *bias_max_abs;
+};
 cudaError_t launch_stats_finalize(const int32_t *counts, const float *p, int T, int E, int k,
                                   float *f, float *p_out, float *aux, float *load,
-                                  cudaStream_t st);
+                                  cudaStream_t st, const ObsArgs &o = ObsArgs{});
+cudaError_t launch_entropy_partials(const float *probs, int T, int E, float *ent_partial,
+                                    cudaStream_t st);
+// Expert output scale over the dispatched rows of `planes` fp32 planes:
+// row statistics into rs [max_rows][3] (fp64), then per expert mean, std and
+// max |o| (each output pointer may be NULL).
+cudaError_t launch_expert_scale(const float *P, int planes, long long plane, int d,
+                                const int32_t *offsets, int E, long long max_rows, double *rs,
+                                float *mean, float *std_, float *maxabs, cudaStream_t st);
 cudaError_t launch_gather_rows(const void *x, int elem_bytes, int d, const int32_t *perm,
                                const int32_t *offsets_end, int k, long long max_rows, void *xs,
                                cudaStream_t st);
-cudaError_t launch_combine(const float *out_sorted, const int32_t *inv, const float *w,
-                           const float *shared_out, int T, int k, int d, int out_dtype, void *y,
-                           cudaStream_t st);
+// out_sorted and shared_out may hold several fp32 planes (partial sums of a
+// split reduction), `planes` / `sh_planes` of them `plane` / `sh_plane`
+// elements apart; they are added in plane order.
+cudaError_t launch_combine(const float *out_sorted, int planes, long long plane,
+                           const int32_t *inv, const float *w, const float *shared_out,
+                           int sh_planes, long long sh_plane, int T, int k, int d,
+                           int out_dtype, void *y, cudaStream_t st);
+cudaError_t launch_combine_rows(const float *out_sorted, int planes, long long plane,
+                                const int32_t *tok_start, const int32_t *tok_rows,
+                                const float *row_w, const float *shared_out, int sh_planes,
+                                long long sh_plane, int T, int d, int out_dtype, void *y,
+                                cudaStream_t st);
+// expert_choice.cu: each expert takes its top-Cn tokens by probability from
+// probsT [E, T]; rows of expert e are [e*Cn, (e+1)*Cn) in token order.
+// rowidx [E][T] (row or -1), per-token row lists tok_start [T+1], tok_rows.
+cudaError_t launch_expert_choice(const float *probsT, int T, int E, int Cn, int32_t *perm,
+                                 float *row_w, int32_t *rowidx, int32_t *counts,
+                                 int32_t *offsets, int32_t *tok_cnt, int32_t *tok_start,
+                                 int32_t *tok_rows, int32_t *n_unchosen, cudaStream_t st);
+cudaError_t launch_slot_outputs(const int32_t *idx, const float *w, const int32_t *inv,
+                                long long n, int32_t *slot_expert, float *slot_w,
+                                cudaStream_t st);
+// h[r] = act(sum_s P_s[r]) in bf16 for rows r < *rows_end of the split
+// partial sums of an up projection (SwiGLU: W1 part at f, W3 part at N + f).
+cudaError_t launch_split_activation(const float *P, int splits, long long plane, int N,
+                                    int swiglu, const int32_t *rows_end, long long max_rows,
+                                    __nv_bfloat16 *h, cudaStream_t st);
+// out[r] = sum_s P_s[r] (fp32) for rows r < *rows_end.
+cudaError_t launch_sum_planes(const float *P, int splits, long long plane, int d,
+                              const int32_t *rows_end, long long max_rows, float *out,
+                              cudaStream_t st);
 cudaError_t launch_build_tiles(const int32_t *offsets, int E, int BM, int32_t *tile_e,
                                int32_t *tile_m0, int32_t *tile_start, int32_t *n_tiles,
                                cudaStream_t st);
@@ -79,10 +147,11 @@ cudaError_t launch_simt_gemm(const GroupedGemmArgs &g, int mode, int dtype, cuda
 
 // gemm_tcgen05.cu: tcgen05/TMEM grouped GEMM for the bf16 workloads.
 constexpr int kTcBM = 128;
-cudaError_t launch_tc_gemm(int mode, const void *A, long long a_rows, int a_cols, const void *B0,
-                           const void *B1, int E, int b_rows, int N, int K, int a_k_period,
-                           int k_splits, long long split_stride, const int32_t *tile_e,
-                           const int32_t *tile_start, const int32_t *n_mtiles,
-                           const int32_t *offsets, void *C, int ldc, cudaStream_t st);
+cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_rows, int a_cols,
+                           const void *B0, const void *B1, int E, int b_rows, int N, int K,
+                           int a_k_period, int k_splits, long long split_stride,
+                           const int32_t *tile_e, const int32_t *tile_start,
+                           const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
+                           cudaStream_t st);
 
 }  // namespace moe

@@ -11,6 +11,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
+
 namespace moe {
 
 // Fixed-order tree reduction of one double per thread over a 256-thread block;
@@ -66,44 +68,178 @@ cudaError_t launch_prob_partials(const float *probs, int T, int E, float *p_part
 
 // f_e = count_e / (T k); aux = E * sum_e f_e p_e (fp64, fixed tree order);
 // load = max_e count_e / (T k / E).  One CTA of 1024 threads, E <= 1024.
+// Optional observability outputs (ObsArgs): drop_ratio = n_dropped / (T k);
+// bias_mean_abs, bias_max_abs = mean and max |b_e| of the selection bias in
+// effect (0 without one).
 __global__ void __launch_bounds__(1024) stats_finalize_kernel(const int32_t *counts,
                                                               const float *p, int T, int E,
                                                               int k, float *f, float *p_out,
-                                                              float *aux, float *load) {
+                                                              float *aux, float *load,
+                                                              ObsArgs o) {
     __shared__ double red[1024];
+    __shared__ double redb[1024];
+    __shared__ float redbm[1024];
     __shared__ int redmax[1024];
     const int e = threadIdx.x;
     const double tk = (double)T * (double)k;
     double fp = 0.0;
     int c = 0;
+    float b = 0.f;
     if (e < E) {
-        c = counts[e];
+        c = counts ? counts[e] : 0;
         const double fe = tk > 0 ? (double)c / tk : 0.0;
         if (f) f[e] = (float)fe;
-        if (p_out && p_out != p) p_out[e] = p[e];
-        fp = fe * (double)p[e];
+        if (p && p_out && p_out != p) p_out[e] = p[e];
+        fp = p ? fe * (double)p[e] : 0.0;
+        if (o.bias) b = fabsf(o.bias[e]);
     }
     red[e] = fp;
     redmax[e] = c;
+    redb[e] = b;
+    redbm[e] = b;
     __syncthreads();
 #pragma unroll
     for (int off = 512; off >= 1; off >>= 1) {
         if (e < off) {
             red[e] += red[e + off];
             redmax[e] = max(redmax[e], redmax[e + off]);
+            redb[e] += redb[e + off];
+            redbm[e] = fmaxf(redbm[e], redbm[e + off]);
         }
         __syncthreads();
     }
     if (e == 0) {
         if (aux) *aux = (float)((double)E * red[0]);
         if (load) *load = tk > 0 ? (float)((double)redmax[0] / (tk / (double)E)) : 0.f;
+        if (o.drop_ratio)
+            *o.drop_ratio = (o.n_dropped && tk > 0) ? (float)((double)*o.n_dropped / tk) : 0.f;
+        if (o.bias_mean_abs) *o.bias_mean_abs = (float)(redb[0] / (double)E);
+        if (o.bias_max_abs) *o.bias_max_abs = redbm[0];
     }
 }
 
 cudaError_t launch_stats_finalize(const int32_t *counts, const float *p, int T, int E, int k,
                                   float *f, float *p_out, float *aux, float *load,
-                                  cudaStream_t st) {
-    stats_finalize_kernel<<<1, 1024, 0, st>>>(counts, p, T, E, k, f, p_out, aux, load);
+                                  cudaStream_t st, const ObsArgs &o) {
+    stats_finalize_kernel<<<1, 1024, 0, st>>>(counts, p, T, E, k, f, p_out, aux, load, o);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Per-block sums of the tokens' gate entropies -sum_e p ln p from stored
+// probabilities [T, E] (terms with p = 0 contribute 0): 32 tokens per block,
+// warp w owns tokens 4w..4w+3, fixed reduction order.
+__global__ void __launch_bounds__(256) entropy_partials_kernel(const float *probs, int T, int E,
+                                                               float *ent_partial) {
+    __shared__ float st_h[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = 0; r < 4; ++r) {
+        const int tt = 4 * warp + r, t = blockIdx.x * 32 + tt;
+        float h = 0.f;
+        if (t < T)
+            for (int e = lane; e < E; e += 32) {
+                const float pv = probs[(size_t)t * E + e];
+                if (pv > 0.f) h -= pv * logf(pv);
+            }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) h += __shfl_xor_sync(0xffffffffu, h, off);
+        if (lane == 0) st_h[tt] = h;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int tt = 0; tt < 32; ++tt) tot += st_h[tt];
+        ent_partial[blockIdx.x] = tot;
+    }
+}
+
+cudaError_t launch_entropy_partials(const float *probs, int T, int E, float *ent_partial,
+                                    cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    entropy_partials_kernel<<<(T + 31) / 32, 256, 0, st>>>(probs, T, E, ent_partial);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Per sorted row r < *rows_end of the expert outputs (the sum of `planes`
+// fp32 planes, in plane order): sum, sum of squares (fp64) and max |o|.
+// One warp per row; lane-strided partial sums, fixed butterfly.
+__global__ void __launch_bounds__(256) row_stats_kernel(const float *P, int planes,
+                                                        long long plane, int d,
+                                                        const int32_t *rows_end,
+                                                        long long max_rows, double *rs) {
+    const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= max_rows || r >= *rows_end) return;
+    double s1 = 0.0, s2 = 0.0;
+    float mx = 0.f;
+    const float *row = P + r * d;
+    for (int c = lane; c < d; c += 32) {
+        float v = row[c];
+        for (int sp = 1; sp < planes; ++sp) v += row[sp * plane + c];
+        s1 += v;
+        s2 += (double)v * v;
+        mx = fmaxf(mx, fabsf(v));
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (lane == 0) {
+        rs[3 * r] = s1;
+        rs[3 * r + 1] = s2;
+        rs[3 * r + 2] = mx;
+    }
+}
+
+// Per expert e over its rows [offsets[e], offsets[e+1]) of row_stats: mean,
+// population standard deviation and max |o| over all n_e * d elements.
+__global__ void __launch_bounds__(256) expert_scale_kernel(const double *rs,
+                                                           const int32_t *offsets, int d,
+                                                           float *mean, float *std_,
+                                                           float *maxabs) {
+    __shared__ double red[256];
+    __shared__ float redm[256];
+    const int e = blockIdx.x;
+    const int a = offsets[e], b = offsets[e + 1];
+    double s1 = 0.0, s2 = 0.0;
+    float mx = 0.f;
+    for (int r = a + threadIdx.x; r < b; r += 256) {
+        s1 += rs[3 * (size_t)r];
+        s2 += rs[3 * (size_t)r + 1];
+        mx = fmaxf(mx, (float)rs[3 * (size_t)r + 2]);
+    }
+    s1 = block_sum_256(s1, red);
+    __syncthreads();
+    s2 = block_sum_256(s2, red);
+    redm[threadIdx.x] = mx;
+    __syncthreads();
+    for (int off = 128; off >= 1; off >>= 1) {
+        if (threadIdx.x < off) redm[threadIdx.x] = fmaxf(redm[threadIdx.x], redm[threadIdx.x + off]);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double n = (double)(b - a) * (double)d;
+        const double mu = n > 0 ? s1 / n : 0.0;
+        const double var = n > 0 ? fmax(s2 / n - mu * mu, 0.0) : 0.0;
+        if (mean) mean[e] = (float)mu;
+        if (std_) std_[e] = (float)sqrt(var);
+        if (maxabs) maxabs[e] = redm[0];
+    }
+}
+
+cudaError_t launch_expert_scale(const float *P, int planes, long long plane, int d,
+                                const int32_t *offsets, int E, long long max_rows, double *rs,
+                                float *mean, float *std_, float *maxabs, cudaStream_t st) {
+    if (max_rows > 0) {
+        row_stats_kernel<<<(unsigned)((max_rows + 7) / 8), 256, 0, st>>>(P, planes, plane, d,
+                                                                         offsets + E, max_rows,
+                                                                         rs);
+        note_launch();
+    }
+    expert_scale_kernel<<<E, 256, 0, st>>>(rs, offsets, d, mean, std_, maxabs);
     note_launch();
     return cudaGetLastError();
 }
@@ -134,10 +270,23 @@ cudaError_t launch_gather_rows(const void *x, int elem_bytes, int d, const int32
     return cudaGetLastError();
 }
 
-// y[t] = sum_j [inv >= 0] w[t,j] out_sorted[inv[t,j]] (j in order) + shared[t].
+// y[t] = sum_j [inv >= 0] w[t,j] o[inv[t,j]] (j in order) + s[t], where
+// o = sum of the out_sorted planes and s = sum of the shared planes, each in
+// plane order.
+__device__ __forceinline__ float4 sum_planes4(const float4 *p, int planes, long long plane4,
+                                              long long i) {
+    float4 o = p[i];
+    for (int s = 1; s < planes; ++s) {
+        const float4 q = p[s * plane4 + i];
+        o.x += q.x; o.y += q.y; o.z += q.z; o.w += q.w;
+    }
+    return o;
+}
+
 template <typename TO>
-__global__ void combine_kernel(const float4 *out_sorted, const int32_t *inv, const float *w,
-                               const float4 *shared_out, int k, int d4, TO *y) {
+__global__ void combine_kernel(const float4 *out_sorted, int planes, long long plane4,
+                               const int32_t *inv, const float *w, const float4 *shared_out,
+                               int sh_planes, long long sh_plane4, int k, int d4, TO *y) {
     const long long t = blockIdx.x;
     for (int c = threadIdx.x; c < d4; c += blockDim.x) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -145,12 +294,12 @@ __global__ void combine_kernel(const float4 *out_sorted, const int32_t *inv, con
             const int s = inv[t * k + j];
             if (s < 0) continue;
             const float wj = w[t * k + j];
-            const float4 o = out_sorted[(long long)s * d4 + c];
+            const float4 o = sum_planes4(out_sorted, planes, plane4, (long long)s * d4 + c);
             acc.x = fmaf(wj, o.x, acc.x); acc.y = fmaf(wj, o.y, acc.y);
             acc.z = fmaf(wj, o.z, acc.z); acc.w = fmaf(wj, o.w, acc.w);
         }
         if (shared_out) {
-            const float4 sv = shared_out[t * d4 + c];
+            const float4 sv = sum_planes4(shared_out, sh_planes, sh_plane4, t * d4 + c);
             acc.x += sv.x; acc.y += sv.y; acc.z += sv.z; acc.w += sv.w;
         }
         if constexpr (sizeof(TO) == 4) {
@@ -166,21 +315,181 @@ __global__ void combine_kernel(const float4 *out_sorted, const int32_t *inv, con
     }
 }
 
-cudaError_t launch_combine(const float *out_sorted, const int32_t *inv, const float *w,
-                           const float *shared_out, int T, int k, int d, int out_dtype, void *y,
-                           cudaStream_t st) {
+cudaError_t launch_combine(const float *out_sorted, int planes, long long plane,
+                           const int32_t *inv, const float *w, const float *shared_out,
+                           int sh_planes, long long sh_plane, int T, int k, int d,
+                           int out_dtype, void *y, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int d4 = d / 4;
     const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
+    const float4 *o4 = reinterpret_cast<const float4 *>(out_sorted);
+    const float4 *s4 = reinterpret_cast<const float4 *>(shared_out);
     if (out_dtype == MOE_DTYPE_FP32)
-        combine_kernel<float><<<T, threads, 0, st>>>(
-            reinterpret_cast<const float4 *>(out_sorted), inv, w,
-            reinterpret_cast<const float4 *>(shared_out), k, d4, static_cast<float *>(y));
+        combine_kernel<float><<<T, threads, 0, st>>>(o4, planes, plane / 4, inv, w, s4,
+                                                     sh_planes, sh_plane / 4, k, d4,
+                                                     static_cast<float *>(y));
     else
         combine_kernel<__nv_bfloat16><<<T, threads, 0, st>>>(
-            reinterpret_cast<const float4 *>(out_sorted), inv, w,
-            reinterpret_cast<const float4 *>(shared_out), k, d4,
+            o4, planes, plane / 4, inv, w, s4, sh_planes, sh_plane / 4, k, d4,
             static_cast<__nv_bfloat16 *>(y));
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Combine over a per-token row list (expert choice): y[t] = sum over
+// i in [tok_start[t], tok_start[t+1]) of row_w[r_i] o[r_i] (list order) +
+// s[t], o and s summed over their planes in plane order.
+template <typename TO>
+__global__ void combine_rows_kernel(const float4 *out_sorted, int planes, long long plane4,
+                                    const int32_t *tok_start, const int32_t *tok_rows,
+                                    const float *row_w, const float4 *shared_out, int sh_planes,
+                                    long long sh_plane4, int d4, TO *y) {
+    const long long t = blockIdx.x;
+    const int a = tok_start[t], b = tok_start[t + 1];
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = a; i < b; ++i) {
+            const int r = tok_rows[i];
+            const float wr = row_w[r];
+            const float4 o = sum_planes4(out_sorted, planes, plane4, (long long)r * d4 + c);
+            acc.x = fmaf(wr, o.x, acc.x); acc.y = fmaf(wr, o.y, acc.y);
+            acc.z = fmaf(wr, o.z, acc.z); acc.w = fmaf(wr, o.w, acc.w);
+        }
+        if (shared_out) {
+            const float4 sv = sum_planes4(shared_out, sh_planes, sh_plane4, t * d4 + c);
+            acc.x += sv.x; acc.y += sv.y; acc.z += sv.z; acc.w += sv.w;
+        }
+        if constexpr (sizeof(TO) == 4) {
+            reinterpret_cast<float4 *>(y)[t * d4 + c] = acc;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(y)[t * d4 + c] = u;
+        }
+    }
+}
+
+cudaError_t launch_combine_rows(const float *out_sorted, int planes, long long plane,
+                                const int32_t *tok_start, const int32_t *tok_rows,
+                                const float *row_w, const float *shared_out, int sh_planes,
+                                long long sh_plane, int T, int d, int out_dtype, void *y,
+                                cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int d4 = d / 4;
+    const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
+    const float4 *o4 = reinterpret_cast<const float4 *>(out_sorted);
+    const float4 *s4 = reinterpret_cast<const float4 *>(shared_out);
+    if (out_dtype == MOE_DTYPE_FP32)
+        combine_rows_kernel<float><<<T, threads, 0, st>>>(o4, planes, plane / 4, tok_start,
+                                                          tok_rows, row_w, s4, sh_planes,
+                                                          sh_plane / 4, d4,
+                                                          static_cast<float *>(y));
+    else
+        combine_rows_kernel<__nv_bfloat16><<<T, threads, 0, st>>>(
+            o4, planes, plane / 4, tok_start, tok_rows, row_w, s4, sh_planes, sh_plane / 4, d4,
+            static_cast<__nv_bfloat16 *>(y));
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Per-slot result of the plain capacity rule: the slot's expert and gate
+// weight, or -1 and 0 when it was dropped.
+__global__ void slot_outputs_kernel(const int32_t *idx, const float *w, const int32_t *inv,
+                                    long long n, int32_t *slot_expert, float *slot_w) {
+    for (long long f = blockIdx.x * (long long)blockDim.x + threadIdx.x; f < n;
+         f += (long long)gridDim.x * blockDim.x) {
+        const bool kept = inv[f] >= 0;
+        if (slot_expert) slot_expert[f] = kept ? idx[f] : -1;
+        if (slot_w) slot_w[f] = kept ? w[f] : 0.f;
+    }
+}
+
+cudaError_t launch_slot_outputs(const int32_t *idx, const float *w, const int32_t *inv,
+                                long long n, int32_t *slot_expert, float *slot_w,
+                                cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int grid = (int)std::min<long long>((n + 255) / 256, 148 * 8);
+    slot_outputs_kernel<<<grid, 256, 0, st>>>(idx, w, inv, n, slot_expert, slot_w);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Activation of split up-projection partial sums: one thread per 8 features
+// of one row; the splits are added in order.
+template <bool SWIGLU>
+__global__ void split_activation_kernel(const float *P, int splits, long long plane, int N,
+                                        const int32_t *rows_end, long long max_rows,
+                                        __nv_bfloat16 *h) {
+    const int n8 = N / 8;
+    const long long ldp = SWIGLU ? 2ll * N : (long long)N;
+    const long long rows = min((long long)*rows_end, max_rows);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < rows * n8;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / n8;
+        const int f = (int)(i - r * n8) * 8;
+        float a[8], b[8];
+        const float *p = P + r * ldp + f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) { a[q] = p[q]; b[q] = SWIGLU ? p[N + q] : 0.f; }
+        for (int s = 1; s < splits; ++s) {
+            const float *ps = p + s * plane;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                a[q] += ps[q];
+                if (SWIGLU) b[q] += ps[N + q];
+            }
+        }
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = SWIGLU ? silu(a[q]) * b[q] : fmaxf(a[q], 0.f);
+        uint4 u;
+        uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+            wv[q] = *reinterpret_cast<uint32_t *>(&pr);
+        }
+        *reinterpret_cast<uint4 *>(h + r * N + f) = u;
+    }
+}
+
+cudaError_t launch_split_activation(const float *P, int splits, long long plane, int N,
+                                    int swiglu, const int32_t *rows_end, long long max_rows,
+                                    __nv_bfloat16 *h, cudaStream_t st) {
+    if (max_rows == 0) return cudaSuccess;
+    const long long work = max_rows * (N / 8);
+    const int grid = (int)std::min<long long>((work + 255) / 256, 148 * 8);
+    if (swiglu)
+        split_activation_kernel<true><<<grid, 256, 0, st>>>(P, splits, plane, N, rows_end,
+                                                            max_rows, h);
+    else
+        split_activation_kernel<false><<<grid, 256, 0, st>>>(P, splits, plane, N, rows_end,
+                                                             max_rows, h);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// out[r] = sum_s P_s[r] for rows r < *rows_end (fp32, split order).
+__global__ void sum_planes_kernel(const float4 *P, int splits, long long plane4, int d4,
+                                  const int32_t *rows_end, long long max_rows, float4 *out) {
+    const long long rows = min((long long)*rows_end, max_rows);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < rows * d4;
+         i += (long long)gridDim.x * blockDim.x)
+        out[i] = sum_planes4(P, splits, plane4, i);
+}
+
+cudaError_t launch_sum_planes(const float *P, int splits, long long plane, int d,
+                              const int32_t *rows_end, long long max_rows, float *out,
+                              cudaStream_t st) {
+    if (max_rows == 0) return cudaSuccess;
+    const long long work = max_rows * (d / 4);
+    const int grid = (int)std::min<long long>((work + 255) / 256, 148 * 8);
+    sum_planes_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4 *>(P), splits,
+                                            plane / 4, d / 4, rows_end, max_rows,
+                                            reinterpret_cast<float4 *>(out));
     note_launch();
     return cudaGetLastError();
 }

@@ -9,6 +9,8 @@
 
 #include "router.cu"
 #include "dispatch.cu"
+#include "reroute.cu"
+#include "expert_choice.cu"
 #include "misc.cu"
 #include "ffn_simt.cu"
 #include "gemm_tcgen05.cu"
@@ -35,17 +37,37 @@ struct Layout {
     size_t p_partial, probsT, hist, block_base, idx, w, counts, offsets, perm, inv, ndrop,
         pvec, sbias, idx_unb, tile_e, tile_m0, tile_start, ntiles, sh_offsets, sh_tile_e,
         sh_tile_m0, sh_tile_start, sh_ntiles, xs, h, out_sorted, sh_h, sh_out, rt_wsplit,
-        rt_logits, rt_offsets, rt_tile_e, rt_tile_start, rt_ntiles, total;
+        rt_logits, rt_offsets, rt_tile_e, rt_tile_start, rt_ntiles, up_part, sh_up_part,
+        ent_partial, row_stats, cand_idx, cand_w, rr_slot_e, rr_slot_w, rr_served, rr_nxt,
+        rr_filled, rr_filled_before, slot_w, ec_row_w, ec_rowidx, ec_tok_cnt, ec_tok_start,
+        ec_tok_rows, probs_rows, total;
 };
 
+long long capacity_of(const moe_config *c) {
+    const long long Tk = (long long)c->T * c->top_k;
+    if (!(c->capacity_factor > 0.f)) return Tk;
+    return (long long)ceil((double)c->capacity_factor * (double)c->T * (double)c->top_k /
+                           (double)c->n_experts);
+}
+
+bool expert_choice(const moe_config *c) { return c->routing == MOE_ROUTING_EXPERT_CHOICE; }
+
+// Rows each expert takes under expert choice: min(C, T).
+long long ec_rows_per_expert(const moe_config *c) {
+    return std::min<long long>(capacity_of(c), c->T);
+}
+
+// Tk: token-choice slots (T*k).  R: rows of the grouped layout, at most Tk
+// for token choice, E * min(C, T) for expert choice.
 struct Sizes {
-    long long T, d, E, k, F, Fs, Tk;
+    long long T, d, E, k, F, Fs, Tk, R;
 };
 
 Sizes sizes(const moe_config *c) {
     Sizes s;
     s.T = c->T; s.d = c->d_model; s.E = c->n_experts; s.k = c->top_k; s.F = c->d_ff;
     s.Fs = c->d_ff_shared; s.Tk = s.T * s.k;
+    s.R = expert_choice(c) ? s.E * ec_rows_per_expert(c) : s.Tk;
     return s;
 }
 
@@ -55,30 +77,87 @@ Sizes sizes(const moe_config *c) {
 // B300: logit error up to 1.3e-4 over one 192-block chain, 1e-5 over chains of
 // about 20 blocks, where the fp32 CUDA-core router reaches 1.4e-5), so the
 // reduction is cut into S chains of at most 16 K blocks, each written as an
-// fp32 partial plane and summed in fixed order by the softmax kernel.  Small T
-// uses more, shorter chains to fill the SMs.
+// fp32 partial plane and summed in fixed order.  S depends on d only, so a
+// token's logits do not depend on the batch it comes in (batch invariance).
 bool tc_router(const moe_config *c) {
     return c->dtype == MOE_DTYPE_BF16 && c->n_experts > 32 && c->n_experts % 4 == 0;
 }
 long long router_dp(const moe_config *c) { return (c->d_model + 63) / 64 * 64; }
 constexpr int kRouterChainBlocks = 16;
 int router_splits(const moe_config *c) {
-    const long long tiles = ((long long)c->T + 127) / 128 * ((c->n_experts + 255) / 256);
     const long long nk = 3 * router_dp(c) / 64;
-    long long S = (nk + kRouterChainBlocks - 1) / kRouterChainBlocks;
-    if (tiles > 0) S = std::max<long long>(S, std::min<long long>((296 + tiles - 1) / tiles,
-                                                                    std::max<long long>(1, nk / 4)));
+    const long long S = (nk + kRouterChainBlocks - 1) / kRouterChainBlocks;
     const long long kbps = (nk + S - 1) / S;
     return (int)((nk + kbps - 1) / kbps);
+}
+// How the grouped GEMMs of one expert FFN run.  nt = 0: 128 token rows per
+// tile on the MMA's M side.  nt = 16/32/64: weights on the M side and nt
+// token rows per tile, for a few rows per expert, where the layer streams
+// weights from HBM and a 128-row token tile would be mostly padding.  With
+// few tiles the reduction is split (s_up, s_down) so that every SM streams
+// weights; the splits' fp32 partial sums are added in split order later.
+struct FfnPlan {
+    int nt, s_up, s_down;
+    int bn_up, bn_down;     // nt = 0: MMA N (256, or 128 when tiles are few)
+};
+constexpr int kPlanSMs = 148;   // SM count the split choice assumes (B300)
+
+int split_count(long long tiles, long long nk) {
+    if (tiles <= 0 || nk <= 0) return 1;
+    long long S = (2 * kPlanSMs + tiles - 1) / tiles;
+    S = std::min<long long>(S, std::min<long long>(16, std::max<long long>(1, nk / 8)));
+    const long long kbps = (nk + S - 1) / S;
+    return (int)((nk + kbps - 1) / kbps);
+}
+
+// rows: dispatched rows (T*k routed, T shared); groups: experts; K = d.
+FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long long F,
+                 bool swiglu) {
+    FfnPlan p{0, 1, 1, 256, 256};
+    if (c->dtype != MOE_DTYPE_BF16 || rows <= 0 || F <= 0) return p;
+    const long long d = c->d_model;
+    const long long active = std::min(groups, rows);
+    const long long per = (rows + active - 1) / active;
+    const long long up_cols = swiglu ? 128 : 256;
+    const long long normal_items = active * ((per + 127) / 128) * ((F + up_cols - 1) / up_cols);
+    if (per <= 16) p.nt = 16;
+    else if (per <= 32) p.nt = 32;
+    else if (per <= 64 || (per <= 256 && normal_items < kPlanSMs)) p.nt = 64;
+    else {
+        // 128-row tiles; halve the MMA N when there are too few output tiles
+        const long long mt = (rows + 127) / 128 + active;
+        if (mt * ((F + up_cols - 1) / up_cols) < 2 * kPlanSMs) p.bn_up = 128;
+        if (mt * ((d + 255) / 256) < 2 * kPlanSMs) p.bn_down = 128;
+        return p;
+    }
+    const long long ttiles = active * ((per + p.nt - 1) / p.nt);
+    p.s_up = split_count(ttiles * ((F + 127) / 128), (d + 63) / 64);
+    p.s_down = split_count(ttiles * ((d + 127) / 128), (F + 63) / 64);
+    return p;
+}
+FfnPlan routed_plan(const moe_config *c) {
+    return ffn_plan(c, sizes(c).R, c->n_experts, c->d_ff, c->act == MOE_ACT_SWIGLU);
+}
+FfnPlan shared_plan(const moe_config *c) {
+    return ffn_plan(c, c->T, 1, c->d_ff_shared, true);
+}
+
+// Experts ranked after the top k that the router reports for redirected
+// overflow: each round gives every unserved slot one more candidate.
+long long n_candidates(const moe_config *c) {
+    if (c->reroute_rounds <= 0) return 0;
+    return std::min<long long>((long long)c->n_experts - c->top_k,
+                               (long long)c->top_k * c->reroute_rounds);
 }
 
 Layout layout(const moe_config *c) {
     const Sizes s = sizes(c);
     const size_t eb = elem_bytes(c->dtype);
-    const long long rb = router_blocks((int)s.T, (int)s.E);
+    const long long rb = router_blocks((int)s.T, (int)s.E, c->dtype);
     const long long nb = dispatch_blocks(s.Tk);
-    const long long mt = max_tiles(s.Tk, (int)s.E, kSimtBM);
-    const long long mts = max_tiles(s.T, 1, kSimtBM);
+    const FfnPlan rp = routed_plan(c), sp = shared_plan(c);
+    const long long mt = max_tiles(s.R, (int)s.E, std::min(kSimtBM, rp.nt ? rp.nt : kSimtBM));
+    const long long mts = max_tiles(s.T, 1, std::min(kSimtBM, sp.nt ? sp.nt : kSimtBM));
     Layout L;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes); return r; };
@@ -90,7 +169,7 @@ Layout layout(const moe_config *c) {
     L.w = take(sizeof(float) * s.Tk);
     L.counts = take(sizeof(int32_t) * s.E);
     L.offsets = take(sizeof(int32_t) * (s.E + 1));
-    L.perm = take(sizeof(int32_t) * s.Tk);
+    L.perm = take(sizeof(int32_t) * s.R);
     L.inv = take(sizeof(int32_t) * s.Tk);
     L.ndrop = take(sizeof(int32_t));
     L.pvec = take(sizeof(float) * s.E);
@@ -105,18 +184,43 @@ Layout layout(const moe_config *c) {
     L.sh_tile_m0 = take(sizeof(int32_t) * mts);
     L.sh_tile_start = take(sizeof(int32_t) * 2);
     L.sh_ntiles = take(sizeof(int32_t));
-    L.xs = take(eb * s.Tk * s.d);
-    L.h = take(eb * s.Tk * s.F);
-    L.out_sorted = take(sizeof(float) * s.Tk * s.d);
+    L.xs = take(eb * s.R * s.d);
+    L.h = take(eb * s.R * s.F);
+    L.out_sorted = take(sizeof(float) * rp.s_down * s.R * s.d);
     L.sh_h = take(eb * s.T * s.Fs);
-    L.sh_out = take(sizeof(float) * s.T * s.d);
+    L.sh_out = take(sizeof(float) * sp.s_down * s.T * s.d);
     const bool rt = tc_router(c);
     L.rt_wsplit = take(rt ? 2 * s.E * 3 * router_dp(c) : 0);
-    L.rt_logits = take(rt ? sizeof(float) * router_splits(c) * s.T * s.E : 0);
+    const long long planes =
+        rt ? router_splits(c) : (s.E <= 32 ? router_slices((int)s.d) : 0);
+    L.rt_logits = take(sizeof(float) * planes * s.T * s.E);
     L.rt_offsets = take(sizeof(int32_t) * 2);
     L.rt_tile_e = take(sizeof(int32_t) * max_tiles(s.T, 1, kTcBM));
     L.rt_tile_start = take(sizeof(int32_t) * 2);
     L.rt_ntiles = take(sizeof(int32_t));
+    const long long upw = c->act == MOE_ACT_SWIGLU ? 2 : 1;
+    L.up_part = take(rp.s_up > 1 ? sizeof(float) * rp.s_up * s.R * upw * s.F : 0);
+    L.sh_up_part = take(sp.s_up > 1 ? sizeof(float) * sp.s_up * s.T * 2 * s.Fs : 0);
+    L.ent_partial = take(sizeof(float) * std::max<long long>(rb, (s.T + 31) / 32));
+    L.row_stats = take(sizeof(double) * 3 * s.R);
+    const long long nc = n_candidates(c);
+    L.cand_idx = take(sizeof(int32_t) * s.T * nc);
+    L.cand_w = take(sizeof(float) * s.T * nc);
+    const bool rr = c->reroute_rounds > 0;
+    L.rr_slot_e = take(rr ? sizeof(int32_t) * s.Tk : 0);
+    L.rr_slot_w = take(rr ? sizeof(float) * s.Tk : 0);
+    L.rr_served = take(rr ? sizeof(int32_t) * s.Tk : 0);
+    L.rr_nxt = take(rr ? sizeof(int32_t) * s.T : 0);
+    L.rr_filled = take(rr ? sizeof(int32_t) * s.E : 0);
+    L.rr_filled_before = take(rr ? sizeof(int32_t) * s.E : 0);
+    L.slot_w = take(rr ? sizeof(float) * s.Tk : 0);
+    const bool ec = expert_choice(c);
+    L.ec_row_w = take(ec ? sizeof(float) * s.R : 0);
+    L.ec_rowidx = take(ec ? sizeof(int32_t) * s.E * s.T : 0);
+    L.ec_tok_cnt = take(ec ? sizeof(int32_t) * s.T : 0);
+    L.ec_tok_start = take(ec ? sizeof(int32_t) * (s.T + 1) : 0);
+    L.ec_tok_rows = take(ec ? sizeof(int32_t) * s.R : 0);
+    L.probs_rows = take(sizeof(float) * s.T * s.E);
     L.total = o;
     return L;
 }
@@ -136,6 +240,16 @@ int check_cfg(const moe_config *c) {
     if (c->d_model % vec || c->d_ff % vec || c->d_ff_shared % vec) return MOE_ERR_INVALID_ARG;
     if ((long long)c->T * c->top_k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
     if (c->quantile_balance && c->select_space != MOE_SELECT_PROBS) return MOE_ERR_UNSUPPORTED;
+    if (c->reroute_rounds < 0 || (c->routing != MOE_ROUTING_TOKEN_CHOICE &&
+                                  c->routing != MOE_ROUTING_EXPERT_CHOICE))
+        return MOE_ERR_INVALID_ARG;
+    if (c->routing == MOE_ROUTING_EXPERT_CHOICE && c->quantile_balance)
+        return MOE_ERR_UNSUPPORTED;
+    if (c->reroute_rounds > 0) {
+        if (!(c->capacity_factor > 0.f) || c->routing != MOE_ROUTING_TOKEN_CHOICE)
+            return MOE_ERR_INVALID_ARG;
+        if ((long long)c->top_k * (1 + c->reroute_rounds) > 32) return MOE_ERR_UNSUPPORTED;
+    }
     return MOE_OK;
 }
 
@@ -146,13 +260,6 @@ int check_cfg(const moe_config *c) {
 
 template <typename P> P *at(void *ws, size_t off) {
     return reinterpret_cast<P *>(static_cast<char *>(ws) + off);
-}
-
-long long capacity_of(const moe_config *c) {
-    const long long Tk = (long long)c->T * c->top_k;
-    if (!(c->capacity_factor > 0.f)) return Tk;
-    return (long long)ceil((double)c->capacity_factor * (double)c->T * (double)c->top_k /
-                           (double)c->n_experts);
 }
 
 __global__ void set_pair_kernel(int32_t *p, int a, int b) { p[0] = a; p[1] = b; }
@@ -178,34 +285,54 @@ struct StageTimer {
     }
 } g_timer;
 
+// Inside a stream capture a plain event record only orders the captured
+// work; the External flag makes it a real record node of the graph, so the
+// event can be timed after a replay.
+void timer_record(cudaEvent_t e, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, st);
+}
 cudaEvent_t stage_begin(cudaStream_t st) {
     if (!g_timer.on) return nullptr;
     cudaEvent_t e = g_timer.get();
-    if (e) cudaEventRecord(e, st);
+    if (e) timer_record(e, st);
     return e;
 }
 void stage_end(int stage, cudaEvent_t a, cudaStream_t st) {
     if (!a) return;
     cudaEvent_t b = g_timer.get();
     if (!b) return;
-    cudaEventRecord(b, st);
+    timer_record(b, st);
     g_timer.recs.push_back({stage, a, b});
 }
 
 // Router incl. quantile balancing; p (mean probs) when p_out != NULL.
 int run_router(const moe_config *c, const void *x, const float *w_r, const float *logit_bias,
                const float *select_bias, int32_t *idx, float *w, float *probs, float *p_out,
-               float *sbias_out, bool want_probsT, void *ws, const Layout &L, cudaStream_t st) {
+               float *sbias_out, bool want_probsT, void *ws, const Layout &L, cudaStream_t st,
+               float *entropy_out = nullptr) {
     const Sizes s = sizes(c);
-    RouterArgs a;
+    RouterArgs a{};
     a.x = x; a.w_r = w_r; a.logit_bias = logit_bias;
-    a.select_bias = c->quantile_balance ? nullptr : select_bias;
+    const bool ec = expert_choice(c);
+    a.select_bias = (c->quantile_balance || ec) ? nullptr : select_bias;
     a.T = (int)s.T; a.d = (int)s.d; a.E = (int)s.E; a.k = (int)s.k;
     a.select_space = c->select_space;
-    a.do_select = c->quantile_balance ? 0 : 1;
-    a.idx = idx; a.w = w; a.probs = probs;
-    a.probsT = (c->quantile_balance || want_probsT) ? at<float>(ws, L.probsT) : nullptr;
+    a.do_select = (c->quantile_balance || ec) ? 0 : 1;
+    a.idx = idx; a.w = w;
+    // expert-major probabilities for the per-expert passes (quantile bias,
+    // expert choice); row-major ones for a second selection pass
+    a.probsT = (c->quantile_balance || ec) ? at<float>(ws, L.probsT) : nullptr;
+    a.probs = probs ? probs
+                    : ((c->quantile_balance || want_probsT) ? at<float>(ws, L.probs_rows) : nullptr);
     a.p_partial = at<float>(ws, L.p_partial);
+    a.ent_partial = entropy_out ? at<float>(ws, L.ent_partial) : nullptr;
+    a.n_cand = (int)n_candidates(c);
+    a.cand_idx = at<int32_t>(ws, L.cand_idx);
+    a.cand_w = at<float>(ws, L.cand_w);
     if (tc_router(c)) {
         const int dp = (int)router_dp(c);
         const int S = router_splits(c);
@@ -219,14 +346,24 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         note_launch();
         MOE_CUDA(cudaGetLastError());
         MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E, 3 * dp, dp,
-                                S, s.T * s.E, te, ts, nt, off, part, a.E, st));
-        MOE_CUDA(launch_router_from_logits(a, part, S, st));
+        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E, 3 * dp,
+                                dp, S, s.T * s.E, te, ts, nt, off, part, a.E, st));
+        int planes = S;
+        if (S > 1) {       // a wide kernel adds the planes (same order), streaming
+            MOE_CUDA(launch_sum_planes(part, S, s.T * s.E, a.E, off + 1, s.T, part, st));
+            planes = 1;
+        }
+        MOE_CUDA(launch_router_from_logits(a, part, planes, st));
     } else {
-        MOE_CUDA(launch_router(a, c->dtype, st));
+        MOE_CUDA(launch_router(a, c->dtype, at<float>(ws, L.rt_logits), st));
     }
     if (p_out && s.T > 0)
-        MOE_CUDA(launch_p_finalize(a.p_partial, router_blocks(a.T, a.E), a.E, a.T, p_out, st));
+        MOE_CUDA(launch_p_finalize(a.p_partial, router_blocks(a.T, a.E, c->dtype), a.E, a.T,
+                                   p_out, st));
+    if (entropy_out && s.T > 0)
+        MOE_CUDA(launch_p_finalize(a.ent_partial, router_blocks(a.T, a.E, c->dtype), 1, a.T,
+                                   entropy_out,
+                                   st));
     if (c->quantile_balance && s.T > 0) {
         // Linear interpolation between order statistics: h = (T-1) q,
         // q = 1 - k/E, lo = floor(h), frac = h - lo.
@@ -235,51 +372,83 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         const double lo = floor(h);
         MOE_CUDA(launch_quantile_bias(a.probsT, a.T, a.E, (long long)lo, (float)(h - lo),
                                       sbias_out, st));
-        MOE_CUDA(launch_select_from_probsT(a.probsT, sbias_out, a.T, a.E, a.k, idx, w, st));
+        MOE_CUDA(launch_select_rows(a.probs, sbias_out, a.T, a.E, a.k, idx, w, st, a.n_cand,
+                                    a.cand_idx, a.cand_w));
     }
     return MOE_OK;
 }
 
-// Grouped expert FFN over the dispatched rows; out_sorted fp32.
-// bf16: gather the rows into x_sorted, tcgen05 up (+activation) into h, tcgen05
-// down into out_sorted.  fp32: SIMT GEMMs reading x through perm directly.
+// Up and down projections of one grouped FFN on the tensor cores: rows of A
+// (x_sorted, or x itself for the shared expert) grouped by `offsets` into
+// `groups` experts; h gets the activation in bf16; the down projection's
+// fp32 output goes to `out` (plan.s_down planes of rows*d elements).
+int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void *A,
+               long long rows, int groups, int F, const int32_t *offsets, const void *w1,
+               const void *w3, const void *w2, void *h, float *up_part, float *out,
+               int32_t *tile_e, int32_t *tile_start, int32_t *ntiles, int up_stage,
+               int down_stage, cudaStream_t st) {
+    const int d = c->d_model;
+    const int nt = plan.nt;
+    cudaEvent_t ev = up_stage >= 0 ? stage_begin(st) : nullptr;
+    MOE_CUDA(launch_build_tiles(offsets, groups, nt ? nt : kTcBM, tile_e, nullptr, tile_start,
+                                ntiles, st));
+    if (plan.s_up > 1) {
+        const int upw = up_mode == GEMM_UP_SWIGLU ? 2 : 1;
+        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, A, rows, d, w1, w3, groups, F, F, d, d,
+                                plan.s_up,
+                                rows * upw * F, tile_e, tile_start, ntiles, offsets, up_part,
+                                upw * F, st));
+        MOE_CUDA(launch_split_activation(up_part, plan.s_up, rows * upw * F, F,
+                                         up_mode == GEMM_UP_SWIGLU, offsets + groups, rows,
+                                         static_cast<__nv_bfloat16 *>(h), st));
+    } else {
+        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, A, rows, d, w1, w3, groups, F, F, d, d,
+                                1, 0, tile_e, tile_start, ntiles, offsets, h, F, st));
+    }
+    if (up_stage >= 0) {
+        stage_end(up_stage, ev, st);
+        ev = stage_begin(st);
+    }
+    MOE_CUDA(launch_tc_gemm(GEMM_DOWN, nt, plan.bn_down, h, rows, F, w2, nullptr, groups, d, d,
+                            F, F,
+                            plan.s_down, rows * d, tile_e, tile_start, ntiles, offsets, out, d,
+                            st));
+    if (down_stage >= 0) stage_end(down_stage, ev, st);
+    return MOE_OK;
+}
+
+// Grouped expert FFN over the dispatched rows; out_sorted fp32 (plan.s_down
+// planes of T*k*d elements).  bf16: gather the rows into x_sorted, tcgen05
+// up (+activation) into h, tcgen05 down into out_sorted.  fp32: SIMT GEMMs
+// reading x through perm directly.
 int run_experts(const moe_config *c, const void *x, const int32_t *perm, const int32_t *offsets,
                 const void *w1, const void *w3, const void *w2, float *out_sorted, void *ws,
                 const Layout &L, cudaStream_t st) {
     const Sizes s = sizes(c);
-    if (s.Tk == 0) return MOE_OK;
+    if (s.R == 0) return MOE_OK;
+    const int gk = expert_choice(c) ? 1 : (int)s.k;   // perm holds t*k+j, or t itself
     int32_t *tile_e = at<int32_t>(ws, L.tile_e), *tile_m0 = at<int32_t>(ws, L.tile_m0);
     int32_t *tile_start = at<int32_t>(ws, L.tile_start), *ntiles = at<int32_t>(ws, L.ntiles);
     const int up_mode = c->act == MOE_ACT_SWIGLU ? GEMM_UP_SWIGLU : GEMM_UP_RELU;
     if (c->dtype == MOE_DTYPE_BF16) {
         void *xs = at<void>(ws, L.xs), *h = at<void>(ws, L.h);
         cudaEvent_t ev = stage_begin(st);
-        MOE_CUDA(launch_gather_rows(x, 2, (int)s.d, perm, offsets + s.E, (int)s.k, s.Tk, xs, st));
-        MOE_CUDA(launch_build_tiles(offsets, (int)s.E, kTcBM, tile_e, nullptr, tile_start, ntiles,
-                                    st));
+        MOE_CUDA(launch_gather_rows(x, 2, (int)s.d, perm, offsets + s.E, gk, s.R, xs, st));
         stage_end(MOE_STAGE_GATHER, ev, st);
-        ev = stage_begin(st);
-        MOE_CUDA(launch_tc_gemm(up_mode, xs, s.Tk, (int)s.d, w1, w3, (int)s.E, (int)s.F,
-                                (int)s.F, (int)s.d, (int)s.d, 1, 0, tile_e, tile_start, ntiles,
-                                offsets, h, (int)s.F, st));
-        stage_end(MOE_STAGE_UP, ev, st);
-        ev = stage_begin(st);
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, h, s.Tk, (int)s.F, w2, nullptr, (int)s.E, (int)s.d,
-                                (int)s.d, (int)s.F, (int)s.F, 1, 0, tile_e, tile_start, ntiles,
-                                offsets, out_sorted, (int)s.d, st));
-        stage_end(MOE_STAGE_DOWN, ev, st);
-        return MOE_OK;
+        return run_tc_ffn(c, routed_plan(c), up_mode, xs, s.R, (int)s.E, (int)s.F, offsets, w1,
+                          w3, w2, h, at<float>(ws, L.up_part), out_sorted, tile_e, tile_start,
+                          ntiles, MOE_STAGE_UP, MOE_STAGE_DOWN, st);
     }
     cudaEvent_t ev = stage_begin(st);
     MOE_CUDA(launch_build_tiles(offsets, (int)s.E, kSimtBM, tile_e, tile_m0, nullptr, ntiles, st));
     stage_end(MOE_STAGE_GATHER, ev, st);
     ev = stage_begin(st);
     GroupedGemmArgs up;
-    up.A = x; up.a_gather = perm; up.gather_k = (int)s.k;
+    up.A = x; up.a_gather = perm; up.gather_k = gk;
     up.B1 = w1; up.B3 = w3; up.b_expert_stride = s.F * s.d; up.N = (int)s.F; up.K = (int)s.d;
     up.C = at<void>(ws, L.h); up.ldc = (int)s.F;
     up.tile_e = tile_e; up.tile_m0 = tile_m0; up.n_tiles = ntiles; up.offsets = offsets;
-    up.max_tiles = max_tiles(s.Tk, (int)s.E, kSimtBM);
+    up.max_tiles = max_tiles(s.R, (int)s.E, kSimtBM);
     MOE_CUDA(launch_simt_gemm(up, up_mode, c->dtype, st));
     stage_end(MOE_STAGE_UP, ev, st);
     ev = stage_begin(st);
@@ -292,8 +461,9 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
     return MOE_OK;
 }
 
-// Shared expert (SwiGLU) on all T rows -> sh_out fp32 [T, d]: the same
-// grouped kernels with one group {0, T} and x read in place.
+// Shared expert (SwiGLU) on all T rows -> sh_out fp32 (shared_plan.s_down
+// planes of T*d elements): the same grouped kernels with one group {0, T}
+// and x read in place.
 int run_shared(const moe_config *c, const void *x, const void *ws1, const void *ws3,
                const void *ws2, void *ws, const Layout &L, cudaStream_t st) {
     const Sizes s = sizes(c);
@@ -306,16 +476,9 @@ int run_shared(const moe_config *c, const void *x, const void *ws1, const void *
     int32_t *ts = at<int32_t>(ws, L.sh_tile_start), *nt = at<int32_t>(ws, L.sh_ntiles);
     void *h = at<void>(ws, L.sh_h);
     float *o = at<float>(ws, L.sh_out);
-    if (c->dtype == MOE_DTYPE_BF16) {
-        MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_UP_SWIGLU, x, s.T, (int)s.d, ws1, ws3, 1, (int)s.Fs,
-                                (int)s.Fs, (int)s.d, (int)s.d, 1, 0, te, ts, nt, off, h,
-                                (int)s.Fs, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, h, s.T, (int)s.Fs, ws2, nullptr, 1, (int)s.d,
-                                (int)s.d, (int)s.Fs, (int)s.Fs, 1, 0, te, ts, nt, off, o,
-                                (int)s.d, st));
-        return MOE_OK;
-    }
+    if (c->dtype == MOE_DTYPE_BF16)
+        return run_tc_ffn(c, shared_plan(c), GEMM_UP_SWIGLU, x, s.T, 1, (int)s.Fs, off, ws1, ws3,
+                          ws2, h, at<float>(ws, L.sh_up_part), o, te, ts, nt, -1, -1, st);
     MOE_CUDA(launch_build_tiles(off, 1, kSimtBM, te, tm, nullptr, nt, st));
     GroupedGemmArgs up;
     up.A = x; up.a_gather = nullptr; up.gather_k = 1;
@@ -329,6 +492,19 @@ int run_shared(const moe_config *c, const void *x, const void *ws1, const void *
     dn.C = o; dn.ldc = (int)s.d;
     MOE_CUDA(launch_simt_gemm(dn, GEMM_DOWN, c->dtype, st));
     return MOE_OK;
+}
+
+RerouteWork reroute_work(void *ws, const Layout &L) {
+    RerouteWork w;
+    w.slot_e = at<int32_t>(ws, L.rr_slot_e);
+    w.slot_w = at<float>(ws, L.rr_slot_w);
+    w.served = at<int32_t>(ws, L.rr_served);
+    w.nxt = at<int32_t>(ws, L.rr_nxt);
+    w.filled = at<int32_t>(ws, L.rr_filled);
+    w.filled_before = at<int32_t>(ws, L.rr_filled_before);
+    w.hist = at<int32_t>(ws, L.hist);
+    w.block_base = at<int32_t>(ws, L.block_base);
+    return w;
 }
 
 // Fixed scratch of moe_dispatch_static (no workspace, no allocation).  In host
@@ -401,6 +577,72 @@ int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, int32_t *counts
     return MOE_OK;
 }
 
+int moe_dispatch_reroute(const moe_config *cfg, const int32_t *topk_idx, const float *topk_w,
+                         const int32_t *cand_idx, const float *cand_w, int32_t *counts,
+                         int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *slot_expert,
+                         float *slot_w, int32_t *n_dropped, void *ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    if (cfg->reroute_rounds <= 0) return MOE_ERR_INVALID_ARG;
+    MOE_PTR(counts); MOE_PTR(offsets); MOE_PTR(n_dropped); MOE_PTR(ws);
+    const long long nc = n_candidates(cfg);
+    if (cfg->T > 0) {
+        MOE_PTR(topk_idx); MOE_PTR(topk_w); MOE_PTR(perm); MOE_PTR(inv);
+        if (nc > 0) { MOE_PTR(cand_idx); MOE_PTR(cand_w); }
+    }
+    MOE_OPT_PTR(slot_expert); MOE_OPT_PTR(slot_w);
+    const Layout L = layout(cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    MOE_CUDA(launch_dispatch_reroute(topk_idx, topk_w, cand_idx, cand_w, (int)nc, cfg->T,
+                                     cfg->top_k, cfg->n_experts, capacity_of(cfg),
+                                     cfg->reroute_rounds, reroute_work(ws, L), counts, offsets,
+                                     perm, inv, slot_expert, slot_w, n_dropped,
+                                     (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int64_t moe_reroute_candidates(const moe_config *cfg) {
+    if (check_cfg(cfg) != MOE_OK) return -1;
+    return n_candidates(cfg);
+}
+
+int64_t moe_expert_choice_rows(const moe_config *cfg) {
+    if (check_cfg(cfg) != MOE_OK) return -1;
+    return ec_rows_per_expert(cfg);
+}
+
+int moe_expert_choice(const moe_config *cfg, const float *probs_t, int32_t *perm, float *row_w,
+                      int32_t *counts, int32_t *offsets, int32_t *tok_start, int32_t *tok_rows,
+                      int32_t *n_unchosen, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!expert_choice(cfg)) return MOE_ERR_INVALID_ARG;
+    MOE_PTR(counts); MOE_PTR(offsets); MOE_PTR(tok_start); MOE_PTR(n_unchosen); MOE_PTR(ws);
+    if (cfg->T > 0) { MOE_PTR(probs_t); MOE_PTR(perm); MOE_PTR(row_w); MOE_PTR(tok_rows); }
+    const Layout L = layout(cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    const Sizes s = sizes(cfg);
+    MOE_CUDA(launch_expert_choice(probs_t, (int)s.T, (int)s.E, (int)ec_rows_per_expert(cfg), perm,
+                                  row_w, at<int32_t>(ws, L.ec_rowidx), counts, offsets,
+                                  at<int32_t>(ws, L.ec_tok_cnt), tok_start, tok_rows, n_unchosen,
+                                  (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int moe_combine_rows(const moe_config *cfg, const float *out_sorted, const float *row_w,
+                     const int32_t *tok_start, const int32_t *tok_rows, const float *shared_out,
+                     void *y, moe_stream_t stream) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    if (cfg->T == 0) return MOE_OK;
+    MOE_PTR(out_sorted); MOE_PTR(row_w); MOE_PTR(tok_start); MOE_PTR(tok_rows); MOE_PTR(y);
+    MOE_OPT_PTR(shared_out);
+    MOE_CUDA(launch_combine_rows(out_sorted, 1, 0, tok_start, tok_rows, row_w, shared_out, 1, 0,
+                                 cfg->T, cfg->d_model, cfg->out_dtype, y, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
 int moe_dispatch_static(const moe_config *cfg, const int32_t *topk_idx, int32_t *counts,
                         int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *n_dropped,
                         moe_stream_t stream) {
@@ -432,8 +674,18 @@ int moe_expert_ffn(const moe_config *cfg, const void *x, const int32_t *perm,
     if (cfg->act == MOE_ACT_SWIGLU) MOE_PTR(w3);
     const Layout L = layout(cfg);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-    return run_experts(cfg, x, perm, offsets, w1, w3, w2, out_sorted, ws, L,
-                       (cudaStream_t)stream);
+    const FfnPlan plan = routed_plan(cfg);
+    if (plan.s_down == 1)
+        return run_experts(cfg, x, perm, offsets, w1, w3, w2, out_sorted, ws, L,
+                           (cudaStream_t)stream);
+    // split reduction: partial planes in the workspace, summed into out_sorted
+    float *planes = at<float>(ws, L.out_sorted);
+    rc = run_experts(cfg, x, perm, offsets, w1, w3, w2, planes, ws, L, (cudaStream_t)stream);
+    if (rc != MOE_OK) return rc;
+    const long long R = sizes(cfg).R;
+    MOE_CUDA(launch_sum_planes(planes, plan.s_down, R * cfg->d_model, cfg->d_model,
+                               offsets + cfg->n_experts, R, out_sorted, (cudaStream_t)stream));
+    return MOE_OK;
 }
 
 int moe_combine(const moe_config *cfg, const float *out_sorted, const int32_t *inv,
@@ -442,7 +694,7 @@ int moe_combine(const moe_config *cfg, const float *out_sorted, const int32_t *i
     if (rc != MOE_OK) return rc;
     if (cfg->T == 0) return MOE_OK;
     MOE_PTR(out_sorted); MOE_PTR(inv); MOE_PTR(topk_w); MOE_PTR(y); MOE_OPT_PTR(shared_out);
-    MOE_CUDA(launch_combine(out_sorted, inv, topk_w, shared_out, cfg->T, cfg->top_k,
+    MOE_CUDA(launch_combine(out_sorted, 1, 0, inv, topk_w, shared_out, 1, 0, cfg->T, cfg->top_k,
                             cfg->d_model, cfg->out_dtype, y, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -469,9 +721,64 @@ int moe_load_stats(const moe_config *cfg, const int32_t *topk_idx, const float *
     return MOE_OK;
 }
 
+int moe_observe(const moe_config *cfg, const float *probs, const float *out_sorted,
+                const int32_t *offsets, const float *select_bias, const int32_t *n_dropped,
+                const moe_observability *obs, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    MOE_REQUIRE(obs != nullptr);
+    MOE_PTR(ws);
+    MOE_OPT_PTR(probs); MOE_OPT_PTR(out_sorted); MOE_OPT_PTR(offsets);
+    MOE_OPT_PTR(select_bias); MOE_OPT_PTR(n_dropped);
+    MOE_REQUIRE((out_sorted == nullptr) == (offsets == nullptr));
+    MOE_OPT_PTR(obs->drop_ratio); MOE_OPT_PTR(obs->gate_entropy);
+    MOE_OPT_PTR(obs->bias_mean_abs); MOE_OPT_PTR(obs->bias_max_abs);
+    MOE_OPT_PTR(obs->expert_out_mean); MOE_OPT_PTR(obs->expert_out_std);
+    MOE_OPT_PTR(obs->expert_out_max_abs);
+    const Layout L = layout(cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    const Sizes s = sizes(cfg);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (obs->gate_entropy) {
+        if (probs && s.T > 0) {
+            float *part = at<float>(ws, L.ent_partial);
+            MOE_CUDA(launch_entropy_partials(probs, (int)s.T, (int)s.E, part, st));
+            MOE_CUDA(launch_p_finalize(part, (int)((s.T + 31) / 32), 1, (int)s.T,
+                                       obs->gate_entropy, st));
+        } else {
+            MOE_CUDA(cudaMemsetAsync(obs->gate_entropy, 0, sizeof(float), st));
+        }
+    }
+    ObsArgs oa{};
+    oa.n_dropped = n_dropped;
+    oa.bias = select_bias;
+    oa.drop_ratio = obs->drop_ratio;
+    oa.bias_mean_abs = obs->bias_mean_abs;
+    oa.bias_max_abs = obs->bias_max_abs;
+    if (oa.drop_ratio || oa.bias_mean_abs || oa.bias_max_abs)
+        MOE_CUDA(launch_stats_finalize(nullptr, nullptr, (int)s.T, (int)s.E, (int)s.k, nullptr,
+                                       nullptr, nullptr, nullptr, st, oa));
+    float *outs[3] = {obs->expert_out_mean, obs->expert_out_std, obs->expert_out_max_abs};
+    for (float *o : outs) {
+        if (o && !out_sorted) MOE_CUDA(cudaMemsetAsync(o, 0, sizeof(float) * s.E, st));
+    }
+    if (out_sorted && (outs[0] || outs[1] || outs[2]))
+        MOE_CUDA(launch_expert_scale(out_sorted, 1, 0, (int)s.d, offsets, (int)s.E, s.Tk,
+                                     at<double>(ws, L.row_stats), outs[0], outs[1], outs[2],
+                                     st));
+    return MOE_OK;
+}
+
 int moe_layer_forward(const moe_config *cfg, const void *x, const moe_layer_weights *wts,
                       const moe_layer_outputs *out, void *ws, size_t ws_bytes,
                       moe_stream_t stream) {
+    return moe_layer_forward_observed(cfg, x, wts, out, nullptr, ws, ws_bytes, stream);
+}
+
+int moe_layer_forward_observed(const moe_config *cfg, const void *x,
+                               const moe_layer_weights *wts, const moe_layer_outputs *out,
+                               const moe_observability *obs, void *ws, size_t ws_bytes,
+                               moe_stream_t stream) {
     int rc = check_cfg(cfg);
     if (rc != MOE_OK) return rc;
     MOE_REQUIRE(wts != nullptr && out != nullptr);
@@ -484,7 +791,13 @@ int moe_layer_forward(const moe_config *cfg, const void *x, const moe_layer_weig
     MOE_OPT_PTR(out->topk_idx); MOE_OPT_PTR(out->topk_w); MOE_OPT_PTR(out->counts);
     MOE_OPT_PTR(out->n_dropped); MOE_OPT_PTR(out->f); MOE_OPT_PTR(out->p); MOE_OPT_PTR(out->aux);
     MOE_OPT_PTR(out->load_max_over_mean); MOE_OPT_PTR(out->select_bias_out);
-    MOE_OPT_PTR(out->counts_unbiased);
+    MOE_OPT_PTR(out->counts_unbiased); MOE_OPT_PTR(out->slot_expert); MOE_OPT_PTR(out->slot_w);
+    if (obs) {
+        MOE_OPT_PTR(obs->drop_ratio); MOE_OPT_PTR(obs->gate_entropy);
+        MOE_OPT_PTR(obs->bias_mean_abs); MOE_OPT_PTR(obs->bias_max_abs);
+        MOE_OPT_PTR(obs->expert_out_mean); MOE_OPT_PTR(obs->expert_out_std);
+        MOE_OPT_PTR(obs->expert_out_max_abs);
+    }
     const Layout L = layout(cfg);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
@@ -507,21 +820,44 @@ int moe_layer_forward(const moe_config *cfg, const void *x, const moe_layer_weig
     cudaEvent_t ev = stage_begin(st);
     if (s.T > 0) {
         rc = run_router(cfg, x, wts->w_r, wts->logit_bias, wts->select_bias, idx, w, nullptr, p,
-                        sbias, want_unb && biased, ws, L, st);
+                        sbias, want_unb && biased, ws, L, st, obs ? obs->gate_entropy : nullptr);
         if (rc != MOE_OK) return rc;
+    } else if (obs && obs->gate_entropy) {
+        MOE_CUDA(cudaMemsetAsync(obs->gate_entropy, 0, sizeof(float), st));
     }
     stage_end(MOE_STAGE_ROUTER, ev, st);
     ev = stage_begin(st);
-    MOE_CUDA(launch_dispatch(idx, s.Tk, (int)s.E, (int)s.k, capacity_of(cfg),
-                             at<int32_t>(ws, L.hist), at<int32_t>(ws, L.block_base), counts,
-                             offsets, perm, inv, ndrop, st));
+    const float *comb_w = w;           // gate weight of each slot in the combine
+    const bool ec = expert_choice(cfg);
+    if (ec) {
+        MOE_CUDA(launch_expert_choice(at<float>(ws, L.probsT), (int)s.T, (int)s.E,
+                                      (int)ec_rows_per_expert(cfg), perm,
+                                      at<float>(ws, L.ec_row_w), at<int32_t>(ws, L.ec_rowidx),
+                                      counts, offsets, at<int32_t>(ws, L.ec_tok_cnt),
+                                      at<int32_t>(ws, L.ec_tok_start),
+                                      at<int32_t>(ws, L.ec_tok_rows), ndrop, st));
+    } else if (cfg->reroute_rounds > 0) {
+        float *sw = out->slot_w ? out->slot_w : at<float>(ws, L.slot_w);
+        MOE_CUDA(launch_dispatch_reroute(idx, w, at<int32_t>(ws, L.cand_idx),
+                                         at<float>(ws, L.cand_w), (int)n_candidates(cfg), s.T,
+                                         (int)s.k, (int)s.E, capacity_of(cfg),
+                                         cfg->reroute_rounds, reroute_work(ws, L), counts,
+                                         offsets, perm, inv, out->slot_expert, sw, ndrop, st));
+        comb_w = sw;
+    } else {
+        MOE_CUDA(launch_dispatch(idx, s.Tk, (int)s.E, (int)s.k, capacity_of(cfg),
+                                 at<int32_t>(ws, L.hist), at<int32_t>(ws, L.block_base), counts,
+                                 offsets, perm, inv, ndrop, st));
+        if (out->slot_expert || out->slot_w)
+            MOE_CUDA(launch_slot_outputs(idx, w, inv, s.Tk, out->slot_expert, out->slot_w, st));
+    }
     stage_end(MOE_STAGE_DISPATCH, ev, st);
     ev = stage_begin(st);
     if (want_unb) {
-        if (biased && s.T > 0) {
+        if (biased && s.T > 0 && !ec) {
             int32_t *iu = at<int32_t>(ws, L.idx_unb);
-            MOE_CUDA(launch_select_from_probsT(at<float>(ws, L.probsT), nullptr, (int)s.T,
-                                               (int)s.E, (int)s.k, iu, nullptr, st));
+            MOE_CUDA(launch_select_rows(at<float>(ws, L.probs_rows), nullptr, (int)s.T,
+                                        (int)s.E, (int)s.k, iu, nullptr, st));
             MOE_CUDA(launch_histogram(iu, s.Tk, (int)s.E, at<int32_t>(ws, L.hist),
                                       out->counts_unbiased, st));
         } else {
@@ -532,12 +868,33 @@ int moe_layer_forward(const moe_config *cfg, const void *x, const moe_layer_weig
     if (s.T == 0) {
         MOE_CUDA(cudaMemsetAsync(p, 0, sizeof(float) * s.E, st));
     }
+    ObsArgs oa{};
+    if (obs) {
+        oa.n_dropped = ndrop;
+        oa.bias = cfg->quantile_balance ? sbias : wts->select_bias;
+        oa.drop_ratio = obs->drop_ratio;
+        oa.bias_mean_abs = obs->bias_mean_abs;
+        oa.bias_max_abs = obs->bias_max_abs;
+    }
     MOE_CUDA(launch_stats_finalize(counts, p, (int)s.T, (int)s.E, (int)s.k, out->f, nullptr,
-                                   out->aux, out->load_max_over_mean, st));
+                                   out->aux, out->load_max_over_mean, st, oa));
     stage_end(MOE_STAGE_STATS, ev, st);
-    if (s.T == 0) return MOE_OK;
+    const bool want_scale =
+        obs && (obs->expert_out_mean || obs->expert_out_std || obs->expert_out_max_abs);
+    if (s.T == 0) {
+        if (want_scale)
+            MOE_CUDA(launch_expert_scale(out_sorted, 1, 0, (int)s.d, offsets, (int)s.E, 0,
+                                         at<double>(ws, L.row_stats), obs->expert_out_mean,
+                                         obs->expert_out_std, obs->expert_out_max_abs, st));
+        return MOE_OK;
+    }
     rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted, ws, L, st);
     if (rc != MOE_OK) return rc;
+    if (want_scale)
+        MOE_CUDA(launch_expert_scale(out_sorted, routed_plan(cfg).s_down, s.R * s.d, (int)s.d,
+                                     offsets, (int)s.E, s.R, at<double>(ws, L.row_stats),
+                                     obs->expert_out_mean, obs->expert_out_std,
+                                     obs->expert_out_max_abs, st));
     const float *shared = nullptr;
     if (s.Fs > 0) {
         ev = stage_begin(st);
@@ -547,8 +904,16 @@ int moe_layer_forward(const moe_config *cfg, const void *x, const moe_layer_weig
         shared = at<float>(ws, L.sh_out);
     }
     ev = stage_begin(st);
-    MOE_CUDA(launch_combine(out_sorted, inv, w, shared, (int)s.T, (int)s.k, (int)s.d,
-                            cfg->out_dtype, out->y, st));
+    if (ec)
+        MOE_CUDA(launch_combine_rows(out_sorted, routed_plan(cfg).s_down, s.R * s.d,
+                                     at<int32_t>(ws, L.ec_tok_start),
+                                     at<int32_t>(ws, L.ec_tok_rows), at<float>(ws, L.ec_row_w),
+                                     shared, shared_plan(cfg).s_down, s.T * s.d, (int)s.T,
+                                     (int)s.d, cfg->out_dtype, out->y, st));
+    else
+        MOE_CUDA(launch_combine(out_sorted, routed_plan(cfg).s_down, s.R * s.d, inv, comb_w,
+                                shared, shared_plan(cfg).s_down, s.T * s.d, (int)s.T, (int)s.k,
+                                (int)s.d, cfg->out_dtype, out->y, st));
     stage_end(MOE_STAGE_COMBINE, ev, st);
     return MOE_OK;
 }
@@ -583,13 +948,13 @@ int moe_stage_timing_read(double *stage_ms, int64_t *calls) {
         float ms = 0.f;
         if (cudaEventSynchronize(r.b) != cudaSuccess ||
             cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+            (void)cudaGetLastError();   // keep the failure out of later launch checks
             rc = MOE_ERR_CUDA;
             continue;
         }
         stage_ms[r.stage] += ms;
     }
     *calls = g_timer.calls;
-    g_timer.recycle();
     return rc;
 }
 

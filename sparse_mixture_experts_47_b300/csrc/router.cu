@@ -23,25 +23,35 @@
 namespace moe {
 
 // --------------------------------------------------------------------------
-// Small E (<= 32): one warp holds TPW = 32/EP tokens x EP (padded) experts.
-// Lanes split d into 16-byte vectors, accumulate all TPW*EP = 32 partial
-// logits, and a reduce-scatter butterfly leaves lane L with the full logit
-// of (token L / EP, expert L % EP).  W_r is staged through shared memory in
-// 32 KB chunks of d.
+// Small E (<= 32): partial logits of one slice of d (kRouterSlice columns)
+// for a tile of tokens; the softmax kernel adds the slices in order.  A warp
+// holds TPW = 32/EP tokens x EP (padded) experts; lanes split the slice into
+// 16-byte vectors, accumulate all TPW*EP = 32 partial logits, and a
+// reduce-scatter butterfly leaves lane L with the slice's logit of
+// (token L / EP, expert L % EP).  The W_r slice is staged in shared memory.
+// Each token's arithmetic is the same whatever the batch size, so a token's
+// routing does not depend on the batch it comes in.
 // --------------------------------------------------------------------------
 template <typename TX, int EP>
-__global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(256) router_partial_kernel(RouterArgs a, float *part) {
     constexpr int VN = Vec<TX>::N;
     constexpr int TPW = 32 / EP;
-    constexpr int R = 32 / EP;            // vectors per lane per chunk
-    constexpr int DC = 32 * VN * R;       // chunk of d held in shared memory
-    extern __shared__ __align__(16) float smem[];
-    float *wsm = smem;                    // [EP][DC]
-    float *part = smem + EP * DC;         // [8 warps][32 lanes]
+    constexpr int DS = kRouterSlice;
+    extern __shared__ __align__(16) float wsm[];   // [EP][DS]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tok0 = (blockIdx.x * 8 + warp) * TPW;
+    const int c0 = blockIdx.y * DS, clen = min(DS, a.d - c0);
     const TX *x = static_cast<const TX *>(a.x);
+
+    for (int i = threadIdx.x * 4; i < EP * DS; i += 256 * 4) {
+        const int e = i / DS, c = i % DS;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < a.E && c < clen)
+            v = *reinterpret_cast<const float4 *>(a.w_r + (size_t)e * a.d + c0 + c);
+        *reinterpret_cast<float4 *>(wsm + i) = v;
+    }
+    __syncthreads();
 
     float acc[TPW][EP];
 #pragma unroll
@@ -49,45 +59,33 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
 #pragma unroll
         for (int e = 0; e < EP; ++e) acc[t][e] = 0.f;
 
-    for (int c0 = 0; c0 < a.d; c0 += DC) {
-        const int clen = min(DC, a.d - c0);
-        __syncthreads();
-        for (int i = threadIdx.x * 4; i < EP * DC; i += 256 * 4) {
-            const int e = i / DC, c = i % DC;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < a.E && c < clen)
-                v = *reinterpret_cast<const float4 *>(a.w_r + (size_t)e * a.d + c0 + c);
-            *reinterpret_cast<float4 *>(wsm + i) = v;
-        }
-        __syncthreads();
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int c = (r * 32 + lane) * VN;
-            if (c < clen) {
-                float xv[TPW][VN];
+    for (int j = 0; j < DS / (32 * VN); ++j) {
+        const int c = (j * 32 + lane) * VN;
+        if (c < clen) {
+            float xv[TPW][VN];
 #pragma unroll
-                for (int t = 0; t < TPW; ++t) {
-                    if (tok0 + t < a.T) {
-                        load16_f32(x + (size_t)(tok0 + t) * a.d + c0 + c, xv[t]);
-                    } else {
+            for (int t = 0; t < TPW; ++t) {
+                if (tok0 + t < a.T) {
+                    load16_f32(x + (size_t)(tok0 + t) * a.d + c0 + c, xv[t]);
+                } else {
 #pragma unroll
-                        for (int i = 0; i < VN; ++i) xv[t][i] = 0.f;
-                    }
+                    for (int i = 0; i < VN; ++i) xv[t][i] = 0.f;
                 }
+            }
 #pragma unroll
-                for (int e = 0; e < EP; ++e) {
-                    if (e < a.E) {
-                        float wv[VN];
+            for (int e = 0; e < EP; ++e) {
+                if (e < a.E) {
+                    float wv[VN];
 #pragma unroll
-                        for (int i = 0; i < VN; i += 4) {
-                            float4 q = *reinterpret_cast<const float4 *>(wsm + e * DC + c + i);
-                            wv[i] = q.x; wv[i + 1] = q.y; wv[i + 2] = q.z; wv[i + 3] = q.w;
-                        }
-#pragma unroll
-                        for (int t = 0; t < TPW; ++t)
-#pragma unroll
-                            for (int i = 0; i < VN; ++i) acc[t][e] = fmaf(xv[t][i], wv[i], acc[t][e]);
+                    for (int i = 0; i < VN; i += 4) {
+                        const float4 q = *reinterpret_cast<const float4 *>(wsm + e * DS + c + i);
+                        wv[i] = q.x; wv[i + 1] = q.y; wv[i + 2] = q.z; wv[i + 3] = q.w;
                     }
+#pragma unroll
+                    for (int t = 0; t < TPW; ++t)
+#pragma unroll
+                        for (int i = 0; i < VN; ++i) acc[t][e] = fmaf(xv[t][i], wv[i], acc[t][e]);
                 }
             }
         }
@@ -110,14 +108,40 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
+    const int ge = lane % EP;
+    const int t = tok0 + lane / EP;
+    if (ge < a.E && t < a.T)
+        part[(size_t)blockIdx.y * a.T * a.E + (size_t)t * a.E + ge] = v[0];
+}
 
-    const int ge = lane % EP;               // expert of this lane
-    const int t = tok0 + lane / EP;          // token of this lane
+// --------------------------------------------------------------------------
+// Small E (<= 32), second step: softmax, top-k and renormalisation with one
+// lane per (token, expert): a warp holds TPW = 32/EP tokens, the slice sums
+// are added in slice order (+ logit offset), the softmax and the top-k run
+// as butterflies over the EP lanes of a token.  Also the per-block partial
+// sums of the probabilities and of the gate entropy, and the candidates
+// ranked after the top k (for redirected overflow).
+// --------------------------------------------------------------------------
+template <int EP>
+__global__ void __launch_bounds__(256) router_small_epilogue_kernel(RouterArgs a,
+                                                                    const float *part,
+                                                                    int S) {
+    constexpr int TPW = 32 / EP;
+    __shared__ float red[256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ge = lane % EP;                               // expert of this lane
+    const int t = (blockIdx.x * 8 + warp) * TPW + lane / EP; // token of this lane
     const bool ve = ge < a.E, vt = t < a.T;
-    float logit = v[0];
-    if (ve && a.logit_bias) logit += a.logit_bias[ge];
-    if (!ve) logit = -CUDART_INF_F;
-
+    float logit = -CUDART_INF_F;
+    if (ve && vt) {
+        const size_t plane = (size_t)a.T * a.E, o = (size_t)t * a.E + ge;
+        float v = 0.f;
+        for (int sp = 0; sp < S; ++sp) v += part[sp * plane + o];
+        if (a.logit_bias) v += a.logit_bias[ge];
+        logit = v;
+    } else if (ve) {
+        logit = 0.f;                                        // padding token, not stored
+    }
     float m = logit;
 #pragma unroll
     for (int off = EP / 2; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -138,7 +162,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
                       (a.select_bias ? a.select_bias[ge] : 0.f);
         float psum = 0.f, my_p = 0.f;
         int my_e = 0;
-        for (int j = 0; j < a.k; ++j) {
+        for (int j = 0; j < a.k + a.n_cand; ++j) {
             float bv = sel;
             int bi = ge;
 #pragma unroll
@@ -148,25 +172,43 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
                 if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
             }
             const float pw = __shfl_sync(0xffffffffu, prob, (lane & ~(EP - 1)) + bi);
-            psum += pw;
+            if (j < a.k) psum += pw;
             if (ge == j) { my_e = bi; my_p = pw; }
             if (ge == bi) sel = -CUDART_INF_F;
         }
         if (vt && ge < a.k) {
             a.idx[(size_t)t * a.k + ge] = my_e;
             a.w[(size_t)t * a.k + ge] = my_p / psum;
+        } else if (vt && ge < a.k + a.n_cand) {
+            a.cand_idx[(size_t)t * a.n_cand + ge - a.k] = my_e;
+            a.cand_w[(size_t)t * a.n_cand + ge - a.k] = my_p / psum;
         }
     }
 
     // Per-block partial sums of the probabilities, fixed order.
-    part[warp * 32 + lane] = (vt && ve) ? prob : 0.f;
+    red[threadIdx.x] = (vt && ve) ? prob : 0.f;
     __syncthreads();
     if (a.p_partial && threadIdx.x < a.E) {
         const int e = threadIdx.x;
         float sum = 0.f;
         for (int w = 0; w < 8; ++w)
-            for (int g = 0; g < TPW; ++g) sum += part[w * 32 + g * EP + e];
+            for (int g = 0; g < TPW; ++g) sum += red[w * 32 + g * EP + e];
         a.p_partial[(size_t)blockIdx.x * a.E + e] = sum;
+    }
+    // Per-block sum of the tokens' gate entropies -sum_e p ln p, with
+    // ln p = (logit - max) - ln(sum): fixed butterfly, then warps in order.
+    if (a.ent_partial) {
+        __syncthreads();
+        float h = (vt && ve) ? -prob * ((logit - m) - logf(s)) : 0.f;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) h += __shfl_xor_sync(0xffffffffu, h, off);
+        if (lane == 0) red[warp] = h;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.f;
+            for (int w = 0; w < 8; ++w) tot += red[w];
+            a.ent_partial[blockIdx.x] = tot;
+        }
     }
 }
 
@@ -179,7 +221,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(RouterArgs a) {
 constexpr int kTB = 32, kEC = 128, kDK = 32;
 
 __host__ __device__ inline size_t router_tiled_smem(int E) {
-    return sizeof(float) * ((size_t)kTB * E + kDK * kTB + kDK * (kEC + 4) + 2 * kTB);
+    return sizeof(float) * ((size_t)kTB * E + kDK * kTB + kDK * (kEC + 4) + 3 * kTB);
 }
 
 __device__ __forceinline__ void load4_f32(const float *p, float *v) {
@@ -192,17 +234,44 @@ __device__ __forceinline__ void load4_f32(const __nv_bfloat16 *p, float *v) {
     v[2] = __uint_as_float(a.y << 16); v[3] = __uint_as_float(a.y & 0xffff0000u);
 }
 
-// Softmax, load-statistics partial sums, optional probs/probsT and top-k with
-// renormalisation for a tile of kTB tokens whose logits (logit offset included)
-// are in shared memory lg[kTB][E].  256 threads; warp w owns tokens 4w..4w+3.
+// One round of top-k selection over a warp: lane L holds the scores of
+// experts L + 32 i in sc[i] (-inf where absent or already taken).  Returns
+// the expert with the largest score, exactly equal scores going to the lower
+// expert index, and marks it taken.
+constexpr int kTopkPerLane = 32;   // E <= 1024
+__device__ __forceinline__ int warp_take_max(float (&sc)[kTopkPerLane], int lane) {
+    float bv = -CUDART_INF_F;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kTopkPerLane; ++i)
+        if (sc[i] > bv) { bv = sc[i]; bi = lane + 32 * i; }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+#pragma unroll
+    for (int i = 0; i < kTopkPerLane; ++i)
+        if (lane + 32 * i == bi) sc[i] = -CUDART_INF_F;
+    return bi;
+}
+
+// Softmax, load-statistics partial sums, optional probs/probsT, optional
+// gate-entropy partial sum and top-k with renormalisation for a tile of TB
+// tokens whose logits (logit offset included) are in shared memory
+// lg[TB][E].  256 threads; warp w owns tokens (TB/8) w .. (TB/8)(w+1) - 1.
+// st_m, st_s, st_h hold TB floats each.
+template <int TB>
 __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m, float *st_s,
-                                     int t0) {
+                                     float *st_h, int t0) {
+    constexpr int TPWR = TB / 8;
     const int E = a.E;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Softmax statistics per token (warp per 4 tokens), optional probs rows.
-    for (int r = 0; r < 4; ++r) {
-        const int tt = 4 * warp + r, t = t0 + tt;
+    for (int r = 0; r < TPWR; ++r) {
+        const int tt = TPWR * warp + r, t = t0 + tt;
         const float *row = lg + tt * E;
         float m = -CUDART_INF_F;
         for (int e = lane; e < E; e += 32) m = fmaxf(m, row[e]);
@@ -212,7 +281,20 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
         for (int e = lane; e < E; e += 32) s += expf(row[e] - m);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) { st_m[tt] = m; st_s[tt] = s; }
+        float hz = 0.f;      // sum_e exp(z) z, z = logit - max: entropy = ln s - hz / s
+        if (a.ent_partial) {
+            for (int e = lane; e < E; e += 32) {
+                const float z = row[e] - m;
+                hz += expf(z) * z;
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) hz += __shfl_xor_sync(0xffffffffu, hz, off);
+        }
+        if (lane == 0) {
+            st_m[tt] = m;
+            st_s[tt] = s;
+            st_h[tt] = t < a.T ? logf(s) - hz / s : 0.f;
+        }
         if (t < a.T && a.probs)
             for (int e = lane; e < E; e += 32) a.probs[(size_t)t * E + e] = expf(row[e] - m) / s;
     }
@@ -222,50 +304,50 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
     // the expert-major copy used by quantile balancing.
     for (int e = tid; e < E; e += 256) {
         float sum = 0.f;
-        for (int tt = 0; tt < kTB && t0 + tt < a.T; ++tt) {
+        for (int tt = 0; tt < TB && t0 + tt < a.T; ++tt) {
             const float p = expf(lg[tt * E + e] - st_m[tt]) / st_s[tt];
             sum += p;
             if (a.probsT) a.probsT[(size_t)e * a.T + t0 + tt] = p;
         }
         if (a.p_partial) a.p_partial[(size_t)blockIdx.x * E + e] = sum;
     }
+    if (a.ent_partial && tid == 0) {
+        float tot = 0.f;
+        for (int tt = 0; tt < TB; ++tt) tot += st_h[tt];
+        a.ent_partial[blockIdx.x] = tot;
+    }
     if (!a.do_select) return;
     __syncthreads();
 
-    // Top-k per token; a taken expert's logit is overwritten with -inf.
-    for (int r = 0; r < 4; ++r) {
-        const int tt = 4 * warp + r, t = t0 + tt;
+    // Top-k per token from the selection scores held in registers.
+    for (int r = 0; r < TPWR; ++r) {
+        const int tt = TPWR * warp + r, t = t0 + tt;
         if (t >= a.T) break;
-        float *row = lg + tt * E;
+        const float *row = lg + tt * E;
         const float m = st_m[tt], s = st_s[tt];
+        float sc[kTopkPerLane];
+#pragma unroll
+        for (int i = 0; i < kTopkPerLane; ++i) {
+            const int e = lane + 32 * i;
+            sc[i] = -CUDART_INF_F;
+            if (e < E)
+                sc[i] = (a.select_space == MOE_SELECT_PROBS ? expf(row[e] - m) / s : row[e]) +
+                        (a.select_bias ? a.select_bias[e] : 0.f);
+        }
         float psum = 0.f, my_p = 0.f;
         int my_e = 0;
-        for (int j = 0; j < a.k; ++j) {
-            float bv = -CUDART_INF_F;
-            int bi = 0x7fffffff;
-            for (int e = lane; e < E; e += 32) {
-                const float l = row[e];
-                if (l == -CUDART_INF_F) continue;
-                const float sc = (a.select_space == MOE_SELECT_PROBS ? expf(l - m) / s : l) +
-                                 (a.select_bias ? a.select_bias[e] : 0.f);
-                if (sc > bv) { bv = sc; bi = e; }
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
+        for (int j = 0; j < a.k + a.n_cand; ++j) {
+            const int bi = warp_take_max(sc, lane);
             const float pw = expf(row[bi] - m) / s;
-            psum += pw;
+            if (j < a.k) psum += pw;
             if (lane == j) { my_e = bi; my_p = pw; }
-            __syncwarp();
-            if (lane == 0) row[bi] = -CUDART_INF_F;
-            __syncwarp();
         }
         if (lane < a.k) {
             a.idx[(size_t)t * a.k + lane] = my_e;
             a.w[(size_t)t * a.k + lane] = my_p / psum;
+        } else if (lane < a.k + a.n_cand) {
+            a.cand_idx[(size_t)t * a.n_cand + lane - a.k] = my_e;
+            a.cand_w[(size_t)t * a.n_cand + lane - a.k] = my_p / psum;
         }
     }
 }
@@ -279,6 +361,7 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
     float *wsh = xs + kDK * kTB;              // [kDK][kEC + 4]
     float *st_m = wsh + kDK * (kEC + 4);      // [kTB]
     float *st_s = st_m + kTB;                 // [kTB]
+    float *st_h = st_s + kTB;                 // [kTB]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTB;
@@ -332,7 +415,7 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
         }
     }
     __syncthreads();
-    router_rows_epilogue(a, lg, st_m, st_s, t0);
+    router_rows_epilogue<kTB>(a, lg, st_m, st_s, st_h, t0);
 }
 
 // --------------------------------------------------------------------------
@@ -363,16 +446,18 @@ __global__ void split_router_weight_kernel(const float *w_r, int E, int d, int d
 
 // Logits = sum of S partial products (fixed order) + logit offset, then the
 // same per-token epilogue as the SIMT router.
+template <int TB>
 __global__ void __launch_bounds__(256) router_from_logits_kernel(RouterArgs a,
                                                                  const float *part, int S) {
     extern __shared__ __align__(16) float smem[];
     const int E = a.E;
     float *lg = smem;
-    float *st_m = lg + kTB * E;
-    float *st_s = st_m + kTB;
-    const int t0 = blockIdx.x * kTB;
+    float *st_m = lg + TB * E;
+    float *st_s = st_m + TB;
+    float *st_h = st_s + TB;
+    const int t0 = blockIdx.x * TB;
     const size_t plane = (size_t)a.T * E;
-    for (int i = threadIdx.x; i < kTB * E; i += blockDim.x) {
+    for (int i = threadIdx.x; i < TB * E; i += blockDim.x) {
         const int tt = i / E, e = i - tt * E, t = t0 + tt;
         float v = 0.f;
         if (t < a.T) {
@@ -383,98 +468,104 @@ __global__ void __launch_bounds__(256) router_from_logits_kernel(RouterArgs a,
         lg[i] = v;
     }
     __syncthreads();
-    router_rows_epilogue(a, lg, st_m, st_s, t0);
-}
-
-// --------------------------------------------------------------------------
-// Top-k from stored expert-major probabilities probsT [E, T] with a bias
-// (second pass of quantile balancing).  32 tokens per CTA, the [E x 32]
-// tile transposed through shared memory.
-// --------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) select_from_probsT_kernel(
-        const float *probsT, const float *bias, int T, int E, int k,
-        int32_t *idx, float *w) {
-    extern __shared__ __align__(16) float tile[];   // [E][33]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = blockIdx.x * 32;
-    for (int i = tid; i < E * 32; i += 256) {
-        const int e = i >> 5, tt = i & 31, t = t0 + tt;
-        tile[e * 33 + tt] = t < T ? probsT[(size_t)e * T + t] : 0.f;
-    }
-    __syncthreads();
-    for (int r = 0; r < 4; ++r) {
-        const int tt = 4 * warp + r, t = t0 + tt;
-        if (t >= T) break;
-        float psum = 0.f, my_p = 0.f;
-        int my_e = 0;
-        for (int j = 0; j < k; ++j) {
-            float bv = -CUDART_INF_F;
-            int bi = 0x7fffffff;
-            for (int e = lane; e < E; e += 32) {
-                const float p = tile[e * 33 + tt];
-                if (p < 0.f) continue;                        // taken
-                const float sc = p + (bias ? bias[e] : 0.f);
-                if (sc > bv) { bv = sc; bi = e; }
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            const float pw = tile[bi * 33 + tt];
-            psum += pw;
-            if (lane == j) { my_e = bi; my_p = pw; }
-            __syncwarp();
-            if (lane == 0) tile[bi * 33 + tt] = -1.f;
-            __syncwarp();
-        }
-        if (lane < k) {
-            if (idx) idx[(size_t)t * k + lane] = my_e;
-            if (w) w[(size_t)t * k + lane] = my_p / psum;
-        }
-    }
+    router_rows_epilogue<TB>(a, lg, st_m, st_s, st_h, t0);
 }
 
 // --------------------------------------------------------------------------
 // Quantile bias: b_e = -(v_lo + frac (v_hi - v_lo)) with v_lo, v_hi the
 // order statistics of rank lo and lo+1 of column e (linear interpolation,
-// h = (T-1) q, lo = floor h, frac = h - lo).  One CTA per expert; exact
-// order statistics by a 4-pass radix select on the fp32 bit patterns
-// (probabilities are >= 0, so bit order equals value order).
+// h = (T-1) q, lo = floor h, frac = h - lo).  One CTA of 512 threads per
+// expert.  v_lo by a 3-pass radix select on the fp32 bit patterns (11, 11
+// and 10 bits; probabilities are >= 0, so bit order equals value order);
+// v_hi from one more pass: v_lo again if at least lo + 2 values are <= v_lo,
+// else the smallest value above it.
 // --------------------------------------------------------------------------
-__device__ float radix_select_col(const float *col, int T, long long r, unsigned *hist,
-                                  unsigned *sh) {
+
+// Exclusive scan of one value per thread of a 512-thread block; *total gets
+// the block sum.  warp_tot holds 16 ints.
+__device__ int block_exclusive_scan_512(int v, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int wt = lane < 16 ? warp_tot[lane] : 0;
+        int wi = wt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        if (lane < 16) warp_tot[lane] = wi - wt;
+        if (lane == 15) *total = wi;
+    }
+    __syncthreads();
+    const int r = warp_tot[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+constexpr int kRadixBins = 2048;
+
+// Shared scratch of the 512-thread radix select.
+struct RadixScratch {
+    unsigned hist[kRadixBins];
+    int warp_tot[16];
+    int total;
+    unsigned sel[2];
+};
+
+// Value of rank r (0-based, ascending) of col[0..T); 512 threads.
+__device__ float radix_select_col(const float *col, int T, long long r, RadixScratch &sc) {
     unsigned prefix = 0, mask = 0;
     const int tid = threadIdx.x, lane = tid & 31;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = shifts[pass];
+        const unsigned nb = 1u << widths[pass];
+        for (unsigned i = tid; i < kRadixBins; i += blockDim.x) sc.hist[i] = 0;
         __syncthreads();
         const int n = (T + blockDim.x - 1) / blockDim.x * blockDim.x;
         for (int i = tid; i < n; i += blockDim.x) {
-            unsigned bin = 256;
+            unsigned bin = 0xffffffffu;
             if (i < T) {
                 const unsigned b = __float_as_uint(col[i]);
-                if ((b & mask) == prefix) bin = (b >> shift) & 255u;
+                if ((b & mask) == prefix) bin = (b >> shift) & (nb - 1);
             }
             const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+            if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sc.hist[bin], __popc(peers));
         }
         __syncthreads();
-        if (tid == 0) {
-            unsigned long long cum = 0;
-            unsigned bin = 0;
-            for (; bin < 255; ++bin) {
-                if (cum + hist[bin] > (unsigned long long)r) break;
-                cum += hist[bin];
+        // thread tid owns bins [4 tid, 4 tid + 4): find the bin holding rank r
+        unsigned loc[4];
+        int local = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            loc[q] = sc.hist[4 * tid + q];
+            local += (int)loc[q];
+        }
+        const int ex = block_exclusive_scan_512(local, sc.warp_tot, &sc.total);
+        if ((long long)ex <= r && r < (long long)ex + local) {
+            long long cum = ex;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (r < cum + (long long)loc[q]) {
+                    sc.sel[0] = 4 * tid + q;
+                    sc.sel[1] = (unsigned)(r - cum);
+                    break;
+                }
+                cum += loc[q];
             }
-            sh[0] = bin;
-            sh[1] = (unsigned)(r - (long long)cum);
         }
         __syncthreads();
-        prefix |= sh[0] << shift;
-        mask |= 255u << shift;
-        r = sh[1];
+        prefix |= sc.sel[0] << shift;
+        mask |= (nb - 1) << shift;
+        r = sc.sel[1];
         __syncthreads();
     }
     return __uint_as_float(prefix);
@@ -483,36 +574,110 @@ __device__ float radix_select_col(const float *col, int T, long long r, unsigned
 __global__ void __launch_bounds__(512) quantile_bias_kernel(const float *probsT, int T,
                                                             long long lo, float frac,
                                                             float *bias_out) {
-    __shared__ unsigned hist[256];
-    __shared__ unsigned sh[2];
+    __shared__ RadixScratch sc;
+    __shared__ unsigned min_gt;
     const float *col = probsT + (size_t)blockIdx.x * T;
-    const float v_lo = radix_select_col(col, T, lo, hist, sh);
-    const float v_hi = (lo + 1 < T) ? radix_select_col(col, T, lo + 1, hist, sh) : v_lo;
+    const float v_lo = radix_select_col(col, T, lo, sc);
+    float v_hi = v_lo;
+    if (lo + 1 < T) {
+        if (threadIdx.x == 0) min_gt = 0xffffffffu;
+        __syncthreads();
+        const unsigned vb = __float_as_uint(v_lo);
+        int le = 0;
+        unsigned mn = 0xffffffffu;
+        for (int i = threadIdx.x; i < T; i += blockDim.x) {
+            const unsigned b = __float_as_uint(col[i]);
+            if (b <= vb) ++le;
+            else mn = min(mn, b);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        if ((threadIdx.x & 31) == 0) atomicMin(&min_gt, mn);
+        block_exclusive_scan_512(le, sc.warp_tot, &sc.total);
+        const long long n_le = sc.total;
+        v_hi = n_le >= lo + 2 ? v_lo : __uint_as_float(min_gt);
+    }
     if (threadIdx.x == 0) bias_out[blockIdx.x] = -(v_lo + frac * (v_hi - v_lo));
+}
+
+// --------------------------------------------------------------------------
+// Top-k from stored probabilities [T, E] plus a bias (second pass of
+// quantile balancing, and the plain top-k of the unbiased counts): one warp
+// per token, the row read coalesced, top-k from registers.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) select_rows_kernel(const float *probs, const float *bias,
+                                                          int T, int E, int k, int32_t *idx,
+                                                          float *w, int n_cand,
+                                                          int32_t *cand_idx, float *cand_w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float *row = probs + (size_t)t * E;
+    float sc[kTopkPerLane];
+#pragma unroll
+    for (int i = 0; i < kTopkPerLane; ++i) {
+        const int e = lane + 32 * i;
+        sc[i] = e < E ? row[e] + (bias ? bias[e] : 0.f) : -CUDART_INF_F;
+    }
+    float psum = 0.f, my_p = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < k + n_cand; ++j) {
+        const int bi = warp_take_max(sc, lane);
+        const float pw = row[bi];
+        if (j < k) psum += pw;
+        if (lane == j) { my_e = bi; my_p = pw; }
+    }
+    if (lane < k) {
+        if (idx) idx[(size_t)t * k + lane] = my_e;
+        if (w) w[(size_t)t * k + lane] = my_p / psum;
+    } else if (lane < k + n_cand) {
+        cand_idx[(size_t)t * n_cand + lane - k] = my_e;
+        cand_w[(size_t)t * n_cand + lane - k] = my_p / psum;
+    }
 }
 
 // --------------------------------------------------------------------------
 // Host launchers
 // --------------------------------------------------------------------------
 template <typename TX, int EP>
-static cudaError_t launch_small(const RouterArgs &a, cudaStream_t st) {
-    constexpr int TPW = 32 / EP, R = 32 / EP, DC = 32 * Vec<TX>::N * R;
-    const size_t smem = sizeof(float) * (EP * DC + 256);
-    auto kern = router_small_kernel<TX, EP>;
+static cudaError_t launch_partial(const RouterArgs &a, float *part, cudaStream_t st) {
+    constexpr int TPW = 32 / EP;
+    const size_t smem = sizeof(float) * EP * kRouterSlice;
+    auto kern = router_partial_kernel<TX, EP>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const int tok_per_cta = 8 * TPW;
-    const int grid = (a.T + tok_per_cta - 1) / tok_per_cta;
-    kern<<<grid, 256, smem, st>>>(a);
+    dim3 grid((a.T + tok_per_cta - 1) / tok_per_cta, router_slices(a.d));
+    kern<<<grid, 256, smem, st>>>(a, part);
     note_launch();
     return cudaGetLastError();
 }
 
-int router_blocks(int T, int E) {
-    if (E <= 8) return (T + 31) / 32;
-    if (E <= 16) return (T + 15) / 16;
-    if (E <= 32) return (T + 7) / 8;
-    return (T + kTB - 1) / kTB;
+// Tokens per CTA of the router's softmax kernels: 8 warps x 32/EP tokens for
+// E <= 32; for E > 32, kTB (fp32 SIMT router) or kTBLogits (bf16, softmax
+// over the tensor-core logits: 16 tokens so that several CTAs fit an SM).
+constexpr int kTBLogits = 16;
+static int router_tokens_per_block(int E, int dtype) {
+    if (E <= 8) return 32;
+    if (E <= 16) return 16;
+    if (E <= 32) return 8;
+    return dtype == MOE_DTYPE_BF16 ? kTBLogits : kTB;
+}
+
+// Blocks of the router's softmax kernels: the row count of the per-block
+// partial sums (p_partial, ent_partial).
+int router_blocks(int T, int E, int dtype) {
+    const int tb = router_tokens_per_block(E, dtype);
+    return (T + tb - 1) / tb;
+}
+
+template <int EP>
+static cudaError_t launch_small_epilogue(const RouterArgs &a, const float *part, int S,
+                                         cudaStream_t st) {
+    router_small_epilogue_kernel<EP><<<router_blocks(a.T, a.E, MOE_DTYPE_FP32), 256, 0, st>>>(
+        a, part, S);
+    note_launch();
+    return cudaGetLastError();
 }
 
 size_t router_smem_bytes(int E, int dtype) {
@@ -522,10 +687,17 @@ size_t router_smem_bytes(int E, int dtype) {
 }
 
 template <typename TX>
-static cudaError_t launch_router_t(const RouterArgs &a, cudaStream_t st) {
-    if (a.E <= 8) return launch_small<TX, 8>(a, st);
-    if (a.E <= 16) return launch_small<TX, 16>(a, st);
-    if (a.E <= 32) return launch_small<TX, 32>(a, st);
+static cudaError_t launch_router_t(const RouterArgs &a, float *part, cudaStream_t st) {
+    if (a.E <= 32) {
+        cudaError_t err = a.E <= 8    ? launch_partial<TX, 8>(a, part, st)
+                          : a.E <= 16 ? launch_partial<TX, 16>(a, part, st)
+                                      : launch_partial<TX, 32>(a, part, st);
+        if (err != cudaSuccess) return err;
+        const int S = router_slices(a.d);
+        return a.E <= 8    ? launch_small_epilogue<8>(a, part, S, st)
+               : a.E <= 16 ? launch_small_epilogue<16>(a, part, S, st)
+                           : launch_small_epilogue<32>(a, part, S, st);
+    }
     const size_t smem = router_tiled_smem(a.E);
     auto kern = router_tiled_kernel<TX>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -535,10 +707,10 @@ static cudaError_t launch_router_t(const RouterArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_router(const RouterArgs &a, int dtype, cudaStream_t st) {
+cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
-    return dtype == MOE_DTYPE_FP32 ? launch_router_t<float>(a, st)
-                                   : launch_router_t<__nv_bfloat16>(a, st);
+    return dtype == MOE_DTYPE_FP32 ? launch_router_t<float>(a, part, st)
+                                   : launch_router_t<__nv_bfloat16>(a, part, st);
 }
 
 cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp,
@@ -553,23 +725,22 @@ cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp,
 cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, int S,
                                       cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * ((size_t)kTB * a.E + 2 * kTB);
-    cudaError_t err = cudaFuncSetAttribute(router_from_logits_kernel,
+    constexpr int TB = kTBLogits;
+    const size_t smem = sizeof(float) * ((size_t)TB * a.E + 3 * TB);
+    cudaError_t err = cudaFuncSetAttribute(router_from_logits_kernel<TB>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    router_from_logits_kernel<<<(a.T + kTB - 1) / kTB, 256, smem, st>>>(a, part, S);
+    router_from_logits_kernel<TB><<<(a.T + TB - 1) / TB, 256, smem, st>>>(a, part, S);
     note_launch();
     return cudaGetLastError();
 }
 
-cudaError_t launch_select_from_probsT(const float *probsT, const float *bias, int T, int E,
-                                      int k, int32_t *idx, float *w, cudaStream_t st) {
+cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int E, int k,
+                               int32_t *idx, float *w, cudaStream_t st, int n_cand,
+                               int32_t *cand_idx, float *cand_w) {
     if (T == 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * (size_t)E * 33;
-    cudaError_t err = cudaFuncSetAttribute(select_from_probsT_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    select_from_probsT_kernel<<<(T + 31) / 32, 256, smem, st>>>(probsT, bias, T, E, k, idx, w);
+    select_rows_kernel<<<(T + 7) / 8, 256, 0, st>>>(probs, bias, T, E, k, idx, w, n_cand,
+                                                    cand_idx, cand_w);
     note_launch();
     return cudaGetLastError();
 }

@@ -37,14 +37,15 @@ def weights_dict(inp):
     return {k: inp.get(k) for k in moe._WEIGHT_KEYS}
 
 
-def gpu_layer(workload, T, inp, out_dtype=moe.DTYPE_FP32, want_unbiased=False, ws=None):
+def gpu_layer(workload, T, inp, out_dtype=moe.DTYPE_FP32, want_unbiased=False, ws=None,
+              want_slots=False):
     cfg = moe.config_for(workload, T, out_dtype)
     out = moe.layer_forward(cfg, inp["x"], weights_dict(inp), workspace=ws,
-                            want_unbiased_counts=want_unbiased)
+                            want_unbiased_counts=want_unbiased, want_slots=want_slots)
     torch.cuda.synchronize()
     assert moe.device_status() == 0
     return {k: (v.float().cpu().numpy() if v.dtype == torch.bfloat16 else v.cpu().numpy())
-            for k, v in out.items() if v is not None}
+            for k, v in out.items() if isinstance(v, torch.Tensor)}
 
 
 def act_dtype(workload) -> str:
@@ -54,7 +55,8 @@ def act_dtype(workload) -> str:
 
 def oracle_layer(workload, inp, tokens=None):
     return om.moe_forward(inp, workload.top_k, workload.act, workload.capacity_factor,
-                          "probs", workload.quantile_balance, tokens, act_dtype(workload))
+                          "probs", workload.quantile_balance, tokens, act_dtype(workload),
+                          reroute_rounds=workload.reroute_rounds)
 
 
 def tie_mask(r: "om.RouterOut", k: int, extra_abs: float = 0.0):

@@ -1,0 +1,156 @@
+"""GPU parity of expert-choice routing (each expert takes its top-C tokens;
+deepseekmodel.com TopKRouter discussion, iwashi.co routing table) against
+the fp64 oracle: the selection stage on the oracle's probabilities
+(bit-exact, ties by lower token index), the combine stage, and the whole
+layer on reduced and full sizes.
+
+Comparison: an expert's token set is bit-exact except for tokens whose
+probability for that expert is within 1e-6 (relative) of the expert's C-th
+largest value (ties of the fp32 and fp64 routers); those tokens and every
+token of such an expert's set are excused from the y comparison; y within
+1e-2 x RMS (bf16) / 1e-4 x RMS (fp32); f, p 1e-6; aux 1e-5 relative."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle.moe_oracle as om
+import sparse_mixture_experts_47_b300 as moe
+from tests.conftest import load_golden
+from tests.parity import FP_ATOL, act_dtype, sample_tokens, weights_dict, y_tol
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _ec_cfg(T, E, C):
+    cfg = moe.MoEConfig(T=T, d_model=8, n_experts=E, top_k=1, d_ff=8,
+                        capacity_factor=float(C) * E / T - 1e-6,
+                        routing=moe.ROUTING_EXPERT_CHOICE)
+    assert min(moe.capacity(cfg), T) == min(C, T)
+    return cfg
+
+
+def _stage_check(probs, C):
+    T, E = probs.shape
+    ref = om.expert_choice(probs, C)
+    cfg = _ec_cfg(T, E, C)
+    pt = torch.tensor(np.ascontiguousarray(probs.T), dtype=torch.float32, device=DEV)
+    out = moe.expert_choice(cfg, pt)
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    Cn = min(C, T)
+    got = out["perm"].cpu().numpy().reshape(E, Cn)
+    assert got.tolist() == ref.chosen.tolist()
+    assert np.array_equal(out["row_w"].cpu().numpy().reshape(E, Cn),
+                          ref.weight.astype(np.float32))
+    assert out["offsets"].cpu().numpy().tolist() == ref.offsets.tolist()
+    assert int(out["n_unchosen"][0]) == ref.n_unchosen
+    # per-token lists: expert order, rows pointing back at the token
+    ts = out["tok_start"].cpu().numpy()
+    tr = out["tok_rows"].cpu().numpy()
+    for t in range(T):
+        rows = tr[ts[t]:ts[t + 1]]
+        experts = rows // Cn
+        assert np.all(np.diff(experts) > 0)
+        assert np.all(got.reshape(-1)[rows] == t)
+        assert set(experts.tolist()) == {e for e in range(E) if t in set(ref.chosen[e].tolist())}
+    return out
+
+
+def test_expert_choice_golden_case():
+    g = load_golden("expert_choice_case.json")
+    probs = np.array(g["probs"], dtype=np.float32).astype(np.float64)
+    _stage_check(probs, g["C"])
+
+
+@pytest.mark.parametrize("T,E,C", [(1000, 8, 250), (4097, 8, 1025), (3000, 64, 100),
+                                    (2000, 896, 18), (5, 4, 9), (300, 16, 300)])
+def test_expert_choice_stage_bit_exact(T, E, C):
+    rng = np.random.default_rng(T * 7 + E)
+    logits = rng.normal(size=(T, E)) * 2
+    logits[::7] = np.round(logits[::7], 1)          # repeated values make exact ties
+    probs = om.softmax(logits).astype(np.float32).astype(np.float64)
+    _stage_check(probs, C)
+
+
+def test_combine_rows_stage():
+    rng = np.random.default_rng(4)
+    T, E, d, C = 300, 8, 64, 90
+    probs = om.softmax(rng.normal(size=(T, E))).astype(np.float32).astype(np.float64)
+    ref = om.expert_choice(probs, C)
+    cfg = _ec_cfg(T, E, C)
+    cfg = moe.MoEConfig(**{**cfg.__dict__, "d_model": d})
+    out = moe.expert_choice(cfg, torch.tensor(np.ascontiguousarray(probs.T), dtype=torch.float32,
+                                              device=DEV))
+    o = rng.normal(size=(E * C, d)).astype(np.float32)
+    sh = rng.normal(size=(T, d)).astype(np.float32)
+    y = moe.combine_rows(cfg, torch.tensor(o, device=DEV), out["row_w"], out["tok_start"],
+                         out["tok_rows"], torch.tensor(sh, device=DEV)).cpu().numpy()
+    yr = sh.astype(np.float64).copy()
+    for e in range(E):
+        for i, t in enumerate(ref.chosen[e]):
+            yr[t] += ref.weight[e, i] * o[e * C + i]
+    assert np.max(np.abs(y - yr)) <= 1e-5 * np.sqrt(np.mean(yr ** 2))
+
+
+def _layer_check(w, T, inp, tokens=None):
+    cfg = moe.config_for(w, T)
+    out = moe.layer_forward(cfg, inp["x"], weights_dict(inp))
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    orc = om.moe_forward_expert_choice(inp, w.top_k, w.act, w.capacity_factor, tokens,
+                                       act_dtype(w))
+    probs, ec = orc["probs"], orc["ec"]
+    Cn = ec.chosen.shape[1]
+    # near-tie tokens per expert: within 1e-6 relative of the Cn-th largest value
+    excused = np.zeros(T, dtype=bool)
+    for e in range(w.n_experts):
+        col = probs[:, e]
+        if Cn < T:
+            v = np.sort(col)[::-1][Cn - 1]
+            near = np.abs(col - v) <= 1e-6 * v
+            if near.sum() > 1:
+                excused |= near
+    st = orc["stats"]
+    assert np.array_equal(out["counts"].cpu().numpy(), st["counts"])
+    assert np.max(np.abs(out["f"].cpu().numpy() - st["f"])) <= FP_ATOL
+    assert np.max(np.abs(out["p"].cpu().numpy() - st["p"])) <= FP_ATOL
+    assert abs(float(out["aux"][0]) - st["aux"]) <= 1e-5 * st["aux"]
+    if not excused.any():
+        assert int(out["n_dropped"][0]) == ec.n_unchosen
+    rows = orc["rows"]
+    yg = out["y"].float().cpu().numpy()[rows].astype(np.float64)
+    keep = ~excused[rows]
+    rms = float(np.sqrt(np.mean(orc["y"] ** 2)))
+    err = float(np.max(np.abs(yg[keep] - orc["y"][keep])))
+    assert err <= y_tol(w) * rms, (err, rms)
+    return {"excused": int(excused.sum()), "y_err_over_rms": err / rms,
+            "unchosen": ec.n_unchosen}
+
+
+SMALL = {
+    "mixtral_ec_small": (mi.workload("mixtral_ec").with_sizes(d_model=512, d_ff=1024), 300),
+    "mixtral_ec_T3": (mi.workload("mixtral_ec").with_sizes(d_model=256, d_ff=512), 3),
+    "tiny_ec": (mi.workload("tiny").with_sizes(capacity_factor=1.0, routing="expert"), 64),
+    "deepseek_ec_small": (mi.workload("deepseek").with_sizes(
+        d_model=256, n_experts=64, d_ff=128, d_ff_shared=192, capacity_factor=1.0,
+        routing="expert", select_bias="none"), 400),
+    "e896_ec_small": (mi.workload("e896").with_sizes(d_model=128, d_ff=64, capacity_factor=1.0,
+                                                     routing="expert", quantile_balance=False),
+                      2000),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_expert_choice_small(name):
+    w, T = SMALL[name]
+    inp = mi.generate(w, T, DEV)
+    print(name, _layer_check(w, T, inp))
+
+
+def test_layer_expert_choice_full_size():
+    w = mi.workload("mixtral_ec")
+    T = 4096
+    inp = mi.generate(w, T, DEV)
+    print(_layer_check(w, T, inp, sample_tokens(T, 96)))

@@ -14,7 +14,8 @@ DEV = "cuda"
 
 FULL = [("switch", 8192, None), ("mixtral", 1, None), ("mixtral", 16, None),
         ("mixtral", 4096, 192), ("mixtral", 16384, 192), ("deepseek", 128, None),
-        ("deepseek", 8192, 96), ("e896", 16384, 96)]
+        ("deepseek", 8192, 96), ("e896", 16384, 96), ("mixtral_cap", 4096, 192),
+        ("deepseek_cap", 8192, 96)]
 
 
 @pytest.mark.parametrize("name,T,n_sample", FULL, ids=[f"{n}-T{T}" for n, T, _ in FULL])
@@ -24,6 +25,8 @@ def test_layer_full_size(name, T, n_sample):
     tokens = None if n_sample is None else sample_tokens(T, n_sample)
     rep, gpu, orc = full_check(w, T, inp, tokens)
     print(name, T, rep)
+    if w.capacity_factor > 0:
+        assert int(gpu["n_dropped"][0]) > 0
     if name == "switch":
         C = om.capacity(T, w.top_k, w.n_experts, w.capacity_factor)
         assert C == 1280
