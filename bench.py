@@ -190,10 +190,19 @@ def blas_threads():
         return os.cpu_count()
 
 
-def sample_size(w):
-    # about 10-30 s of fp64 CPU work per timed sample on a many-core host
-    per_token = 2.0 * (3 if w.act == "swiglu" else 2) * w.d_model * w.d_ff * w.top_k
-    return int(max(8, min(512, 4e10 / per_token)))
+def calibrated_sample(w, inp64, T, target_s):
+    """Tokens S for which one oracle run on the first S tokens takes about
+    target_s seconds on this host: a line t = a + b S through timed runs at
+    8 and 32 tokens, capped at T."""
+    s1, s2 = min(T, 8), min(T, 32)
+    oracle_sample_run(w, inp64, s1)
+    t1 = oracle_sample_run(w, inp64, s1)
+    if s2 == s1:
+        return s1
+    t2 = oracle_sample_run(w, inp64, s2)
+    b = max((t2 - t1) / (s2 - s1), 1e-9)
+    a = max(t1 - b * s1, 0.0)
+    return int(max(s1, min(T, (target_s - a) / b)))
 
 
 # --------------------------------------------------------------------------- arms
@@ -202,9 +211,11 @@ def run_reference(args, w, T):
     # Under torchrun only rank 0 times the oracle; the other ranks exit at once.
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    S = min(T, sample_size(w))
-    inp = mi.generate(w, S, "cpu")
+    # each step a bounded sample: about 4 s, so that warm-up and timed steps
+    # end within a few minutes
+    inp = mi.generate(w, T, "cpu")
     inp64 = host_inputs_f64(inp)
+    S = calibrated_sample(w, inp64, T, 4.0)
     for _ in range(args.warmup):
         oracle_sample_run(w, inp64, S)
     times = [oracle_sample_run(w, inp64, S) for _ in range(args.steps)]
@@ -418,8 +429,8 @@ def run_ours(args, w, T):
         return
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        S = min(T, sample_size(w))
-        inp64 = host_inputs_f64({k: (v[:S] if k == "x" else v) for k, v in inp.items()})
+        inp64 = host_inputs_f64(inp)
+        S = calibrated_sample(w, inp64, T, 15.0)      # about 15 s of CPU work
         t = oracle_sample_run(w, inp64, S)
         cpu = {"value": S / t, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"first {S} of the {T} tokens as one batch (routing, dispatch, "
