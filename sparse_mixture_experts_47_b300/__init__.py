@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "MoEConfig", "MoEError", "lib", "capacity", "workspace_size", "router_topk", "dispatch",
     "expert_ffn", "combine", "load_stats", "layer_forward", "device_status", "Workspace",
-    "LayerGraph", "observe", "OBS_KEYS", "dispatch_reroute", "reroute_candidates",
+    "LayerGraph", "LayerPipeline", "observe", "OBS_KEYS", "dispatch_reroute", "reroute_candidates",
     "ROUTING_TOKEN_CHOICE", "ROUTING_EXPERT_CHOICE", "expert_choice", "expert_choice_rows",
     "combine_rows",
     "ACT_RELU", "ACT_SWIGLU", "DTYPE_FP32", "DTYPE_BF16", "SELECT_PROBS", "SELECT_LOGITS",
@@ -445,6 +445,70 @@ class LayerGraph:
         """Enqueue the captured layer on torch's current stream."""
         self.graph.replay()
         return self.outputs
+
+
+class LayerPipeline:
+    """The layer over a sequence of host batches, copies overlapped.
+
+    Each batch goes host→device, through one replay of a captured layer, and
+    its output back device→host.  The three run on separate CUDA streams
+    with two device buffers per side, so the copy in of batch i+1 and the
+    copy out of batch i-1 overlap the layer on batch i.  Host tensors should
+    be pinned, shaped [T, d] in the layer dtype (inputs) and the output dtype
+    (outputs).  Batches under a megabyte run copies and layer in sequence on
+    the current stream instead."""
+
+    def __init__(self, cfg: MoEConfig, weights: Dict[str, Optional[torch.Tensor]], device,
+                 workspace: Optional[Workspace] = None):
+        dev = torch.device(device)
+        self.cfg = cfg
+        self.workspace = workspace or Workspace(dev)
+        xs = [torch.zeros((cfg.T, cfg.d_model), dtype=cfg.torch_dtype, device=dev)
+              for _ in range(2)]
+        # both graphs share the workspace: they never run at the same time
+        self.graphs = [LayerGraph(cfg, x, weights, workspace=self.workspace) for x in xs]
+        self.streams = [torch.cuda.Stream(dev) for _ in range(3)]     # in, layer, out
+        self.ev = [[torch.cuda.Event() for _ in range(2)] for _ in range(3)]
+
+    # Below this batch size (bytes in) the copies take a few microseconds and
+    # the cross-stream waits cost more than the overlap saves: one stream.
+    OVERLAP_MIN_BYTES = 1 << 20
+
+    def run(self, xs_host, ys_host) -> None:
+        """Enqueue batch i = xs_host[i] -> ys_host[i] for every i (no host
+        synchronisation; synchronise the device before reading ys_host)."""
+        s_in, s_layer, s_out = self.streams
+        ev_in, ev_layer, ev_out = self.ev
+        cur = torch.cuda.current_stream(s_in.device)
+        g0 = self.graphs[0]
+        if g0.x.numel() * g0.x.element_size() < self.OVERLAP_MIN_BYTES:
+            for xh, yh in zip(xs_host, ys_host):
+                g0.x.copy_(xh, non_blocking=True)
+                g0.replay()
+                yh.copy_(g0.outputs["y"], non_blocking=True)
+            return
+        for s in self.streams:
+            s.wait_stream(cur)
+        for i, (xh, yh) in enumerate(zip(xs_host, ys_host)):
+            b = i % 2
+            g = self.graphs[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_layer[b])      # batch i-2 has read this buffer
+                g.x.copy_(xh, non_blocking=True)
+                ev_in[b].record(s_in)
+            with torch.cuda.stream(s_layer):
+                s_layer.wait_event(ev_in[b])
+                if i >= 2:
+                    s_layer.wait_event(ev_out[b])     # batch i-2's output is copied out
+                g.replay()
+                ev_layer[b].record(s_layer)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_layer[b])
+                yh.copy_(g.outputs["y"], non_blocking=True)
+                ev_out[b].record(s_out)
+        for s in self.streams:
+            cur.wait_stream(s)
 
 
 STAGES = ("router", "dispatch", "stats", "gather", "up", "down", "shared", "combine")

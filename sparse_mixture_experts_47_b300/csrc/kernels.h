@@ -31,7 +31,7 @@ inline int router_slices(int d) { return (d + kRouterSlice - 1) / kRouterSlice; 
 int router_blocks(int T, int E, int dtype);
 size_t router_smem_bytes(int E, int dtype);
 cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStream_t st);
-cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp,
+cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp, int parts,
                                        __nv_bfloat16 *out, cudaStream_t st);
 cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, int S,
                                       cudaStream_t st);

@@ -255,7 +255,16 @@ __global__ void gather_rows_kernel(const uint4 *x, int vec_per_row, const int32_
     const long long t = perm[s] / k;
     const uint4 *src = x + t * vec_per_row;
     uint4 *dst = xs + s * vec_per_row;
-    for (int i = lane; i < vec_per_row; i += 32) dst[i] = src[i];
+    // four 16-byte loads in flight per lane before the stores
+    int i = lane;
+    for (; i + 96 < vec_per_row; i += 128) {
+        const uint4 a = src[i], b = src[i + 32], c = src[i + 64], d = src[i + 96];
+        dst[i] = a;
+        dst[i + 32] = b;
+        dst[i + 64] = c;
+        dst[i + 96] = d;
+    }
+    for (; i < vec_per_row; i += 32) dst[i] = src[i];
 }
 
 cudaError_t launch_gather_rows(const void *x, int elem_bytes, int d, const int32_t *perm,

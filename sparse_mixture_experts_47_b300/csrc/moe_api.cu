@@ -72,20 +72,25 @@ Sizes sizes(const moe_config *c) {
 }
 
 // Router logits on the tensor cores (bf16 x, E > 32, E % 4 == 0): W_r split
-// into three bf16 parts over a 3*dp reduction.  The tensor core's fp32
-// accumulation loses a little with every step of a long chain (measured on
-// B300: logit error up to 1.3e-4 over one 192-block chain, 1e-5 over chains of
-// about 20 blocks, where the fp32 CUDA-core router reaches 1.4e-5), so the
-// reduction is cut into S chains of at most 16 K blocks, each written as an
-// fp32 partial plane and summed in fixed order.  S depends on d only, so a
-// token's logits do not depend on the batch it comes in (batch invariance).
+// into kRouterParts bf16 parts over a kRouterParts*dp reduction.  Two parts
+// (hi + lo) leave a residual of at most 2^-18 |w| per weight, a logit error
+// of about 2e-6 rms at d = 4096, the size of the fp32 CUDA-core router's
+// rounding.  The tensor
+// core's fp32 accumulation loses a little with every step of a long chain
+// (measured on B300: logit error up to 1.3e-4 over one 192-block chain, 1e-5
+// over chains of about 20 blocks, where the fp32 CUDA-core router reaches
+// 1.4e-5), so the reduction is cut into S chains of at most 16 K blocks, each
+// written as an fp32 partial plane and summed in fixed order.  S depends on
+// d only, so a token's logits do not depend on the batch it comes in (batch
+// invariance).
 bool tc_router(const moe_config *c) {
     return c->dtype == MOE_DTYPE_BF16 && c->n_experts > 32 && c->n_experts % 4 == 0;
 }
 long long router_dp(const moe_config *c) { return (c->d_model + 63) / 64 * 64; }
 constexpr int kRouterChainBlocks = 16;
+constexpr int kRouterParts = 2;
 int router_splits(const moe_config *c) {
-    const long long nk = 3 * router_dp(c) / 64;
+    const long long nk = kRouterParts * router_dp(c) / 64;
     const long long S = (nk + kRouterChainBlocks - 1) / kRouterChainBlocks;
     const long long kbps = (nk + S - 1) / S;
     return (int)((nk + kbps - 1) / kbps);
@@ -102,9 +107,15 @@ struct FfnPlan {
 };
 constexpr int kPlanSMs = 148;   // SM count the split choice assumes (B300)
 
+// Split the reduction only when the tiles do not fill the SMs once, and then
+// only up to one round of work items: measured at the Mixtral shape, a split
+// that spreads the items over more rounds, or any split of the up projection
+// at T = 1 and 16, costs more in partial sums than it gains in balance, while
+// splitting the down projection at T = 1 (64 tiles) in two cuts it from 68
+// to 45 us.
 int split_count(long long tiles, long long nk) {
-    if (tiles <= 0 || nk <= 0) return 1;
-    long long S = (2 * kPlanSMs + tiles - 1) / tiles;
+    if (tiles <= 0 || nk <= 0 || tiles >= kPlanSMs) return 1;
+    long long S = kPlanSMs / tiles;
     S = std::min<long long>(S, std::min<long long>(16, std::max<long long>(1, nk / 8)));
     const long long kbps = (nk + S - 1) / S;
     return (int)((nk + kbps - 1) / kbps);
@@ -190,7 +201,7 @@ Layout layout(const moe_config *c) {
     L.sh_h = take(eb * s.T * s.Fs);
     L.sh_out = take(sizeof(float) * sp.s_down * s.T * s.d);
     const bool rt = tc_router(c);
-    L.rt_wsplit = take(rt ? 2 * s.E * 3 * router_dp(c) : 0);
+    L.rt_wsplit = take(rt ? 2 * s.E * kRouterParts * router_dp(c) : 0);
     const long long planes =
         rt ? router_splits(c) : (s.E <= 32 ? router_slices((int)s.d) : 0);
     L.rt_logits = take(sizeof(float) * planes * s.T * s.E);
@@ -341,12 +352,13 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         int32_t *off = at<int32_t>(ws, L.rt_offsets);
         int32_t *te = at<int32_t>(ws, L.rt_tile_e), *ts = at<int32_t>(ws, L.rt_tile_start);
         int32_t *nt = at<int32_t>(ws, L.rt_ntiles);
-        MOE_CUDA(launch_split_router_weight(w_r, a.E, a.d, dp, wsplit, st));
+        MOE_CUDA(launch_split_router_weight(w_r, a.E, a.d, dp, kRouterParts, wsplit, st));
         set_pair_kernel<<<1, 1, 0, st>>>(off, 0, a.T);
         note_launch();
         MOE_CUDA(cudaGetLastError());
         MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E, 3 * dp,
+        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E,
+                                kRouterParts * dp,
                                 dp, S, s.T * s.E, te, ts, nt, off, part, a.E, st));
         int planes = S;
         if (S > 1) {       // a wide kernel adds the planes (same order), streaming

@@ -419,28 +419,27 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
 }
 
 // --------------------------------------------------------------------------
-// Tensor-core router support.  W_r (fp32) is split exactly into three bf16
-// parts, w = hi + mid + lo (8 + 8 + 8 significant bits, residual at most
-// 2^-24 |w|), laid out as one [E, 3*dp] bf16 matrix (dp = d rounded up to 64,
-// zero padded), so that x W_r^T = x [hi|mid|lo]^T over a 3*dp reduction with
-// x's column taken mod dp.  bf16 x bf16 products are exact in fp32.
+// Tensor-core router support.  W_r (fp32) is split into `parts` bf16 parts,
+// each the nearest bf16 of what the earlier parts leave (two parts: w = hi +
+// lo + r with |r| <= 2^-18 |w|; three: |r| <= 2^-24 |w|), laid out as one
+// [E, parts*dp] bf16 matrix (dp = d rounded up to 64, zero padded), so that
+// x W_r^T = x [hi|lo|..]^T over a parts*dp reduction with x's column taken
+// mod dp.  bf16 x bf16 products are exact in fp32.
 // --------------------------------------------------------------------------
-__global__ void split_router_weight_kernel(const float *w_r, int E, int d, int dp,
+__global__ void split_router_weight_kernel(const float *w_r, int E, int d, int dp, int parts,
                                            __nv_bfloat16 *out) {
     const long long n = (long long)E * dp;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         const int e = (int)(i / dp), c = (int)(i % dp);
-        const float w = c < d ? w_r[(size_t)e * d + c] : 0.f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-        const float r1 = w - __bfloat162float(hi);
-        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-        const float r2 = r1 - __bfloat162float(mid);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-        __nv_bfloat16 *row = out + (size_t)e * 3 * dp;
-        row[c] = hi;
-        row[dp + c] = mid;
-        row[2 * dp + c] = lo;
+        float r = c < d ? w_r[(size_t)e * d + c] : 0.f;
+        __nv_bfloat16 *row = out + (size_t)e * parts * dp;
+        // each part is the round-to-nearest bf16 of what the earlier parts left
+        for (int q = 0; q < parts; ++q) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(r);
+            row[q * dp + c] = b;
+            r -= __bfloat162float(b);
+        }
     }
 }
 
@@ -713,11 +712,11 @@ cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStrea
                                    : launch_router_t<__nv_bfloat16>(a, part, st);
 }
 
-cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp,
+cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp, int parts,
                                        __nv_bfloat16 *out, cudaStream_t st) {
     const long long n = (long long)E * dp;
     const int grid = (int)std::min<long long>((n + 255) / 256, 148 * 8);
-    split_router_weight_kernel<<<grid, 256, 0, st>>>(w_r, E, d, dp, out);
+    split_router_weight_kernel<<<grid, 256, 0, st>>>(w_r, E, d, dp, parts, out);
     note_launch();
     return cudaGetLastError();
 }

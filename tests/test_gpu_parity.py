@@ -31,6 +31,7 @@ SMALL = {
     "mixtral_T1_split": (mi.workload("mixtral").with_sizes(d_model=1024, d_ff=2048), 1),
     "mixtral_T5_split": (mi.workload("mixtral").with_sizes(d_model=1024, d_ff=2048), 5),
     "switch_T20_split": (mi.workload("switch").with_sizes(d_model=1024, d_ff=2048), 20),
+    "switch_T3_split": (mi.workload("switch").with_sizes(d_model=2048, d_ff=512), 3),
     "deepseek_T100_split": (mi.workload("deepseek").with_sizes(d_model=1024, n_experts=64,
                                                                d_ff=256, d_ff_shared=1024), 100),
     # capacity factor 1.0 with k > 1: overflow dropped in (t, j) order
@@ -46,7 +47,7 @@ def test_layer_small_full_oracle(name):
     inp = mi.generate(w, T, DEV)
     rep, gpu, orc = full_check(w, T, inp)
     print(name, rep)
-    if w.capacity_factor > 0:
+    if w.capacity_factor > 0 and T >= 16:
         assert orc["dispatch"].n_dropped > 0          # the skewed expert overflows
 
 
@@ -85,6 +86,34 @@ def test_batch_invariance(name, T):
         assert np.array_equal(small["w"], big["w"][:t])
         rms = float(np.sqrt(np.mean(big["y"].astype(np.float64) ** 2)))
         assert np.max(np.abs(small["y"] - big["y"][:t])) <= y_tol(w) * rms
+
+
+def test_layer_graph_and_pipeline_match_eager():
+    """The captured layer (LayerGraph) and the copy-overlapped pipeline
+    (LayerPipeline) give exactly the eager call's outputs, batch by batch."""
+    w, T = SMALL["mixtral_small"]
+    inp = mi.generate(w, T, DEV)
+    cfg = moe.config_for(w, T, moe.DTYPE_BF16)
+    wts = weights_dict(inp)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(11)
+    batches = [torch.randn(inp["x"].shape, generator=g, device=DEV).to(inp["x"].dtype)
+               for _ in range(5)]
+    eager = [moe.layer_forward(cfg, b, wts)["y"].float().cpu() for b in batches]
+    graph = moe.LayerGraph(cfg, batches[0].clone(), wts)
+    for b, ref in zip(batches, eager):
+        graph.x.copy_(b)
+        assert torch.equal(graph.replay()["y"].float().cpu(), ref)
+    xs = [b.cpu().pin_memory() for b in batches]
+    for overlap in (True, False):      # three streams, and the one-stream path
+        pipe = moe.LayerPipeline(cfg, wts, DEV)
+        pipe.OVERLAP_MIN_BYTES = 0 if overlap else 1 << 62
+        ys = [torch.empty((T, w.d_model), dtype=torch.bfloat16).pin_memory() for _ in batches]
+        pipe.run(xs, ys)
+        torch.cuda.synchronize()
+        assert moe.device_status() == 0
+        for y, ref in zip(ys, eager):
+            assert torch.equal(y.float(), ref)
 
 
 def test_empty_batch():
