@@ -201,7 +201,10 @@ int moe_expert_choice(const moe_config *cfg, const float *probs_t,
 
 /* Combine over per-token row lists (expert choice):
  * y[t] = sum_{i in [tok_start[t], tok_start[t+1])} row_w[r_i] out_sorted[r_i]
- *        + shared_out[t], in list order.  out_sorted [rows, d] fp32. */
+ *        + shared_out[t], in list order.  out_sorted [rows, d] fp32.  In a
+ * bf16 layer each out_sorted and shared_out value is first rounded to the
+ * nearest bf16 (expert outputs are bf16 tensors there; no-op on the output
+ * of moe_expert_ffn). */
 int moe_combine_rows(const moe_config *cfg, const float *out_sorted,
                      const float *row_w, const int32_t *tok_start,
                      const int32_t *tok_rows, const float *shared_out, void *y,
@@ -233,7 +236,9 @@ int moe_dispatch_static(const moe_config *cfg, const int32_t *topk_idx,
 
 /* Per-expert FFN on the grouped rows: out_sorted[s] = FFN_e(x[perm[s] / k])
  * for offsets[e] <= s < offsets[e+1] (expert choice: x[perm[s]]).
- * Source: ch. 30 §30.2.4 / §30.6.1.
+ * Source: ch. 30 §30.2.4 / §30.6.1.  fp32 accumulation; in a bf16 layer h
+ * and the output row are bf16 values (rounded once to nearest even; the
+ * output held in fp32 here), as the layer's modules return in a bf16 model.
  *   x          [T, d]; perm, offsets as produced by moe_dispatch (or
  *              moe_dispatch_reroute, moe_expert_choice)
  *   w1, w3, w2 expert weights (w3 NULL for ReLU)
@@ -246,7 +251,9 @@ int moe_expert_ffn(const moe_config *cfg, const void *x, const int32_t *perm,
 
 /* Combine: y[t] = sum_j [inv[t*k+j] >= 0] w[t,j] out_sorted[inv[t*k+j]]
  *               + shared_out[t].   Source: ch. 30 §30.6.1 (weighted
- * accumulate), §30.4.5 (routed + shared).
+ * accumulate), §30.4.5 (routed + shared).  fp32 accumulation; in a bf16
+ * layer out_sorted and shared_out values are first rounded to bf16 as in
+ * moe_combine_rows.
  *   out_sorted [*, d] fp32; inv [T*k]; topk_w [T, k]
  *   shared_out [T, d] fp32 or NULL;  y [T, d] in cfg->out_dtype */
 int moe_combine(const moe_config *cfg, const float *out_sorted,
@@ -294,7 +301,11 @@ typedef struct {
 
 /* The whole forward pass (router, dispatch, experts, shared expert,
  * combine, statistics) on one stream, with no host synchronisation.
- * Source: ch. 30 §30.6.1 MoELayer.forward returning (output, aux_loss). */
+ * Source: ch. 30 §30.6.1 MoELayer.forward returning (output, aux_loss).
+ * Precision: fp32 accumulation throughout; in a bf16 layer the activation h
+ * and each expert's output row (routed and shared) are bf16 values, rounded
+ * once, before the fp32 weighted combine: the results of the stage calls
+ * moe_expert_ffn and moe_combine. */
 int moe_layer_forward(const moe_config *cfg, const void *x,
                       const moe_layer_weights *wts,
                       const moe_layer_outputs *out, void *ws,

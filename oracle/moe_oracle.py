@@ -386,6 +386,7 @@ def moe_forward_expert_choice(inp: Dict, k: int, act: str, capacity_factor: floa
     rows = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     pos = {int(t): i for i, t in enumerate(rows)}
     y = np.zeros((rows.shape[0], x.shape[1]))
+    y_abs = np.zeros_like(y)       # sum of |terms| of y, for rounding-aware comparisons
     for e in range(E):
         sel = [(n, int(t)) for n, t in enumerate(ec.chosen[e]) if int(t) in pos]
         if not sel:
@@ -395,9 +396,13 @@ def moe_forward_expert_choice(inp: Dict, k: int, act: str, capacity_factor: floa
                          inp["w2"][e], act, act_dtype)
         for i, (n, t) in enumerate(sel):
             y[pos[t]] += ec.weight[e, n] * out[i]
+            y_abs[pos[t]] += np.abs(ec.weight[e, n] * out[i])
     if inp.get("ws1") is not None:
-        y += expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
-    return {"probs": probs, "ec": ec, "stats": stats, "capacity": C, "rows": rows, "y": y}
+        sh = expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
+        y += sh
+        y_abs += np.abs(sh)
+    return {"probs": probs, "ec": ec, "stats": stats, "capacity": C, "rows": rows, "y": y,
+            "y_abs": y_abs}
 
 
 # --------------------------------------------------------------------------
@@ -433,8 +438,10 @@ def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str, act_dtype: str = "fp64"
 
     SwiGLU: w2(silu(w1 x) * w3 x)  ([MoE-ch30] §30.2.4), ReLU: w2(relu(w1 x)).
     Weights are nn.Linear-shaped: w1, w3 [F, d], w2 [d, F]; no biases.
-    ``act_dtype`` is the storage type of the intermediate activation h
-    (reading R8): "fp64" keeps it exact, "fp32"/"bf16" round it once.
+    ``act_dtype`` is the layer's storage type (reading R8): the intermediate
+    activation h and the expert's output row are tensors of that type (the
+    Expert module's result in [MoE-ch30] §30.6.1 MoELayer.forward), each
+    rounded once; "fp64" keeps both exact.  Products and sums are exact.
     """
     a = x_rows @ _f64(w1).T
     if act == "swiglu":
@@ -444,7 +451,7 @@ def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str, act_dtype: str = "fp64"
     else:
         raise ValueError(act)
     h = ACT_ROUNDING[act_dtype](h)
-    return h @ _f64(w2).T
+    return ACT_ROUNDING[act_dtype](h @ _f64(w2).T)
 
 
 # --------------------------------------------------------------------------
@@ -555,6 +562,7 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
     st = load_stats(r.probs, r.idx, E)
     rows = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     y = np.zeros((rows.shape[0], x.shape[1]))
+    y_abs = np.zeros_like(y)       # sum of |terms| of y, for rounding-aware comparisons
     pos = {int(t): i for i, t in enumerate(rows)}
     groups: Dict[int, list] = {}
     for t in rows:
@@ -570,9 +578,13 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
         outputs[e] = out
         for n, (t, _) in enumerate(tj):
             y[pos[int(t)]] += ww[n] * out[n]
+            y_abs[pos[int(t)]] += np.abs(ww[n] * out[n])
     if inp.get("ws1") is not None:
-        y += expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
-    res = {"router": r, "dispatch": dp, "stats": st, "capacity": C, "rows": rows, "y": y}
+        sh = expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
+        y += sh
+        y_abs += np.abs(sh)
+    res = {"router": r, "dispatch": dp, "stats": st, "capacity": C, "rows": rows, "y": y,
+           "y_abs": y_abs}
     if observe_outputs:
         assert tokens is None, "observability needs every token"
         res["observe"] = observe(r, dp, outputs, E, k)

@@ -28,6 +28,10 @@
 // against a narrow token tile instead of padding 128 token rows.  The
 // reduction can then be split over CTAs (k_splits): each split writes fp32
 // partial sums that a later kernel adds in split order.
+// NT = 256 (down projection only) is the same swapped pipeline with the
+// MMA's N chosen per tile: a tile holds up to 256 of one expert's rows and
+// its MMA N is that count rounded up to 16, so an expert with 146 rows costs
+// a 160-wide tile instead of two 128-row tiles.
 // Every mbarrier wait is bounded (about 2 s of no progress); on expiry the
 // kernel sets the device error word, stops issuing, lets its own copies and
 // MMAs land, frees TMEM and returns.
@@ -47,6 +51,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 256;        // columns of one of the two accumulators
 constexpr int kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KB)
 constexpr int kSmemExtra = 1024 /* alignment slack */ + 256 /* barriers */;
+constexpr int kVarRows = 256;        // NT of the per-tile-width geometry
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 
 // Tile geometry of one kernel instantiation.  NT = 0: token rows on the M
@@ -56,6 +61,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 // weight tile(s); every tile is a multiple of 1024 bytes.
 template <int MODE, int NT, int BN> struct Geo {
     static constexpr bool SWAP = NT > 0;
+    static constexpr bool VARN = NT == kVarRows;                 // MMA N chosen per tile
+    static_assert(!VARN || MODE == GEMM_DOWN, "per-tile width: down projection only");
     static constexpr int ROWS = SWAP ? NT : BM;                  // activation rows per tile
     static constexpr int WT = (SWAP && MODE == GEMM_UP_SWIGLU) ? 2 : 1;
     // rows of one weight TMA box: 128 (NT > 0), BN / 2 (NT = 0: two boxes)
@@ -75,7 +82,7 @@ struct Args {
     int N;             // output columns
     int K;             // reduction length (B's columns)
     int a_k_period;    // A's column of reduction index k is k mod a_k_period
-    int n_ntiles;      // N-tiles of the output (128 cols for SwiGLU, 256 otherwise)
+    int n_ntiles;      // output-column tiles (OUTC columns each)
     int b_rows;        // weight rows per expert (F for up, d for down)
     int k_splits;      // work items per output tile along K
     int kb_per_split;  // K blocks of one split
@@ -83,6 +90,7 @@ struct Args {
     const int32_t *tile_e, *tile_start, *n_mtiles, *offsets;
     void *C;
     int ldc;
+    int out_mode;      // GEMM_DOWN, one split: kOutF32, kOutBF16, kOutF32Rounded
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -219,6 +227,14 @@ __device__ __forceinline__ TileCoord decode_tile(const Args &g, int L, int tiles
     return c;
 }
 
+// Token rows a tile covers, rounded up to the MMA's N granularity of 16
+// (NT = 256 geometry; rows past the expert's end are computed, never stored).
+template <int ROWS>
+__device__ __forceinline__ int tile_n16(const TileCoord &c) {
+    const int r = min(ROWS, c.mend - c.m0);
+    return (r + 15) & ~15;
+}
+
 __device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
     uint4 u;
     uint32_t *w = reinterpret_cast<uint32_t *>(&u);
@@ -233,6 +249,9 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
 template <int MODE, int NT, int BN>
 __global__ void __launch_bounds__(256, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmA64,
+                       const __grid_constant__ CUtensorMap tmA32,
+                       const __grid_constant__ CUtensorMap tmA16,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, Args g) {
     using G = Geo<MODE, NT, BN>;
@@ -290,13 +309,32 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             if (G::SWAP) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
             else if (MODE == GEMM_UP_SWIGLU) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
             else { b0 = c.e * g.b_rows + c.n0; b1 = b0 + BN / 2; }
+            const int n16 = G::VARN ? tile_n16<G::ROWS>(c) : G::ROWS;
+            const uint32_t stage_tx = G::W_BYTES + n16 * BK * 2;
             for (int kb = c.kb0; kb < c.kb1; ++kb) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
-                mbar_expect_tx(fb, G::STAGE_BYTES);
+                mbar_expect_tx(fb, stage_tx);
                 const uint32_t sa = smem_u32(smem + stage * G::STAGE_BYTES);
                 const uint32_t sb = sa + G::ACT_BYTES;
-                tma_load_2d(sa, &tmA, (kb * BK) % g.a_k_period, c.m0, fb);
+                const int ka = (kb * BK) % g.a_k_period;
+                if (G::VARN) {
+                    // n16 token rows as boxes of 128, 64, 32 and 16 rows
+                    int r = 0;
+                    for (; r + 128 <= n16; r += 128)
+                        tma_load_2d(sa + r * BK * 2, &tmA, ka, c.m0 + r, fb);
+                    if (n16 - r >= 64) {
+                        tma_load_2d(sa + r * BK * 2, &tmA64, ka, c.m0 + r, fb);
+                        r += 64;
+                    }
+                    if (n16 - r >= 32) {
+                        tma_load_2d(sa + r * BK * 2, &tmA32, ka, c.m0 + r, fb);
+                        r += 32;
+                    }
+                    if (n16 - r >= 16) tma_load_2d(sa + r * BK * 2, &tmA16, ka, c.m0 + r, fb);
+                } else {
+                    tma_load_2d(sa, &tmA, ka, c.m0, fb);
+                }
                 tma_load_2d(sb, &tmB0, kb * BK, b0, fb);
                 if (!G::SWAP || MODE == GEMM_UP_SWIGLU)
                     tma_load_2d(sb + G::BOX * BK * 2, &tmB1, kb * BK, b1, fb);
@@ -316,17 +354,21 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = G::SWAP ? idesc_bf16(WROWS, NT) : idesc_bf16(BM, BN);
+        constexpr uint32_t idesc_fixed = G::SWAP ? idesc_bf16(WROWS, NT) : idesc_bf16(BM, BN);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
-            // Only the K range is needed here; it depends on the split alone,
-            // so the issuing thread never waits on the tile table.
+            // The K range depends on the split alone; only the per-tile
+            // width (NT = 256) needs the tile table here.
             const int kb0 = (L / tiles) * g.kb_per_split;
             const int kb1 = min(nk, kb0 + g.kb_per_split);
+            uint32_t idesc = idesc_fixed;
+            if (G::VARN)
+                idesc = idesc_bf16(
+                    WROWS, tile_n16<G::ROWS>(decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk)));
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
@@ -377,10 +419,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int f = c.n0 + quarter * 32 + lane;
                 const bool vf = f < g.N;
                 const bool raw = MODE == GEMM_DOWN || g.k_splits > 1;
+                const int ncols = G::VARN ? tile_n16<G::ROWS>(c) : NT;
                 float *P = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
                 __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
 #pragma unroll 1
-                for (int j0 = 0; j0 < NT; j0 += 16) {
+                for (int j0 = 0; j0 < ncols; j0 += 16) {
                     float a[16], b[16];
                     tmem_ld16(tbase + j0, a);
                     if (MODE == GEMM_UP_SWIGLU) tmem_ld16(tbase + NT + j0, b);
@@ -389,9 +432,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int i = 0; i < 16; ++i) {
                         const int row = c.m0 + j0 + i;
                         if (!vf || row >= c.mend) continue;
-                        if (raw) {
+                        if (MODE == GEMM_DOWN && g.out_mode == kOutBF16) {
+                            H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(a[i]);
+                        } else if (raw) {
                             float *dst = P + (size_t)row * g.ldc + f;
-                            dst[0] = a[i];
+                            dst[0] = MODE == GEMM_DOWN && g.out_mode == kOutF32Rounded
+                                         ? __bfloat162float(__float2bfloat16_rn(a[i]))
+                                         : a[i];
                             if (MODE == GEMM_UP_SWIGLU) dst[g.N] = b[i];
                         } else if (MODE == GEMM_UP_SWIGLU) {
                             H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(silu(a[i]) * b[i]);
@@ -439,6 +486,21 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                 *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
                         }
                     }
+                } else if (g.out_mode == kOutBF16) {
+                    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(g.C);
+#pragma unroll 1
+                    for (int cc = 0; cc < BN; cc += 16) {
+                        float v[16];
+                        tmem_ld16(tbase + cc, v);
+                        tmem_ld_wait();
+                        const int col = c.n0 + cc;
+                        if (vrow) {
+                            __nv_bfloat16 *dst = O + (size_t)row * g.ldc + col;
+                            if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
+                            if (col + 8 < g.N)
+                                *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
+                        }
+                    }
                 } else {
                     float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
 #pragma unroll 1
@@ -446,6 +508,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         float v[16];
                         tmem_ld16(tbase + cc, v);
                         tmem_ld_wait();
+                        if (g.out_mode == kOutF32Rounded)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
                         const int col = c.n0 + cc;
                         if (vrow) {
                             float *dst = O + (size_t)row * g.ldc + col;
@@ -518,30 +584,36 @@ static int num_sms() {
     return n;
 }
 
+struct Maps {
+    CUtensorMap a, a64, a32, a16, b0, b1;
+};
+
 template <int MODE, int NT, int BN>
-static cudaError_t launch_geo(const CUtensorMap &mA, const CUtensorMap &mB0,
-                              const CUtensorMap &mB1, const Args &g, cudaStream_t st) {
+static cudaError_t launch_geo(const Maps &m, const Args &g, cudaStream_t st) {
     using G = Geo<MODE, NT, BN>;
     static_assert(G::SMEM <= (size_t)kSmemLimit, "shared memory");
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, NT, BN>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)G::SMEM);
     if (err != cudaSuccess) return err;
-    grouped_gemm_tc_kernel<MODE, NT, BN><<<num_sms(), 256, G::SMEM, st>>>(mA, mB0, mB1, g);
+    grouped_gemm_tc_kernel<MODE, NT, BN><<<num_sms(), 256, G::SMEM, st>>>(m.a, m.a64, m.a32,
+                                                                          m.a16, m.b0, m.b1, g);
     note_launch();
     return cudaGetLastError();
 }
 
 template <int MODE>
-static cudaError_t launch_mode(int nt, int bn, const CUtensorMap &mA, const CUtensorMap &mB0,
-                               const CUtensorMap &mB1, const Args &g, cudaStream_t st) {
+static cudaError_t launch_mode(int nt, int bn, const Maps &m, const Args &g, cudaStream_t st) {
     switch (nt) {
         case 0:
-            return bn == BNM ? launch_geo<MODE, 0, BNM>(mA, mB0, mB1, g, st)
-                             : launch_geo<MODE, 0, BNM / 2>(mA, mB0, mB1, g, st);
-        case 16: return launch_geo<MODE, 16, BNM>(mA, mB0, mB1, g, st);
-        case 32: return launch_geo<MODE, 32, BNM>(mA, mB0, mB1, g, st);
-        case 64: return launch_geo<MODE, 64, BNM>(mA, mB0, mB1, g, st);
+            return bn == BNM ? launch_geo<MODE, 0, BNM>(m, g, st)
+                             : launch_geo<MODE, 0, BNM / 2>(m, g, st);
+        case 16: return launch_geo<MODE, 16, BNM>(m, g, st);
+        case 32: return launch_geo<MODE, 32, BNM>(m, g, st);
+        case 64: return launch_geo<MODE, 64, BNM>(m, g, st);
+        case kVarRows:
+            if constexpr (MODE == GEMM_DOWN) return launch_geo<MODE, kVarRows, BNM>(m, g, st);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -550,35 +622,48 @@ static cudaError_t launch_mode(int nt, int bn, const CUtensorMap &mA, const CUte
 
 // A [a_rows, a_cols], weights B0/B1 [E*b_rows, K]; tile table from
 // launch_build_tiles with row tiles of 128 (nt = 0) or nt rows (nt = 16, 32,
-// 64: weights on the MMA's M side).  bn (nt = 0 only): MMA N of 256 or 128;
-// 128 doubles the output tiles when there are too few to fill the SMs.  A's column for reduction index k is
-// k mod a_k_period (a_k_period = K: no wrap).  With k_splits > 1 split s of
+// 64, 256: weights on the MMA's M side; 256, down projection only, sets the
+// MMA N per tile).  bn (nt = 0 only): MMA N of 256 or 128; 128 doubles the
+// output tiles when there are too few to fill the SMs.  A's column for
+// reduction index k is k mod a_k_period (a_k_period = K: no wrap).  With k_splits > 1 split s of
 // every tile writes fp32 partial sums to C + s * split_stride: GEMM_DOWN
 // always (row-major [rows, ldc]); the up modes only with nt > 0, writing the
 // pre-activation sums (SwiGLU: W1 part at column f, W3 part at N + f).
-// k_splits = 1 up modes write the activation in bf16.
+// k_splits = 1 up modes write the activation in bf16.  out_mode (GEMM_DOWN
+// with k_splits = 1 only): kOutF32, kOutBF16 (bf16 output), kOutF32Rounded
+// (fp32 output holding the nearest bf16 of each value).
 cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_rows, int a_cols,
                            const void *B0, const void *B1, int E, int b_rows, int N, int K,
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,
                            const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           cudaStream_t st) {
+                           int out_mode, cudaStream_t st) {
     using namespace tc;
     if (a_rows == 0) return cudaSuccess;
     const int nk = (K + BK - 1) / BK;
-    if (nt != 0 && nt != 16 && nt != 32 && nt != 64) return cudaErrorInvalidValue;
+    if (nt != 0 && nt != 16 && nt != 32 && nt != 64 && nt != kVarRows) return cudaErrorInvalidValue;
     if (bn != BNM && bn != BNM / 2) return cudaErrorInvalidValue;
+    if (out_mode != kOutF32 && (mode != GEMM_DOWN || k_splits != 1 || N % 8 != 0 ||
+                                (out_mode != kOutBF16 && out_mode != kOutF32Rounded)))
+        return cudaErrorInvalidValue;
     if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN && nt == 0) ||
         (a_k_period % BK != 0 && a_k_period != K))
         return cudaErrorInvalidValue;
     const int kbps = (nk + k_splits - 1) / k_splits;
     k_splits = (nk + kbps - 1) / kbps;          // every split gets at least one K block
-    const int rows = nt ? nt : BM;
-    CUtensorMap mA, mB0, mB1;
-    if (!make_map(&mA, A, a_rows, a_cols, rows)) return cudaErrorInvalidValue;
+    const bool var = nt == kVarRows;
+    if (var && mode != GEMM_DOWN) return cudaErrorInvalidValue;
+    const int rows = var ? 128 : nt ? nt : BM;
+    Maps m;
+    if (!make_map(&m.a, A, a_rows, a_cols, rows)) return cudaErrorInvalidValue;
+    m.a64 = m.a32 = m.a16 = m.a;
+    if (var && (!make_map(&m.a64, A, a_rows, a_cols, 64) ||
+                !make_map(&m.a32, A, a_rows, a_cols, 32) ||
+                !make_map(&m.a16, A, a_rows, a_cols, 16)))
+        return cudaErrorInvalidValue;
     const int box = nt ? WROWS : bn / 2;
-    if (!make_map(&mB0, B0, (long long)E * b_rows, K, box)) return cudaErrorInvalidValue;
-    if (!make_map(&mB1, B1 ? B1 : B0, (long long)E * b_rows, K, box))
+    if (!make_map(&m.b0, B0, (long long)E * b_rows, K, box)) return cudaErrorInvalidValue;
+    if (!make_map(&m.b1, B1 ? B1 : B0, (long long)E * b_rows, K, box))
         return cudaErrorInvalidValue;
     const int outc = nt ? WROWS : (mode == GEMM_UP_SWIGLU ? bn / 2 : bn);
     Args g;
@@ -597,9 +682,10 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_
     g.offsets = offsets;
     g.C = C;
     g.ldc = ldc;
-    if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, mA, mB0, mB1, g, st);
-    if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, mA, mB0, mB1, g, st);
-    return launch_mode<GEMM_DOWN>(nt, bn, mA, mB0, mB1, g, st);
+    g.out_mode = out_mode;
+    if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, m, g, st);
+    if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, m, g, st);
+    return launch_mode<GEMM_DOWN>(nt, bn, m, g, st);
 }
 
 }  // namespace moe

@@ -83,27 +83,40 @@ cudaError_t launch_stats_finalize(const int32_t *counts, const float *p, int T, 
                                   cudaStream_t st, const ObsArgs &o = ObsArgs{});
 cudaError_t launch_entropy_partials(const float *probs, int T, int E, float *ent_partial,
                                     cudaStream_t st);
-// Expert output scale over the dispatched rows of `planes` fp32 planes:
-// row statistics into rs [max_rows][3] (fp64), then per expert mean, std and
-// max |o| (each output pointer may be NULL).
-cudaError_t launch_expert_scale(const float *P, int planes, long long plane, int d,
-                                const int32_t *offsets, int E, long long max_rows, double *rs,
-                                float *mean, float *std_, float *maxabs, cudaStream_t st);
+// Expert outputs o in row order: one bf16 plane (bf16 = 1), or `planes`
+// fp32 planes `plane` elements apart (partial sums of a split reduction,
+// added in plane order), their sum rounded to the nearest bf16 when round_bf16
+// is set (a bf16 layer's expert output is a bf16 tensor).
+struct ExpertOut {
+    const void *p;
+    int bf16;
+    int planes;
+    long long plane;
+    int round_bf16;
+};
+inline ExpertOut expert_out_f32(const float *p, int planes = 1, long long plane = 0,
+                                bool round_bf16 = false) {
+    return ExpertOut{p, 0, planes, plane, round_bf16 ? 1 : 0};
+}
+// Output modes of the down projection (launch_tc_gemm).
+enum { kOutF32 = 0, kOutBF16 = 1, kOutF32Rounded = 2 };
+// Expert output scale over the dispatched rows: row statistics into
+// rs [max_rows][3] (fp64), then per expert mean, std and max |o| (each
+// output pointer may be NULL).
+cudaError_t launch_expert_scale(const ExpertOut &o, int d, const int32_t *offsets, int E,
+                                long long max_rows, double *rs, float *mean, float *std_,
+                                float *maxabs, cudaStream_t st);
 cudaError_t launch_gather_rows(const void *x, int elem_bytes, int d, const int32_t *perm,
                                const int32_t *offsets_end, int k, long long max_rows, void *xs,
                                cudaStream_t st);
-// out_sorted and shared_out may hold several fp32 planes (partial sums of a
-// split reduction), `planes` / `sh_planes` of them `plane` / `sh_plane`
-// elements apart; they are added in plane order.
-cudaError_t launch_combine(const float *out_sorted, int planes, long long plane,
-                           const int32_t *inv, const float *w, const float *shared_out,
-                           int sh_planes, long long sh_plane, int T, int k, int d,
-                           int out_dtype, void *y, cudaStream_t st);
-cudaError_t launch_combine_rows(const float *out_sorted, int planes, long long plane,
-                                const int32_t *tok_start, const int32_t *tok_rows,
-                                const float *row_w, const float *shared_out, int sh_planes,
-                                long long sh_plane, int T, int d, int out_dtype, void *y,
-                                cudaStream_t st);
+// y[t] = sum_j w o[row] + s[t]; `sh` (the shared expert's output, p NULL
+// when there is none) is read like `o`.
+cudaError_t launch_combine(const ExpertOut &o, const int32_t *inv, const float *w,
+                           const ExpertOut &sh, int T, int k, int d, int out_dtype, void *y,
+                           cudaStream_t st);
+cudaError_t launch_combine_rows(const ExpertOut &o, const int32_t *tok_start,
+                                const int32_t *tok_rows, const float *row_w, const ExpertOut &sh,
+                                int T, int d, int out_dtype, void *y, cudaStream_t st);
 // expert_choice.cu: each expert takes its top-Cn tokens by probability from
 // probsT [E, T]; rows of expert e are [e*Cn, (e+1)*Cn) in token order.
 // rowidx [E][T] (row or -1), per-token row lists tok_start [T+1], tok_rows.
@@ -119,10 +132,11 @@ cudaError_t launch_slot_outputs(const int32_t *idx, const float *w, const int32_
 cudaError_t launch_split_activation(const float *P, int splits, long long plane, int N,
                                     int swiglu, const int32_t *rows_end, long long max_rows,
                                     __nv_bfloat16 *h, cudaStream_t st);
-// out[r] = sum_s P_s[r] (fp32) for rows r < *rows_end.
+// out[r] = sum_s P_s[r] (fp32) for rows r < *rows_end; round_bf16: each sum
+// replaced by its nearest bf16.
 cudaError_t launch_sum_planes(const float *P, int splits, long long plane, int d,
                               const int32_t *rows_end, long long max_rows, float *out,
-                              cudaStream_t st);
+                              cudaStream_t st, bool round_bf16 = false);
 cudaError_t launch_build_tiles(const int32_t *offsets, int E, int BM, int32_t *tile_e,
                                int32_t *tile_m0, int32_t *tile_start, int32_t *n_tiles,
                                cudaStream_t st);
@@ -152,6 +166,6 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,
                            const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           cudaStream_t st);
+                           int out_mode, cudaStream_t st);
 
 }  // namespace moe

@@ -161,11 +161,40 @@ cudaError_t launch_entropy_partials(const float *probs, int T, int E, float *ent
     return cudaGetLastError();
 }
 
-// Per sorted row r < *rows_end of the expert outputs (the sum of `planes`
-// fp32 planes, in plane order): sum, sum of squares (fp64) and max |o|.
-// One warp per row; lane-strided partial sums, fixed butterfly.
-__global__ void __launch_bounds__(256) row_stats_kernel(const float *P, int planes,
-                                                        long long plane, int d,
+__device__ __forceinline__ float round_bf16(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ float4 round4_bf16(float4 v) {
+    return make_float4(round_bf16(v.x), round_bf16(v.y), round_bf16(v.z), round_bf16(v.w));
+}
+// Element i of the expert outputs (planes added in plane order).
+__device__ __forceinline__ float expert_out_at(const ExpertOut &o, long long i) {
+    if (o.bf16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(o.p)[i]);
+    const float *P = static_cast<const float *>(o.p);
+    float v = P[i];
+    for (int sp = 1; sp < o.planes; ++sp) v += P[sp * o.plane + i];
+    return o.round_bf16 ? round_bf16(v) : v;
+}
+// Elements 4i .. 4i+3 of the expert outputs.
+__device__ __forceinline__ float4 expert_out4(const ExpertOut &o, long long i) {
+    if (o.bf16) {
+        const uint2 u = static_cast<const uint2 *>(o.p)[i];
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+    const float4 *P = static_cast<const float4 *>(o.p);
+    float4 v = P[i];
+    for (int sp = 1; sp < o.planes; ++sp) {
+        const float4 q = P[sp * (o.plane / 4) + i];
+        v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+    }
+    return o.round_bf16 ? round4_bf16(v) : v;
+}
+
+// Per sorted row r < *rows_end of the expert outputs: sum, sum of squares
+// (fp64) and max |o|.  One warp per row; lane-strided partial sums, fixed
+// butterfly.
+__global__ void __launch_bounds__(256) row_stats_kernel(ExpertOut o, int d,
                                                         const int32_t *rows_end,
                                                         long long max_rows, double *rs) {
     const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -173,10 +202,8 @@ __global__ void __launch_bounds__(256) row_stats_kernel(const float *P, int plan
     if (r >= max_rows || r >= *rows_end) return;
     double s1 = 0.0, s2 = 0.0;
     float mx = 0.f;
-    const float *row = P + r * d;
     for (int c = lane; c < d; c += 32) {
-        float v = row[c];
-        for (int sp = 1; sp < planes; ++sp) v += row[sp * plane + c];
+        const float v = expert_out_at(o, r * d + c);
         s1 += v;
         s2 += (double)v * v;
         mx = fmaxf(mx, fabsf(v));
@@ -230,13 +257,12 @@ __global__ void __launch_bounds__(256) expert_scale_kernel(const double *rs,
     }
 }
 
-cudaError_t launch_expert_scale(const float *P, int planes, long long plane, int d,
-                                const int32_t *offsets, int E, long long max_rows, double *rs,
-                                float *mean, float *std_, float *maxabs, cudaStream_t st) {
+cudaError_t launch_expert_scale(const ExpertOut &o, int d, const int32_t *offsets, int E,
+                                long long max_rows, double *rs, float *mean, float *std_,
+                                float *maxabs, cudaStream_t st) {
     if (max_rows > 0) {
-        row_stats_kernel<<<(unsigned)((max_rows + 7) / 8), 256, 0, st>>>(P, planes, plane, d,
-                                                                         offsets + E, max_rows,
-                                                                         rs);
+        row_stats_kernel<<<(unsigned)((max_rows + 7) / 8), 256, 0, st>>>(o, d, offsets + E,
+                                                                         max_rows, rs);
         note_launch();
     }
     expert_scale_kernel<<<E, 256, 0, st>>>(rs, offsets, d, mean, std_, maxabs);
@@ -293,9 +319,8 @@ __device__ __forceinline__ float4 sum_planes4(const float4 *p, int planes, long 
 }
 
 template <typename TO>
-__global__ void combine_kernel(const float4 *out_sorted, int planes, long long plane4,
-                               const int32_t *inv, const float *w, const float4 *shared_out,
-                               int sh_planes, long long sh_plane4, int k, int d4, TO *y) {
+__global__ void combine_kernel(ExpertOut out_sorted, const int32_t *inv, const float *w,
+                               ExpertOut sh, int k, int d4, TO *y) {
     const long long t = blockIdx.x;
     for (int c = threadIdx.x; c < d4; c += blockDim.x) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -303,12 +328,12 @@ __global__ void combine_kernel(const float4 *out_sorted, int planes, long long p
             const int s = inv[t * k + j];
             if (s < 0) continue;
             const float wj = w[t * k + j];
-            const float4 o = sum_planes4(out_sorted, planes, plane4, (long long)s * d4 + c);
+            const float4 o = expert_out4(out_sorted, (long long)s * d4 + c);
             acc.x = fmaf(wj, o.x, acc.x); acc.y = fmaf(wj, o.y, acc.y);
             acc.z = fmaf(wj, o.z, acc.z); acc.w = fmaf(wj, o.w, acc.w);
         }
-        if (shared_out) {
-            const float4 sv = sum_planes4(shared_out, sh_planes, sh_plane4, t * d4 + c);
+        if (sh.p) {
+            const float4 sv = expert_out4(sh, t * d4 + c);
             acc.x += sv.x; acc.y += sv.y; acc.z += sv.z; acc.w += sv.w;
         }
         if constexpr (sizeof(TO) == 4) {
@@ -324,23 +349,18 @@ __global__ void combine_kernel(const float4 *out_sorted, int planes, long long p
     }
 }
 
-cudaError_t launch_combine(const float *out_sorted, int planes, long long plane,
-                           const int32_t *inv, const float *w, const float *shared_out,
-                           int sh_planes, long long sh_plane, int T, int k, int d,
-                           int out_dtype, void *y, cudaStream_t st) {
+cudaError_t launch_combine(const ExpertOut &o, const int32_t *inv, const float *w,
+                           const ExpertOut &sh, int T, int k, int d, int out_dtype, void *y,
+                           cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int d4 = d / 4;
     const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
-    const float4 *o4 = reinterpret_cast<const float4 *>(out_sorted);
-    const float4 *s4 = reinterpret_cast<const float4 *>(shared_out);
     if (out_dtype == MOE_DTYPE_FP32)
-        combine_kernel<float><<<T, threads, 0, st>>>(o4, planes, plane / 4, inv, w, s4,
-                                                     sh_planes, sh_plane / 4, k, d4,
+        combine_kernel<float><<<T, threads, 0, st>>>(o, inv, w, sh, k, d4,
                                                      static_cast<float *>(y));
     else
-        combine_kernel<__nv_bfloat16><<<T, threads, 0, st>>>(
-            o4, planes, plane / 4, inv, w, s4, sh_planes, sh_plane / 4, k, d4,
-            static_cast<__nv_bfloat16 *>(y));
+        combine_kernel<__nv_bfloat16><<<T, threads, 0, st>>>(o, inv, w, sh, k, d4,
+                                                             static_cast<__nv_bfloat16 *>(y));
     note_launch();
     return cudaGetLastError();
 }
@@ -349,10 +369,9 @@ cudaError_t launch_combine(const float *out_sorted, int planes, long long plane,
 // i in [tok_start[t], tok_start[t+1]) of row_w[r_i] o[r_i] (list order) +
 // s[t], o and s summed over their planes in plane order.
 template <typename TO>
-__global__ void combine_rows_kernel(const float4 *out_sorted, int planes, long long plane4,
-                                    const int32_t *tok_start, const int32_t *tok_rows,
-                                    const float *row_w, const float4 *shared_out, int sh_planes,
-                                    long long sh_plane4, int d4, TO *y) {
+__global__ void combine_rows_kernel(ExpertOut out_sorted, const int32_t *tok_start,
+                                    const int32_t *tok_rows, const float *row_w, ExpertOut sh,
+                                    int d4, TO *y) {
     const long long t = blockIdx.x;
     const int a = tok_start[t], b = tok_start[t + 1];
     for (int c = threadIdx.x; c < d4; c += blockDim.x) {
@@ -360,12 +379,12 @@ __global__ void combine_rows_kernel(const float4 *out_sorted, int planes, long l
         for (int i = a; i < b; ++i) {
             const int r = tok_rows[i];
             const float wr = row_w[r];
-            const float4 o = sum_planes4(out_sorted, planes, plane4, (long long)r * d4 + c);
+            const float4 o = expert_out4(out_sorted, (long long)r * d4 + c);
             acc.x = fmaf(wr, o.x, acc.x); acc.y = fmaf(wr, o.y, acc.y);
             acc.z = fmaf(wr, o.z, acc.z); acc.w = fmaf(wr, o.w, acc.w);
         }
-        if (shared_out) {
-            const float4 sv = sum_planes4(shared_out, sh_planes, sh_plane4, t * d4 + c);
+        if (sh.p) {
+            const float4 sv = expert_out4(sh, t * d4 + c);
             acc.x += sv.x; acc.y += sv.y; acc.z += sv.z; acc.w += sv.w;
         }
         if constexpr (sizeof(TO) == 4) {
@@ -381,25 +400,18 @@ __global__ void combine_rows_kernel(const float4 *out_sorted, int planes, long l
     }
 }
 
-cudaError_t launch_combine_rows(const float *out_sorted, int planes, long long plane,
-                                const int32_t *tok_start, const int32_t *tok_rows,
-                                const float *row_w, const float *shared_out, int sh_planes,
-                                long long sh_plane, int T, int d, int out_dtype, void *y,
-                                cudaStream_t st) {
+cudaError_t launch_combine_rows(const ExpertOut &o, const int32_t *tok_start,
+                                const int32_t *tok_rows, const float *row_w, const ExpertOut &sh,
+                                int T, int d, int out_dtype, void *y, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int d4 = d / 4;
     const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
-    const float4 *o4 = reinterpret_cast<const float4 *>(out_sorted);
-    const float4 *s4 = reinterpret_cast<const float4 *>(shared_out);
     if (out_dtype == MOE_DTYPE_FP32)
-        combine_rows_kernel<float><<<T, threads, 0, st>>>(o4, planes, plane / 4, tok_start,
-                                                          tok_rows, row_w, s4, sh_planes,
-                                                          sh_plane / 4, d4,
+        combine_rows_kernel<float><<<T, threads, 0, st>>>(o, tok_start, tok_rows, row_w, sh, d4,
                                                           static_cast<float *>(y));
     else
         combine_rows_kernel<__nv_bfloat16><<<T, threads, 0, st>>>(
-            o4, planes, plane / 4, tok_start, tok_rows, row_w, s4, sh_planes, sh_plane / 4, d4,
-            static_cast<__nv_bfloat16 *>(y));
+            o, tok_start, tok_rows, row_w, sh, d4, static_cast<__nv_bfloat16 *>(y));
     note_launch();
     return cudaGetLastError();
 }
@@ -481,24 +493,29 @@ cudaError_t launch_split_activation(const float *P, int splits, long long plane,
     return cudaGetLastError();
 }
 
-// out[r] = sum_s P_s[r] for rows r < *rows_end (fp32, split order).
+// out[r] = sum_s P_s[r] for rows r < *rows_end (fp32, split order), rounded
+// to the nearest bf16 when round_bf16 is set.
 __global__ void sum_planes_kernel(const float4 *P, int splits, long long plane4, int d4,
-                                  const int32_t *rows_end, long long max_rows, float4 *out) {
+                                  const int32_t *rows_end, long long max_rows, float4 *out,
+                                  int round_bf16) {
     const long long rows = min((long long)*rows_end, max_rows);
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < rows * d4;
-         i += (long long)gridDim.x * blockDim.x)
-        out[i] = sum_planes4(P, splits, plane4, i);
+         i += (long long)gridDim.x * blockDim.x) {
+        float4 v = sum_planes4(P, splits, plane4, i);
+        if (round_bf16) v = round4_bf16(v);
+        out[i] = v;
+    }
 }
 
 cudaError_t launch_sum_planes(const float *P, int splits, long long plane, int d,
                               const int32_t *rows_end, long long max_rows, float *out,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool round_bf16) {
     if (max_rows == 0) return cudaSuccess;
     const long long work = max_rows * (d / 4);
     const int grid = (int)std::min<long long>((work + 255) / 256, 148 * 8);
     sum_planes_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4 *>(P), splits,
                                             plane / 4, d / 4, rows_end, max_rows,
-                                            reinterpret_cast<float4 *>(out));
+                                            reinterpret_cast<float4 *>(out), round_bf16 ? 1 : 0);
     note_launch();
     return cudaGetLastError();
 }

@@ -101,11 +101,21 @@ int router_splits(const moe_config *c) {
 // weights from HBM and a 128-row token tile would be mostly padding.  With
 // few tiles the reduction is split (s_up, s_down) so that every SM streams
 // weights; the splits' fp32 partial sums are added in split order later.
+// nt_down = 256 (with nt = 0): the down projection runs on tiles of up to 256
+// rows whose MMA N is each tile's row count rounded to 16.
 struct FfnPlan {
     int nt, s_up, s_down;
     int bn_up, bn_down;     // nt = 0: MMA N (256, or 128 when tiles are few)
+    int nt_down;            // geometry of the down projection
 };
 constexpr int kPlanSMs = 148;   // SM count the split choice assumes (B300)
+constexpr int kVarTileRows = 256;
+// Measured on B300: with the same work per tile, the per-tile-width geometry
+// runs the down projection 1.26x slower than 128-row tiles (DeepSeek shape,
+// at most 256 rows per expert), and 1.49x faster where the last 128-row tile
+// of every expert is mostly padding (896 experts of about 146 rows).  It is
+// chosen when the padding of 128-row tiles exceeds its own by more than this.
+constexpr double kVarPadGain = 1.3;
 
 // Split the reduction only when the tiles do not fill the SMs once, and then
 // only up to one round of work items: measured at the Mixtral shape, a split
@@ -124,7 +134,7 @@ int split_count(long long tiles, long long nk) {
 // rows: dispatched rows (T*k routed, T shared); groups: experts; K = d.
 FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long long F,
                  bool swiglu) {
-    FfnPlan p{0, 1, 1, 256, 256};
+    FfnPlan p{0, 1, 1, 256, 256, 0};
     if (c->dtype != MOE_DTYPE_BF16 || rows <= 0 || F <= 0) return p;
     const long long d = c->d_model;
     const long long active = std::min(groups, rows);
@@ -139,8 +149,17 @@ FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long lon
         const long long mt = (rows + 127) / 128 + active;
         if (mt * ((F + up_cols - 1) / up_cols) < 2 * kPlanSMs) p.bn_up = 128;
         if (mt * ((d + 255) / 256) < 2 * kPlanSMs) p.bn_down = 128;
+        const double pad128 = (double)((per + 127) / 128 * 128) / per;
+        const double pad16 = (double)((per + 15) / 16 * 16) / per;
+        if (pad128 > kVarPadGain * pad16) {
+            p.nt_down = kVarTileRows;
+            p.s_down = split_count(active * ((per + kVarTileRows - 1) / kVarTileRows) *
+                                       ((d + 127) / 128),
+                                   (F + 63) / 64);
+        }
         return p;
     }
+    p.nt_down = p.nt;
     const long long ttiles = active * ((per + p.nt - 1) / p.nt);
     p.s_up = split_count(ttiles * ((F + 127) / 128), (d + 63) / 64);
     p.s_down = split_count(ttiles * ((d + 127) / 128), (F + 63) / 64);
@@ -359,7 +378,7 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
         MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E,
                                 kRouterParts * dp,
-                                dp, S, s.T * s.E, te, ts, nt, off, part, a.E, st));
+                                dp, S, s.T * s.E, te, ts, nt, off, part, a.E, 0, st));
         int planes = S;
         if (S > 1) {       // a wide kernel adds the planes (same order), streaming
             MOE_CUDA(launch_sum_planes(part, S, s.T * s.E, a.E, off + 1, s.T, part, st));
@@ -393,10 +412,11 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
 // Up and down projections of one grouped FFN on the tensor cores: rows of A
 // (x_sorted, or x itself for the shared expert) grouped by `offsets` into
 // `groups` experts; h gets the activation in bf16; the down projection's
-// fp32 output goes to `out` (plan.s_down planes of rows*d elements).
+// output goes to `out`: plan.s_down fp32 planes of rows*d elements, or with
+// one split the format out_mode names (kOutF32, kOutBF16, kOutF32Rounded).
 int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void *A,
                long long rows, int groups, int F, const int32_t *offsets, const void *w1,
-               const void *w3, const void *w2, void *h, float *up_part, float *out,
+               const void *w3, const void *w2, void *h, float *up_part, void *out, int out_mode,
                int32_t *tile_e, int32_t *tile_start, int32_t *ntiles, int up_stage,
                int down_stage, cudaStream_t st) {
     const int d = c->d_model;
@@ -409,35 +429,39 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
         MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, A, rows, d, w1, w3, groups, F, F, d, d,
                                 plan.s_up,
                                 rows * upw * F, tile_e, tile_start, ntiles, offsets, up_part,
-                                upw * F, st));
+                                upw * F, 0, st));
         MOE_CUDA(launch_split_activation(up_part, plan.s_up, rows * upw * F, F,
                                          up_mode == GEMM_UP_SWIGLU, offsets + groups, rows,
                                          static_cast<__nv_bfloat16 *>(h), st));
     } else {
         MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, A, rows, d, w1, w3, groups, F, F, d, d,
-                                1, 0, tile_e, tile_start, ntiles, offsets, h, F, st));
+                                1, 0, tile_e, tile_start, ntiles, offsets, h, F, 0, st));
     }
     if (up_stage >= 0) {
         stage_end(up_stage, ev, st);
         ev = stage_begin(st);
     }
-    MOE_CUDA(launch_tc_gemm(GEMM_DOWN, nt, plan.bn_down, h, rows, F, w2, nullptr, groups, d, d,
-                            F, F,
-                            plan.s_down, rows * d, tile_e, tile_start, ntiles, offsets, out, d,
-                            st));
+    if (plan.nt_down != nt)
+        MOE_CUDA(launch_build_tiles(offsets, groups, plan.nt_down ? plan.nt_down : kTcBM, tile_e,
+                                    nullptr, tile_start, ntiles, st));
+    MOE_CUDA(launch_tc_gemm(GEMM_DOWN, plan.nt_down, plan.bn_down, h, rows, F, w2, nullptr,
+                            groups, d, d, F, F, plan.s_down, rows * d, tile_e, tile_start, ntiles,
+                            offsets, out, d, plan.s_down == 1 ? out_mode : kOutF32, st));
     if (down_stage >= 0) stage_end(down_stage, ev, st);
     return MOE_OK;
 }
 
 // Grouped expert FFN over the dispatched rows; out_sorted fp32 (plan.s_down
-// planes of T*k*d elements).  bf16: gather the rows into x_sorted, tcgen05
+// planes of R*d elements), or with one split the format out_mode names
+// (bf16 layers only for kOutBF16 and kOutF32Rounded).  bf16: gather the rows into x_sorted, tcgen05
 // up (+activation) into h, tcgen05 down into out_sorted.  fp32: SIMT GEMMs
 // reading x through perm directly.
 int run_experts(const moe_config *c, const void *x, const int32_t *perm, const int32_t *offsets,
-                const void *w1, const void *w3, const void *w2, float *out_sorted, void *ws,
-                const Layout &L, cudaStream_t st) {
+                const void *w1, const void *w3, const void *w2, void *out_sorted,
+                int out_mode, void *ws, const Layout &L, cudaStream_t st) {
     const Sizes s = sizes(c);
     if (s.R == 0) return MOE_OK;
+    if (out_mode != kOutF32 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
     const int gk = expert_choice(c) ? 1 : (int)s.k;   // perm holds t*k+j, or t itself
     int32_t *tile_e = at<int32_t>(ws, L.tile_e), *tile_m0 = at<int32_t>(ws, L.tile_m0);
     int32_t *tile_start = at<int32_t>(ws, L.tile_start), *ntiles = at<int32_t>(ws, L.ntiles);
@@ -448,8 +472,8 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
         MOE_CUDA(launch_gather_rows(x, 2, (int)s.d, perm, offsets + s.E, gk, s.R, xs, st));
         stage_end(MOE_STAGE_GATHER, ev, st);
         return run_tc_ffn(c, routed_plan(c), up_mode, xs, s.R, (int)s.E, (int)s.F, offsets, w1,
-                          w3, w2, h, at<float>(ws, L.up_part), out_sorted, tile_e, tile_start,
-                          ntiles, MOE_STAGE_UP, MOE_STAGE_DOWN, st);
+                          w3, w2, h, at<float>(ws, L.up_part), out_sorted, out_mode, tile_e,
+                          tile_start, ntiles, MOE_STAGE_UP, MOE_STAGE_DOWN, st);
     }
     cudaEvent_t ev = stage_begin(st);
     MOE_CUDA(launch_build_tiles(offsets, (int)s.E, kSimtBM, tile_e, tile_m0, nullptr, ntiles, st));
@@ -473,11 +497,11 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
     return MOE_OK;
 }
 
-// Shared expert (SwiGLU) on all T rows -> sh_out fp32 (shared_plan.s_down
-// planes of T*d elements): the same grouped kernels with one group {0, T}
-// and x read in place.
+// Shared expert (SwiGLU) on all T rows -> sh_out: shared_plan.s_down fp32
+// planes of T*d elements, or one bf16 plane (out_mode kOutBF16, one split):
+// the same grouped kernels with one group {0, T} and x read in place.
 int run_shared(const moe_config *c, const void *x, const void *ws1, const void *ws3,
-               const void *ws2, void *ws, const Layout &L, cudaStream_t st) {
+               const void *ws2, int out_mode, void *ws, const Layout &L, cudaStream_t st) {
     const Sizes s = sizes(c);
     if (s.T == 0) return MOE_OK;
     int32_t *off = at<int32_t>(ws, L.sh_offsets);
@@ -490,7 +514,8 @@ int run_shared(const moe_config *c, const void *x, const void *ws1, const void *
     float *o = at<float>(ws, L.sh_out);
     if (c->dtype == MOE_DTYPE_BF16)
         return run_tc_ffn(c, shared_plan(c), GEMM_UP_SWIGLU, x, s.T, 1, (int)s.Fs, off, ws1, ws3,
-                          ws2, h, at<float>(ws, L.sh_up_part), o, te, ts, nt, -1, -1, st);
+                          ws2, h, at<float>(ws, L.sh_up_part), o, out_mode, te, ts, nt, -1,
+                          -1, st);
     MOE_CUDA(launch_build_tiles(off, 1, kSimtBM, te, tm, nullptr, nt, st));
     GroupedGemmArgs up;
     up.A = x; up.a_gather = nullptr; up.gather_k = 1;
@@ -650,7 +675,9 @@ int moe_combine_rows(const moe_config *cfg, const float *out_sorted, const float
     if (cfg->T == 0) return MOE_OK;
     MOE_PTR(out_sorted); MOE_PTR(row_w); MOE_PTR(tok_start); MOE_PTR(tok_rows); MOE_PTR(y);
     MOE_OPT_PTR(shared_out);
-    MOE_CUDA(launch_combine_rows(out_sorted, 1, 0, tok_start, tok_rows, row_w, shared_out, 1, 0,
+    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
+    MOE_CUDA(launch_combine_rows(expert_out_f32(out_sorted, 1, 0, bf16), tok_start, tok_rows,
+                                 row_w, expert_out_f32(shared_out, 1, 0, bf16),
                                  cfg->T, cfg->d_model, cfg->out_dtype, y, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -687,16 +714,20 @@ int moe_expert_ffn(const moe_config *cfg, const void *x, const int32_t *perm,
     const Layout L = layout(cfg);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     const FfnPlan plan = routed_plan(cfg);
+    // a bf16 layer's expert outputs are bf16 values (held here in fp32)
+    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
     if (plan.s_down == 1)
-        return run_experts(cfg, x, perm, offsets, w1, w3, w2, out_sorted, ws, L,
-                           (cudaStream_t)stream);
+        return run_experts(cfg, x, perm, offsets, w1, w3, w2, out_sorted,
+                           bf16 ? kOutF32Rounded : kOutF32, ws, L, (cudaStream_t)stream);
     // split reduction: partial planes in the workspace, summed into out_sorted
     float *planes = at<float>(ws, L.out_sorted);
-    rc = run_experts(cfg, x, perm, offsets, w1, w3, w2, planes, ws, L, (cudaStream_t)stream);
+    rc = run_experts(cfg, x, perm, offsets, w1, w3, w2, planes, kOutF32, ws, L,
+                     (cudaStream_t)stream);
     if (rc != MOE_OK) return rc;
     const long long R = sizes(cfg).R;
     MOE_CUDA(launch_sum_planes(planes, plan.s_down, R * cfg->d_model, cfg->d_model,
-                               offsets + cfg->n_experts, R, out_sorted, (cudaStream_t)stream));
+                               offsets + cfg->n_experts, R, out_sorted, (cudaStream_t)stream,
+                               bf16));
     return MOE_OK;
 }
 
@@ -706,7 +737,9 @@ int moe_combine(const moe_config *cfg, const float *out_sorted, const int32_t *i
     if (rc != MOE_OK) return rc;
     if (cfg->T == 0) return MOE_OK;
     MOE_PTR(out_sorted); MOE_PTR(inv); MOE_PTR(topk_w); MOE_PTR(y); MOE_OPT_PTR(shared_out);
-    MOE_CUDA(launch_combine(out_sorted, 1, 0, inv, topk_w, shared_out, 1, 0, cfg->T, cfg->top_k,
+    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
+    MOE_CUDA(launch_combine(expert_out_f32(out_sorted, 1, 0, bf16), inv, topk_w,
+                            expert_out_f32(shared_out, 1, 0, bf16), cfg->T, cfg->top_k,
                             cfg->d_model, cfg->out_dtype, y, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -775,9 +808,9 @@ int moe_observe(const moe_config *cfg, const float *probs, const float *out_sort
         if (o && !out_sorted) MOE_CUDA(cudaMemsetAsync(o, 0, sizeof(float) * s.E, st));
     }
     if (out_sorted && (outs[0] || outs[1] || outs[2]))
-        MOE_CUDA(launch_expert_scale(out_sorted, 1, 0, (int)s.d, offsets, (int)s.E, s.Tk,
-                                     at<double>(ws, L.row_stats), outs[0], outs[1], outs[2],
-                                     st));
+        MOE_CUDA(launch_expert_scale(expert_out_f32(out_sorted), (int)s.d, offsets, (int)s.E,
+                                     s.Tk, at<double>(ws, L.row_stats), outs[0], outs[1],
+                                     outs[2], st));
     return MOE_OK;
 }
 
@@ -823,7 +856,19 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     float *sbias = out->select_bias_out ? out->select_bias_out : at<float>(ws, L.sbias);
     int32_t *offsets = at<int32_t>(ws, L.offsets);
     int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
-    float *out_sorted = at<float>(ws, L.out_sorted);
+    // Expert outputs: one bf16 plane for bf16 layers whose down projection is
+    // not split (half the bytes written by the down projection and read by
+    // the combine); fp32 planes otherwise.
+    // (a bf16 layer's expert outputs are bf16 tensors: split planes are
+    // rounded after their sum)
+    void *out_sorted = at<void>(ws, L.out_sorted);
+    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
+    const FfnPlan rplan = routed_plan(cfg), splan = shared_plan(cfg);
+    const bool o_bf16 = bf16 && rplan.s_down == 1;
+    const ExpertOut eo{out_sorted, o_bf16 ? 1 : 0, rplan.s_down, s.R * s.d,
+                       (bf16 && !o_bf16) ? 1 : 0};
+    const bool sh_bf16 = bf16 && splan.s_down == 1;
+    ExpertOut sh{nullptr, sh_bf16 ? 1 : 0, splan.s_down, s.T * s.d, (bf16 && !sh_bf16) ? 1 : 0};
 
     const bool biased = cfg->quantile_balance || wts->select_bias != nullptr;
     const bool want_unb = out->counts_unbiased != nullptr;
@@ -895,37 +940,35 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
         obs && (obs->expert_out_mean || obs->expert_out_std || obs->expert_out_max_abs);
     if (s.T == 0) {
         if (want_scale)
-            MOE_CUDA(launch_expert_scale(out_sorted, 1, 0, (int)s.d, offsets, (int)s.E, 0,
+            MOE_CUDA(launch_expert_scale(eo, (int)s.d, offsets, (int)s.E, 0,
                                          at<double>(ws, L.row_stats), obs->expert_out_mean,
                                          obs->expert_out_std, obs->expert_out_max_abs, st));
         return MOE_OK;
     }
-    rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted, ws, L, st);
+    rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted,
+                     o_bf16 ? kOutBF16 : kOutF32, ws, L, st);
     if (rc != MOE_OK) return rc;
     if (want_scale)
-        MOE_CUDA(launch_expert_scale(out_sorted, routed_plan(cfg).s_down, s.R * s.d, (int)s.d,
-                                     offsets, (int)s.E, s.R, at<double>(ws, L.row_stats),
+        MOE_CUDA(launch_expert_scale(eo, (int)s.d, offsets, (int)s.E, s.R,
+                                     at<double>(ws, L.row_stats),
                                      obs->expert_out_mean, obs->expert_out_std,
                                      obs->expert_out_max_abs, st));
-    const float *shared = nullptr;
     if (s.Fs > 0) {
         ev = stage_begin(st);
-        rc = run_shared(cfg, x, wts->ws1, wts->ws3, wts->ws2, ws, L, st);
+        rc = run_shared(cfg, x, wts->ws1, wts->ws3, wts->ws2, sh_bf16 ? kOutBF16 : kOutF32, ws,
+                        L, st);
         if (rc != MOE_OK) return rc;
         stage_end(MOE_STAGE_SHARED, ev, st);
-        shared = at<float>(ws, L.sh_out);
+        sh.p = at<void>(ws, L.sh_out);
     }
     ev = stage_begin(st);
     if (ec)
-        MOE_CUDA(launch_combine_rows(out_sorted, routed_plan(cfg).s_down, s.R * s.d,
-                                     at<int32_t>(ws, L.ec_tok_start),
+        MOE_CUDA(launch_combine_rows(eo, at<int32_t>(ws, L.ec_tok_start),
                                      at<int32_t>(ws, L.ec_tok_rows), at<float>(ws, L.ec_row_w),
-                                     shared, shared_plan(cfg).s_down, s.T * s.d, (int)s.T,
-                                     (int)s.d, cfg->out_dtype, out->y, st));
+                                     sh, (int)s.T, (int)s.d, cfg->out_dtype, out->y, st));
     else
-        MOE_CUDA(launch_combine(out_sorted, routed_plan(cfg).s_down, s.R * s.d, inv, comb_w,
-                                shared, shared_plan(cfg).s_down, s.T * s.d, (int)s.T, (int)s.k,
-                                (int)s.d, cfg->out_dtype, out->y, st));
+        MOE_CUDA(launch_combine(eo, inv, comb_w, sh, (int)s.T, (int)s.k, (int)s.d,
+                                cfg->out_dtype, out->y, st));
     stage_end(MOE_STAGE_COMBINE, ev, st);
     return MOE_OK;
 }

@@ -220,8 +220,13 @@ __global__ void __launch_bounds__(256) router_small_epilogue_kernel(RouterArgs a
 // --------------------------------------------------------------------------
 constexpr int kTB = 32, kEC = 128, kDK = 32;
 
+// Row stride (floats) of a logit tile in shared memory: E made odd, so that
+// reading one expert's column of the tile touches distinct banks.
+__host__ __device__ inline int router_lde(int E) { return E | 1; }
+
 __host__ __device__ inline size_t router_tiled_smem(int E) {
-    return sizeof(float) * ((size_t)kTB * E + kDK * kTB + kDK * (kEC + 4) + 3 * kTB);
+    return sizeof(float) *
+           ((size_t)kTB * router_lde(E) + kDK * kTB + kDK * (kEC + 4) + 3 * kTB);
 }
 
 __device__ __forceinline__ void load4_f32(const float *p, float *v) {
@@ -260,19 +265,21 @@ __device__ __forceinline__ int warp_take_max(float (&sc)[kTopkPerLane], int lane
 // Softmax, load-statistics partial sums, optional probs/probsT, optional
 // gate-entropy partial sum and top-k with renormalisation for a tile of TB
 // tokens whose logits (logit offset included) are in shared memory
-// lg[TB][E].  256 threads; warp w owns tokens (TB/8) w .. (TB/8)(w+1) - 1.
-// st_m, st_s, st_h hold TB floats each.
+// lg[TB][router_lde(E)].  256 threads; warp w owns tokens (TB/8) w ..
+// (TB/8)(w+1) - 1.  st_m, st_s, st_h hold TB floats each.  Without top-k
+// (do_select = 0) the tile is turned into probabilities in place and the
+// expert-major copy probsT is written from it in segments of TB tokens.
 template <int TB>
 __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m, float *st_s,
                                      float *st_h, int t0) {
     constexpr int TPWR = TB / 8;
-    const int E = a.E;
+    const int E = a.E, lde = router_lde(E);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Softmax statistics per token (warp per 4 tokens), optional probs rows.
     for (int r = 0; r < TPWR; ++r) {
         const int tt = TPWR * warp + r, t = t0 + tt;
-        const float *row = lg + tt * E;
+        float *row = lg + tt * lde;
         float m = -CUDART_INF_F;
         for (int e = lane; e < E; e += 32) m = fmaxf(m, row[e]);
 #pragma unroll
@@ -295,21 +302,42 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
             st_s[tt] = s;
             st_h[tt] = t < a.T ? logf(s) - hz / s : 0.f;
         }
-        if (t < a.T && a.probs)
+        if (!a.do_select) {
+            for (int e = lane; e < E; e += 32) {
+                const float p = expf(row[e] - m) / s;
+                row[e] = p;
+                if (t < a.T && a.probs) a.probs[(size_t)t * E + e] = p;
+            }
+        } else if (t < a.T && a.probs) {
             for (int e = lane; e < E; e += 32) a.probs[(size_t)t * E + e] = expf(row[e] - m) / s;
+        }
     }
     __syncthreads();
 
     // Column pass: per-block partial sums of probs (fixed token order) and
-    // the expert-major copy used by quantile balancing.
-    for (int e = tid; e < E; e += 256) {
-        float sum = 0.f;
-        for (int tt = 0; tt < TB && t0 + tt < a.T; ++tt) {
-            const float p = expf(lg[tt * E + e] - st_m[tt]) / st_s[tt];
-            sum += p;
-            if (a.probsT) a.probsT[(size_t)e * a.T + t0 + tt] = p;
+    // the expert-major copy used by quantile balancing and expert choice.
+    const int nt = min(TB, a.T - t0);
+    if (!a.do_select) {
+        for (int e = tid; e < E; e += 256) {
+            float sum = 0.f;
+            for (int tt = 0; tt < nt; ++tt) sum += lg[tt * lde + e];
+            if (a.p_partial) a.p_partial[(size_t)blockIdx.x * E + e] = sum;
         }
-        if (a.p_partial) a.p_partial[(size_t)blockIdx.x * E + e] = sum;
+        if (a.probsT)
+            for (int i = tid; i < TB * E; i += 256) {
+                const int e = i / TB, tt = i - e * TB;
+                if (tt < nt) a.probsT[(size_t)e * a.T + t0 + tt] = lg[tt * lde + e];
+            }
+    } else {
+        for (int e = tid; e < E; e += 256) {
+            float sum = 0.f;
+            for (int tt = 0; tt < nt; ++tt) {
+                const float p = expf(lg[tt * lde + e] - st_m[tt]) / st_s[tt];
+                sum += p;
+                if (a.probsT) a.probsT[(size_t)e * a.T + t0 + tt] = p;
+            }
+            if (a.p_partial) a.p_partial[(size_t)blockIdx.x * E + e] = sum;
+        }
     }
     if (a.ent_partial && tid == 0) {
         float tot = 0.f;
@@ -323,7 +351,7 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
     for (int r = 0; r < TPWR; ++r) {
         const int tt = TPWR * warp + r, t = t0 + tt;
         if (t >= a.T) break;
-        const float *row = lg + tt * E;
+        const float *row = lg + tt * lde;
         const float m = st_m[tt], s = st_s[tt];
         float sc[kTopkPerLane];
 #pragma unroll
@@ -355,9 +383,9 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
 template <typename TX>
 __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
     extern __shared__ __align__(16) float smem[];
-    const int E = a.E, d = a.d;
-    float *lg = smem;                         // [kTB][E]
-    float *xs = lg + kTB * E;                 // [kDK][kTB]
+    const int E = a.E, d = a.d, lde = router_lde(E);
+    float *lg = smem;                         // [kTB][lde]
+    float *xs = lg + kTB * lde;               // [kDK][kTB]
     float *wsh = xs + kDK * kTB;              // [kDK][kEC + 4]
     float *st_m = wsh + kDK * (kEC + 4);      // [kTB]
     float *st_s = st_m + kTB;                 // [kTB]
@@ -410,7 +438,7 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
             if (e < E) {
                 const float lb = a.logit_bias ? a.logit_bias[e] : 0.f;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) lg[(4 * warp + r) * E + e] = acc[r][i] + lb;
+                for (int r = 0; r < 4; ++r) lg[(4 * warp + r) * lde + e] = acc[r][i] + lb;
             }
         }
     }
@@ -449,22 +477,54 @@ template <int TB>
 __global__ void __launch_bounds__(256) router_from_logits_kernel(RouterArgs a,
                                                                  const float *part, int S) {
     extern __shared__ __align__(16) float smem[];
-    const int E = a.E;
+    const int E = a.E, lde = router_lde(E);
     float *lg = smem;
-    float *st_m = lg + TB * E;
+    float *st_m = lg + TB * lde;
     float *st_s = st_m + TB;
     float *st_h = st_s + TB;
     const int t0 = blockIdx.x * TB;
     const size_t plane = (size_t)a.T * E;
-    for (int i = threadIdx.x; i < TB * E; i += blockDim.x) {
-        const int tt = i / E, e = i - tt * E, t = t0 + tt;
-        float v = 0.f;
-        if (t < a.T) {
-            const size_t o = (size_t)t * E + e;
-            for (int sp = 0; sp < S; ++sp) v += part[sp * plane + o];
-            if (a.logit_bias) v += a.logit_bias[e];
+    // The tile's logits are TB * E consecutive floats of each plane: read
+    // them as float4 (E % 4 == 0), four per thread in flight.
+    const int n = min(TB, a.T - t0) * E;
+    const float *src = part + (size_t)t0 * E;
+    if ((E & 3) == 0) {
+        constexpr int kV = 4;
+        for (int j0 = threadIdx.x; j0 < TB * E / 4; j0 += kV * blockDim.x) {
+            float4 v[kV];
+#pragma unroll
+            for (int q = 0; q < kV; ++q) {
+                const int j = j0 + q * blockDim.x;
+                v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (4 * j < n)
+                    for (int sp = 0; sp < S; ++sp) {
+                        const float4 u =
+                            reinterpret_cast<const float4 *>(src + sp * plane)[j];
+                        v[q].x += u.x; v[q].y += u.y; v[q].z += u.z; v[q].w += u.w;
+                    }
+            }
+#pragma unroll
+            for (int q = 0; q < kV; ++q) {
+                const int j = j0 + q * blockDim.x;
+                if (j >= TB * E / 4) break;
+                const int i = 4 * j, tt = i / E, e = i - tt * E;
+                const float w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    lg[tt * lde + e + c] =
+                        w[c] + (a.logit_bias && i < n ? a.logit_bias[e + c] : 0.f);
+            }
         }
-        lg[i] = v;
+    } else {
+        for (int i = threadIdx.x; i < TB * E; i += blockDim.x) {
+            const int tt = i / E, e = i - tt * E;
+            float v = 0.f;
+            if (i < n) {
+                for (int sp = 0; sp < S; ++sp) v += src[sp * plane + i];
+                if (a.logit_bias) v += a.logit_bias[e];
+            }
+            lg[tt * lde + e] = v;
+        }
     }
     __syncthreads();
     router_rows_epilogue<TB>(a, lg, st_m, st_s, st_h, t0);
@@ -474,8 +534,8 @@ __global__ void __launch_bounds__(256) router_from_logits_kernel(RouterArgs a,
 // Quantile bias: b_e = -(v_lo + frac (v_hi - v_lo)) with v_lo, v_hi the
 // order statistics of rank lo and lo+1 of column e (linear interpolation,
 // h = (T-1) q, lo = floor h, frac = h - lo).  One CTA of 512 threads per
-// expert.  v_lo by a 3-pass radix select on the fp32 bit patterns (11, 11
-// and 10 bits; probabilities are >= 0, so bit order equals value order);
+// expert.  v_lo by a 4-pass radix select on the fp32 bit patterns (8 bits a
+// pass; probabilities are >= 0, so bit order equals value order);
 // v_hi from one more pass: v_lo again if at least lo + 2 values are <= v_lo,
 // else the smallest value above it.
 // --------------------------------------------------------------------------
@@ -509,61 +569,67 @@ __device__ int block_exclusive_scan_512(int v, int *warp_tot, int *total) {
     return r;
 }
 
-constexpr int kRadixBins = 2048;
+constexpr int kRadixDigit = 8;                   // bits resolved per pass (4 passes)
+constexpr int kRadixBins = 1 << kRadixDigit;
+constexpr int kRadixWarps = 16;                  // 512 threads
+constexpr int kRadixBatch = 8;       // column values loaded per thread before binning
 
-// Shared scratch of the 512-thread radix select.
+// Shared scratch of the 512-thread radix select: one histogram per warp, so
+// that warps never contend for a counter (probabilities of similar size share
+// their top bits, and one block-wide histogram serialised on a few bins).
 struct RadixScratch {
-    unsigned hist[kRadixBins];
+    unsigned hist[kRadixWarps][kRadixBins];
     int warp_tot[16];
     int total;
     unsigned sel[2];
 };
 
-// Value of rank r (0-based, ascending) of col[0..T); 512 threads.
+// Value of rank r (0-based, ascending) of col[0..T); 512 threads.  Four
+// passes of 8 bits over the fp32 bit patterns (values >= 0, so bit order is
+// value order).
 __device__ float radix_select_col(const float *col, int T, long long r, RadixScratch &sc) {
     unsigned prefix = 0, mask = 0;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = shifts[pass];
-        const unsigned nb = 1u << widths[pass];
-        for (unsigned i = tid; i < kRadixBins; i += blockDim.x) sc.hist[i] = 0;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned *my_hist = sc.hist[warp];
+    for (int shift = 32 - kRadixDigit; shift >= 0; shift -= kRadixDigit) {
+        for (int i = tid; i < kRadixWarps * kRadixBins; i += blockDim.x)
+            (&sc.hist[0][0])[i] = 0;
         __syncthreads();
+        // kRadixBatch loads in flight per thread; every lane of a warp runs
+        // the same number of iterations (n is a multiple of the block size)
         const int n = (T + blockDim.x - 1) / blockDim.x * blockDim.x;
-        for (int i = tid; i < n; i += blockDim.x) {
-            unsigned bin = 0xffffffffu;
-            if (i < T) {
-                const unsigned b = __float_as_uint(col[i]);
-                if ((b & mask) == prefix) bin = (b >> shift) & (nb - 1);
+        for (int i0 = tid; i0 < n; i0 += kRadixBatch * blockDim.x) {
+            unsigned v[kRadixBatch];
+#pragma unroll
+            for (int q = 0; q < kRadixBatch; ++q) {
+                const int i = i0 + q * blockDim.x;
+                v[q] = i < T ? __float_as_uint(col[i]) : 0u;
             }
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sc.hist[bin], __popc(peers));
+#pragma unroll
+            for (int q = 0; q < kRadixBatch; ++q) {
+                const int i = i0 + q * blockDim.x;
+                if (i0 - tid + q * (int)blockDim.x >= n) break;     // uniform over the block
+                unsigned bin = 0xffffffffu;
+                if (i < T && (v[q] & mask) == prefix) bin = (v[q] >> shift) & (kRadixBins - 1);
+                const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                if (bin != 0xffffffffu && lane == __ffs(peers) - 1)
+                    atomicAdd(&my_hist[bin], __popc(peers));
+            }
         }
         __syncthreads();
-        // thread tid owns bins [4 tid, 4 tid + 4): find the bin holding rank r
-        unsigned loc[4];
+        // thread tid < 256 owns bin tid: its count over all warps, then the
+        // bin holding rank r
         int local = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            loc[q] = sc.hist[4 * tid + q];
-            local += (int)loc[q];
-        }
+        if (tid < kRadixBins)
+            for (int w = 0; w < kRadixWarps; ++w) local += (int)sc.hist[w][tid];
         const int ex = block_exclusive_scan_512(local, sc.warp_tot, &sc.total);
-        if ((long long)ex <= r && r < (long long)ex + local) {
-            long long cum = ex;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (r < cum + (long long)loc[q]) {
-                    sc.sel[0] = 4 * tid + q;
-                    sc.sel[1] = (unsigned)(r - cum);
-                    break;
-                }
-                cum += loc[q];
-            }
+        if (local > 0 && (long long)ex <= r && r < (long long)ex + local) {
+            sc.sel[0] = (unsigned)tid;
+            sc.sel[1] = (unsigned)(r - ex);
         }
         __syncthreads();
         prefix |= sc.sel[0] << shift;
-        mask |= (nb - 1) << shift;
+        mask |= (unsigned)(kRadixBins - 1) << shift;
         r = sc.sel[1];
         __syncthreads();
     }
@@ -584,10 +650,19 @@ __global__ void __launch_bounds__(512) quantile_bias_kernel(const float *probsT,
         const unsigned vb = __float_as_uint(v_lo);
         int le = 0;
         unsigned mn = 0xffffffffu;
-        for (int i = threadIdx.x; i < T; i += blockDim.x) {
-            const unsigned b = __float_as_uint(col[i]);
-            if (b <= vb) ++le;
-            else mn = min(mn, b);
+        for (int i0 = threadIdx.x; i0 < T; i0 += kRadixBatch * blockDim.x) {
+            unsigned v[kRadixBatch];
+#pragma unroll
+            for (int q = 0; q < kRadixBatch; ++q) {
+                const int i = i0 + q * blockDim.x;
+                v[q] = i < T ? __float_as_uint(col[i]) : 0xffffffffu;
+            }
+#pragma unroll
+            for (int q = 0; q < kRadixBatch; ++q) {
+                if (i0 + q * (int)blockDim.x >= T) break;
+                if (v[q] <= vb) ++le;
+                else mn = min(mn, v[q]);
+            }
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
@@ -608,21 +683,29 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const float *probs, co
                                                           int T, int E, int k, int32_t *idx,
                                                           float *w, int n_cand,
                                                           int32_t *cand_idx, float *cand_w) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    extern __shared__ float srows[];      // [8][E]: the probabilities of the block's tokens
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int t = blockIdx.x * 8 + wib;
     if (t >= T) return;
     const float *row = probs + (size_t)t * E;
+    float *srow = srows + wib * E;
     float sc[kTopkPerLane];
 #pragma unroll
     for (int i = 0; i < kTopkPerLane; ++i) {
         const int e = lane + 32 * i;
-        sc[i] = e < E ? row[e] + (bias ? bias[e] : 0.f) : -CUDART_INF_F;
+        sc[i] = -CUDART_INF_F;
+        if (e < E) {
+            const float p = row[e];
+            srow[e] = p;
+            sc[i] = p + (bias ? bias[e] : 0.f);
+        }
     }
+    __syncwarp();
     float psum = 0.f, my_p = 0.f;
     int my_e = 0;
     for (int j = 0; j < k + n_cand; ++j) {
         const int bi = warp_take_max(sc, lane);
-        const float pw = row[bi];
+        const float pw = srow[bi];
         if (j < k) psum += pw;
         if (lane == j) { my_e = bi; my_p = pw; }
     }
@@ -725,7 +808,7 @@ cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, in
                                       cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     constexpr int TB = kTBLogits;
-    const size_t smem = sizeof(float) * ((size_t)TB * a.E + 3 * TB);
+    const size_t smem = sizeof(float) * ((size_t)TB * router_lde(a.E) + 3 * TB);
     cudaError_t err = cudaFuncSetAttribute(router_from_logits_kernel<TB>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -738,8 +821,8 @@ cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int
                                int32_t *idx, float *w, cudaStream_t st, int n_cand,
                                int32_t *cand_idx, float *cand_w) {
     if (T == 0) return cudaSuccess;
-    select_rows_kernel<<<(T + 7) / 8, 256, 0, st>>>(probs, bias, T, E, k, idx, w, n_cand,
-                                                    cand_idx, cand_w);
+    select_rows_kernel<<<(T + 7) / 8, 256, sizeof(float) * 8 * E, st>>>(
+        probs, bias, T, E, k, idx, w, n_cand, cand_idx, cand_w);
     note_launch();
     return cudaGetLastError();
 }

@@ -10,7 +10,7 @@ import oracle.moe_oracle as om
 import sparse_mixture_experts_47_b300 as moe
 from tests.conftest import load_golden
 from tests.parity import (FP_ATOL, W_ATOL, act_dtype, compare_y, full_check, gpu_layer,
-                          oracle_layer, weights_dict, y_tol)
+                          oracle_layer, weights_dict, y_allow)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -34,6 +34,15 @@ SMALL = {
     "switch_T3_split": (mi.workload("switch").with_sizes(d_model=2048, d_ff=512), 3),
     "deepseek_T100_split": (mi.workload("deepseek").with_sizes(d_model=1024, n_experts=64,
                                                                d_ff=256, d_ff_shared=1024), 100),
+    # about 75-280 rows per expert: 128-row tiles up, and a down projection on
+    # tiles of up to 256 rows whose MMA N is the tile's row count rounded to
+    # 16 (ragged widths, a split reduction, many experts, skewed loads)
+    "mixtral_var": (mi.workload("mixtral").with_sizes(d_model=512, d_ff=1024), 1100),
+    "switch_var_ragged": (mi.workload("switch").with_sizes(d_model=136, d_ff=264), 2080),
+    "mixtral_var_split": (mi.workload("mixtral").with_sizes(d_model=1024, d_ff=2048), 584),
+    "e896_var": (mi.workload("e896").with_sizes(d_model=128, d_ff=64), 8192),
+    "deepseek_var": (mi.workload("deepseek").with_sizes(d_model=256, n_experts=64, d_ff=384,
+                                                        d_ff_shared=192), 1200),
     # capacity factor 1.0 with k > 1: overflow dropped in (t, j) order
     "mixtral_cap_small": (mi.workload("mixtral_cap").with_sizes(d_model=512, d_ff=1024), 300),
     "deepseek_cap_small": (mi.workload("deepseek_cap").with_sizes(
@@ -78,14 +87,16 @@ def test_batch_invariance(name, T):
     w, _ = SMALL[name]
     inp = mi.generate(w, T, DEV)
     big = gpu_layer(w, T, inp)
+    # magnitude of y's terms for the rounding allowance of both runs
+    y_abs = oracle_layer(w, inp, tokens=range(16))["y_abs"]
+    rms = float(np.sqrt(np.mean(big["y"].astype(np.float64) ** 2)))
     for t in (1, 16):
         sub = dict(inp)
         sub["x"] = inp["x"][:t].contiguous()
         small = gpu_layer(w, t, sub)
         assert np.array_equal(small["idx"], big["idx"][:t])
         assert np.array_equal(small["w"], big["w"][:t])
-        rms = float(np.sqrt(np.mean(big["y"].astype(np.float64) ** 2)))
-        assert np.max(np.abs(small["y"] - big["y"][:t])) <= y_tol(w) * rms
+        assert np.all(np.abs(small["y"] - big["y"][:t]) <= y_allow(w, rms, y_abs[:t]))
 
 
 def test_layer_graph_and_pipeline_match_eager():
@@ -251,7 +262,7 @@ def test_expert_ffn_and_combine_stages(name):
         ref[a:b] = om.expert_ffn(x[rows], inp["w1"][e], None if inp["w3"] is None else inp["w3"][e],
                                  inp["w2"][e], w.act, act_dtype(w))
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    assert np.max(np.abs(got - ref)) <= y_tol(w) * rms
+    assert np.all(np.abs(got - ref) <= y_allow(w, rms, np.abs(ref)))
     # combine with the oracle's expert outputs (rounded to fp32) and weights
     shared = None
     if w.d_ff_shared:

@@ -284,16 +284,19 @@ def pin_round_to_bf16():
 
 
 def pin_bf16_activation_ffn():
-    # E = 1 with a bf16 intermediate: the page's Expert in a bf16 model stores
-    # h in bf16 before w2; torch.nn.functional in float64 with h rounded by torch.
+    # E = 1 with bf16 storage: the page's Expert in a bf16 model stores h in
+    # bf16 before w2 and returns its output as a bf16 tensor (gate weight 1
+    # here); torch.nn.functional in float64 with both tensors rounded by torch.
     inp = _rand_layer(13, 16, 1, 24, "swiglu")
     out = om.moe_forward(inp, 1, "swiglu", act_dtype="bf16")
     x, w1, w3, w2 = (torch.tensor(np.asarray(a, dtype=np.float64))
                      for a in (inp["x"], inp["w1"][0], inp["w3"][0], inp["w2"][0]))
     h = Fnn.silu(Fnn.linear(x, w1)) * Fnn.linear(x, w3)
     h = h.to(torch.float32).to(torch.bfloat16).to(torch.float64)
-    ref = Fnn.linear(h, w2).numpy()
+    o = Fnn.linear(h, w2)
+    ref = o.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
     assert np.allclose(out["y"], ref, atol=1e-12)
+    assert not np.allclose(ref, o.numpy(), atol=1e-6)   # the output rounding is visible
     exact = om.moe_forward(inp, 1, "swiglu")
     assert not np.allclose(out["y"], exact["y"], atol=1e-6)   # the rounding is visible
 
@@ -566,6 +569,12 @@ def _mut_round_truncate(a):
     return np.trunc(a / q) * q                      # truncation instead of nearest-even
 
 
+def _mut_ffn_output_unrounded(x_rows, w1, w3, w2, act, act_dtype="fp64"):
+    a = x_rows @ om._f64(w1).T
+    h = om._silu(a) * (x_rows @ om._f64(w3).T) if act == "swiglu" else np.maximum(a, 0.0)
+    return om.ACT_ROUNDING[act_dtype](h) @ om._f64(w2).T   # output row left unrounded
+
+
 def _mut_capacity_floor(T, k, E, cf):
     return T * k if cf <= 0 else int(cf * T / E)    # drops k (one of the page variants)
 
@@ -661,6 +670,7 @@ MUTATIONS = [
     ("topk_desc", _mut_topk_ascending),
     ("topk_desc", _mut_topk_unstable_ties),
     ("expert_ffn", _mut_silu_on_w3),
+    ("expert_ffn", _mut_ffn_output_unrounded),
     ("router_logits", _mut_router_reversed_experts),
     ("router_logits", _mut_router_sign),
     ("dispatch", _mut_drop_last),
