@@ -32,6 +32,10 @@
 // MMA's N chosen per tile: a tile holds up to 256 of one expert's rows and
 // its MMA N is that count rounded up to 16, so an expert with 146 rows costs
 // a 160-wide tile instead of two 128-row tiles.
+// MH = 2 (NT = 0, N = 256): tiles of 256 token rows, two M = 128 MMAs per
+// K step sharing the weight tile, so a 64 KB stage feeds twice the MMA work
+// of a 48 KB one; the 256 x 256 fp32 accumulator fills TMEM, so there is one
+// accumulator and the epilogue does not overlap the next tile's MMAs.
 // Every mbarrier wait is bounded (about 2 s of no progress); on expiry the
 // kernel sets the device error word, stops issuing, lets its own copies and
 // MMAs land, frees TMEM and returns.
@@ -59,11 +63,12 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 // the M side (A = 128 rows of W1, plus 128 rows of W3 for SwiGLU), token rows
 // on the N side (NT rows).  A stage holds the activation tile first, then the
 // weight tile(s); every tile is a multiple of 1024 bytes.
-template <int MODE, int NT, int BN> struct Geo {
+template <int MODE, int NT, int BN, int MH> struct Geo {
+    static_assert(MH == 1 || (MH == 2 && NT == 0 && BN == BNM), "256-row tiles: NT 0, N 256");
     static constexpr bool SWAP = NT > 0;
     static constexpr bool VARN = NT == kVarRows;                 // MMA N chosen per tile
     static_assert(!VARN || MODE == GEMM_DOWN, "per-tile width: down projection only");
-    static constexpr int ROWS = SWAP ? NT : BM;                  // activation rows per tile
+    static constexpr int ROWS = SWAP ? NT : BM * MH;             // activation rows per tile
     static constexpr int WT = (SWAP && MODE == GEMM_UP_SWIGLU) ? 2 : 1;
     // rows of one weight TMA box: 128 (NT > 0), BN / 2 (NT = 0: two boxes)
     static constexpr int BOX = SWAP ? WROWS : BN / 2;
@@ -71,7 +76,9 @@ template <int MODE, int NT, int BN> struct Geo {
     static constexpr int W_BYTES = SWAP ? WT * WROWS * BK * 2 : BN * BK * 2;
     static constexpr int STAGE_BYTES = ACT_BYTES + W_BYTES;
     static constexpr int FIT = (kSmemLimit - kSmemExtra) / STAGE_BYTES;
-    static constexpr int STAGES = SWAP ? (FIT < 8 ? FIT : 8) : (BN == BNM ? 4 : 6);
+    static constexpr int STAGES =
+        SWAP ? (FIT < 8 ? FIT : 8) : MH == 2 ? 3 : (BN == BNM ? 4 : 6);
+    static constexpr int NACC = MH == 2 ? 1 : 2;                 // accumulator buffers
     // output columns (features) of one tile
     static constexpr int OUTC = SWAP ? WROWS : (MODE == GEMM_UP_SWIGLU ? BN / 2 : BN);
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + kSmemExtra;
@@ -246,7 +253,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
     return u;
 }
 
-template <int MODE, int NT, int BN>
+template <int MODE, int NT, int BN, int MH>
 __global__ void __launch_bounds__(256, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmA64,
@@ -254,7 +261,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmA16,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1, Args g) {
-    using G = Geo<MODE, NT, BN>;
+    using G = Geo<MODE, NT, BN, MH>;
     constexpr int STAGES = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -390,6 +397,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     } else {
                         tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
                                accum);
+                        if (MH == 2)    // rows 128..255 of the tile into columns 256..511
+                            tc_mma(d_tmem + BN, desc_sw128(sa + BM * BK * 2 + kk * 32),
+                                   desc_sw128(sb + kk * 32), idesc, accum);
                     }
                 }
                 tc_commit(empty0 + 8 * stage);
@@ -397,7 +407,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             if (!ok) break;
             tc_commit(tfull0 + 8 * acc);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            if (++acc == G::NACC) { acc = 0; acc_phase ^= 1; }
         }
         // All MMAs of this thread complete before TMEM can be freed.
         tc_commit(done_bar);
@@ -413,8 +423,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             const TileCoord c = decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
             tc_fence_after();
-            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+            const uint32_t tbase0 =
+                tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
             if (G::SWAP) {
+                const uint32_t tbase = tbase0;
                 // TMEM lane = output feature f, column = token row m0 + j.
                 const int f = c.n0 + quarter * 32 + lane;
                 const bool vf = f < g.N;
@@ -448,8 +460,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                 }
             } else {
-                const int row = c.m0 + quarter * 32 + lane;
+#pragma unroll 1
+              for (int hh = 0; hh < MH; ++hh) {    // 128-row halves (MH = 2)
+                const int row = c.m0 + hh * BM + quarter * 32 + lane;
                 const bool vrow = row < c.mend;
+                const uint32_t tbase = tbase0 + hh * BN;
                 if (MODE == GEMM_UP_SWIGLU) {
                     __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
 #pragma unroll 1
@@ -523,11 +538,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         }
                     }
                 }
+              }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            if (++acc == G::NACC) { acc = 0; acc_phase ^= 1; }
         }
     }
 
@@ -588,24 +604,25 @@ struct Maps {
     CUtensorMap a, a64, a32, a16, b0, b1;
 };
 
-template <int MODE, int NT, int BN>
+template <int MODE, int NT, int BN, int MH = 1>
 static cudaError_t launch_geo(const Maps &m, const Args &g, cudaStream_t st) {
-    using G = Geo<MODE, NT, BN>;
+    using G = Geo<MODE, NT, BN, MH>;
     static_assert(G::SMEM <= (size_t)kSmemLimit, "shared memory");
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, NT, BN>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)G::SMEM);
+    auto kern = grouped_gemm_tc_kernel<MODE, NT, BN, MH>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::SMEM);
     if (err != cudaSuccess) return err;
-    grouped_gemm_tc_kernel<MODE, NT, BN><<<num_sms(), 256, G::SMEM, st>>>(m.a, m.a64, m.a32,
-                                                                          m.a16, m.b0, m.b1, g);
+    kern<<<num_sms(), 256, G::SMEM, st>>>(m.a, m.a64, m.a32, m.a16, m.b0, m.b1, g);
     note_launch();
     return cudaGetLastError();
 }
 
 template <int MODE>
-static cudaError_t launch_mode(int nt, int bn, const Maps &m, const Args &g, cudaStream_t st) {
+static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args &g,
+                               cudaStream_t st) {
     switch (nt) {
         case 0:
+            if (mh == 2) return launch_geo<MODE, 0, BNM, 2>(m, g, st);
             return bn == BNM ? launch_geo<MODE, 0, BNM>(m, g, st)
                              : launch_geo<MODE, 0, BNM / 2>(m, g, st);
         case 16: return launch_geo<MODE, 16, BNM>(m, g, st);
@@ -624,7 +641,8 @@ static cudaError_t launch_mode(int nt, int bn, const Maps &m, const Args &g, cud
 // launch_build_tiles with row tiles of 128 (nt = 0) or nt rows (nt = 16, 32,
 // 64, 256: weights on the MMA's M side; 256, down projection only, sets the
 // MMA N per tile).  bn (nt = 0 only): MMA N of 256 or 128; 128 doubles the
-// output tiles when there are too few to fill the SMs.  A's column for
+// output tiles when there are too few to fill the SMs.  mh = 2 (nt = 0,
+// bn = 256 only): 256-row tiles, tile table built with 256-row tiles.  A's column for
 // reduction index k is k mod a_k_period (a_k_period = K: no wrap).  With k_splits > 1 split s of
 // every tile writes fp32 partial sums to C + s * split_stride: GEMM_DOWN
 // always (row-major [rows, ldc]); the up modes only with nt > 0, writing the
@@ -632,7 +650,8 @@ static cudaError_t launch_mode(int nt, int bn, const Maps &m, const Args &g, cud
 // k_splits = 1 up modes write the activation in bf16.  out_mode (GEMM_DOWN
 // with k_splits = 1 only): kOutF32, kOutBF16 (bf16 output), kOutF32Rounded
 // (fp32 output holding the nearest bf16 of each value).
-cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_rows, int a_cols,
+cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long long a_rows,
+                           int a_cols,
                            const void *B0, const void *B1, int E, int b_rows, int N, int K,
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,
@@ -643,6 +662,7 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_
     const int nk = (K + BK - 1) / BK;
     if (nt != 0 && nt != 16 && nt != 32 && nt != 64 && nt != kVarRows) return cudaErrorInvalidValue;
     if (bn != BNM && bn != BNM / 2) return cudaErrorInvalidValue;
+    if (mh != 1 && (mh != 2 || nt != 0 || bn != BNM)) return cudaErrorInvalidValue;
     if (out_mode != kOutF32 && (mode != GEMM_DOWN || k_splits != 1 || N % 8 != 0 ||
                                 (out_mode != kOutBF16 && out_mode != kOutF32Rounded)))
         return cudaErrorInvalidValue;
@@ -653,7 +673,7 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_
     k_splits = (nk + kbps - 1) / kbps;          // every split gets at least one K block
     const bool var = nt == kVarRows;
     if (var && mode != GEMM_DOWN) return cudaErrorInvalidValue;
-    const int rows = var ? 128 : nt ? nt : BM;
+    const int rows = var ? 128 : nt ? nt : BM * mh;
     Maps m;
     if (!make_map(&m.a, A, a_rows, a_cols, rows)) return cudaErrorInvalidValue;
     m.a64 = m.a32 = m.a16 = m.a;
@@ -683,9 +703,9 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_
     g.C = C;
     g.ldc = ldc;
     g.out_mode = out_mode;
-    if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, m, g, st);
-    if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, m, g, st);
-    return launch_mode<GEMM_DOWN>(nt, bn, m, g, st);
+    if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, mh, m, g, st);
+    if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, mh, m, g, st);
+    return launch_mode<GEMM_DOWN>(nt, bn, mh, m, g, st);
 }
 
 }  // namespace moe

@@ -161,7 +161,8 @@ cudaError_t launch_simt_gemm(const GroupedGemmArgs &g, int mode, int dtype, cuda
 
 // gemm_tcgen05.cu: tcgen05/TMEM grouped GEMM for the bf16 workloads.
 constexpr int kTcBM = 128;
-cudaError_t launch_tc_gemm(int mode, int nt, int bn, const void *A, long long a_rows, int a_cols,
+cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long long a_rows,
+                           int a_cols,
                            const void *B0, const void *B1, int E, int b_rows, int N, int K,
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,

@@ -107,6 +107,7 @@ struct FfnPlan {
     int nt, s_up, s_down;
     int bn_up, bn_down;     // nt = 0: MMA N (256, or 128 when tiles are few)
     int nt_down;            // geometry of the down projection
+    int mh_down;            // nt_down = 0: 128-row halves per tile (1, or 2: 256 rows)
 };
 constexpr int kPlanSMs = 148;   // SM count the split choice assumes (B300)
 constexpr int kVarTileRows = 256;
@@ -116,6 +117,14 @@ constexpr int kVarTileRows = 256;
 // of every expert is mostly padding (896 experts of about 146 rows).  It is
 // chosen when the padding of 128-row tiles exceeds its own by more than this.
 constexpr double kVarPadGain = 1.3;
+// 256-row tiles for the down projection (two M = 128 MMAs per weight stage;
+// one TMEM accumulator, so the epilogue is not overlapped) when the experts
+// hold at least kWideMinRows rows on average and the reduction is at least
+// kWideMinK long.  Measured at the Mixtral shape (K = 14336): down 2.70 ->
+// 2.41 ms at T = 16384; the SwiGLU up projection (K = 4096) went 5.0 ->
+// 6.1 ms, its unoverlapped epilogue being a fifth of a tile.
+constexpr long long kWideMinRows = 512;
+constexpr long long kWideMinK = 8192;
 
 // Split the reduction only when the tiles do not fill the SMs once, and then
 // only up to one round of work items: measured at the Mixtral shape, a split
@@ -134,7 +143,7 @@ int split_count(long long tiles, long long nk) {
 // rows: dispatched rows (T*k routed, T shared); groups: experts; K = d.
 FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long long F,
                  bool swiglu) {
-    FfnPlan p{0, 1, 1, 256, 256, 0};
+    FfnPlan p{0, 1, 1, 256, 256, 0, 1};   // nt s_up s_down bn_up bn_down nt_down mh_down
     if (c->dtype != MOE_DTYPE_BF16 || rows <= 0 || F <= 0) return p;
     const long long d = c->d_model;
     const long long active = std::min(groups, rows);
@@ -149,6 +158,7 @@ FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long lon
         const long long mt = (rows + 127) / 128 + active;
         if (mt * ((F + up_cols - 1) / up_cols) < 2 * kPlanSMs) p.bn_up = 128;
         if (mt * ((d + 255) / 256) < 2 * kPlanSMs) p.bn_down = 128;
+        if (per >= kWideMinRows && F >= kWideMinK && p.bn_down == 256) p.mh_down = 2;
         const double pad128 = (double)((per + 127) / 128 * 128) / per;
         const double pad16 = (double)((per + 15) / 16 * 16) / per;
         if (pad128 > kVarPadGain * pad16) {
@@ -376,7 +386,7 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         note_launch();
         MOE_CUDA(cudaGetLastError());
         MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E,
+        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E,
                                 kRouterParts * dp,
                                 dp, S, s.T * s.E, te, ts, nt, off, part, a.E, 0, st));
         int planes = S;
@@ -426,25 +436,26 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
                                 ntiles, st));
     if (plan.s_up > 1) {
         const int upw = up_mode == GEMM_UP_SWIGLU ? 2 : 1;
-        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, A, rows, d, w1, w3, groups, F, F, d, d,
-                                plan.s_up,
+        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, 1, A, rows, d, w1, w3, groups, F, F, d,
+                                d, plan.s_up,
                                 rows * upw * F, tile_e, tile_start, ntiles, offsets, up_part,
                                 upw * F, 0, st));
         MOE_CUDA(launch_split_activation(up_part, plan.s_up, rows * upw * F, F,
                                          up_mode == GEMM_UP_SWIGLU, offsets + groups, rows,
                                          static_cast<__nv_bfloat16 *>(h), st));
     } else {
-        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, A, rows, d, w1, w3, groups, F, F, d, d,
-                                1, 0, tile_e, tile_start, ntiles, offsets, h, F, 0, st));
+        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, 1, A, rows, d, w1, w3, groups, F, F, d,
+                                d, 1, 0, tile_e, tile_start, ntiles, offsets, h, F, 0, st));
     }
     if (up_stage >= 0) {
         stage_end(up_stage, ev, st);
         ev = stage_begin(st);
     }
-    if (plan.nt_down != nt)
-        MOE_CUDA(launch_build_tiles(offsets, groups, plan.nt_down ? plan.nt_down : kTcBM, tile_e,
-                                    nullptr, tile_start, ntiles, st));
-    MOE_CUDA(launch_tc_gemm(GEMM_DOWN, plan.nt_down, plan.bn_down, h, rows, F, w2, nullptr,
+    const int mh_down = plan.nt_down ? 1 : plan.mh_down;
+    if (plan.nt_down != nt || mh_down != 1)
+        MOE_CUDA(launch_build_tiles(offsets, groups, plan.nt_down ? plan.nt_down : kTcBM * mh_down,
+                                    tile_e, nullptr, tile_start, ntiles, st));
+    MOE_CUDA(launch_tc_gemm(GEMM_DOWN, plan.nt_down, plan.bn_down, mh_down, h, rows, F, w2, nullptr,
                             groups, d, d, F, F, plan.s_down, rows * d, tile_e, tile_start, ntiles,
                             offsets, out, d, plan.s_down == 1 ? out_mode : kOutF32, st));
     if (down_stage >= 0) stage_end(down_stage, ev, st);

@@ -43,6 +43,9 @@ SMALL = {
     "e896_var": (mi.workload("e896").with_sizes(d_model=128, d_ff=64), 8192),
     "deepseek_var": (mi.workload("deepseek").with_sizes(d_model=256, n_experts=64, d_ff=384,
                                                         d_ff_shared=192), 1200),
+    # about 525 rows per expert and a reduction of 8192: the down projection
+    # on tiles of 256 rows, two M = 128 MMAs per weight stage (ragged tails)
+    "mixtral_wide": (mi.workload("mixtral").with_sizes(d_model=2048, d_ff=8192), 2100),
     # capacity factor 1.0 with k > 1: overflow dropped in (t, j) order
     "mixtral_cap_small": (mi.workload("mixtral_cap").with_sizes(d_model=512, d_ff=1024), 300),
     "deepseek_cap_small": (mi.workload("deepseek_cap").with_sizes(
