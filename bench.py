@@ -408,7 +408,8 @@ def run_ours(args, w, T):
     up_ms = stage_ms["up"] / max(calls, 1)
     up_tflops = up_flops / (up_ms / 1e3) / 1e12
     up_gbs = up_bytes / (up_ms / 1e3) / 1e9
-    recs = [r for r in traffic_record("gemm_tcgen05.cu") or [] if r.get("workload") == w.name]
+    recs = [r for r in traffic_record("gemm_tcgen05.cu") or []
+            if r.get("workload") == w.name and not args.n_experts]
     exact = [r for r in recs if r.get("T") == T]
     tr = exact[0] if exact else (recs[-1] if recs else None)
     up_tensor_bound = up_flops / tc_peak >= up_bytes / hbm
@@ -490,9 +491,14 @@ def main():
     ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
                     help="replay one captured CUDA graph of the layer per step (default) "
                          "or call the layer eagerly")
+    ap.add_argument("--n-experts", type=int, default=None,
+                    help="override the workload's expert count (a reduced case for profiler "
+                         "captures; with --T scaled alike it keeps the rows per expert)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     w = mi.workload(args.workload)
+    if args.n_experts:
+        w = w.with_sizes(n_experts=args.n_experts)
     T = args.T or max(w.tokens)
     if args.impl == "reference":
         run_reference(args, w, T)
