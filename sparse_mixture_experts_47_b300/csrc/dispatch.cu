@@ -15,6 +15,8 @@
 //      its expert is base[b][e] + (earlier slots of e in the chunk), found
 //      with __match_any_sync; rank < C keeps the slot at row offsets[e] +
 //      rank.
+// A batch of at most one chunk (T*k <= 1024) runs the three steps in one
+// CTA instead, with the same results.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -143,12 +145,84 @@ __global__ void dispatch_scatter_kernel(const int32_t *idx, long long n, int E, 
     }
 }
 
+// n <= kDispatchChunk slots: histogram, counts and offsets, then warp 0's
+// in-order walk, in one CTA of 1024 threads (E <= 1024).
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t *idx, int n, int E,
+                                                              long long C, int32_t *counts,
+                                                              int32_t *offsets, int32_t *perm,
+                                                              int32_t *inv, int32_t *n_dropped) {
+    extern __shared__ int sh[];          // [E] counts, then running ranks; [E] offsets
+    int *h = sh, *off = sh + E;
+    __shared__ int warp_tot[32];
+    __shared__ int total;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < E; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    if (tid < n) {
+        const int e = idx[tid];
+        if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+        else flag_error(kErrBadIndex);
+    }
+    __syncthreads();
+    int run = 0, kept = 0;
+    if (tid < E) {
+        run = h[tid];
+        kept = (long long)run < C ? run : (int)C;
+        if (counts) counts[tid] = run;
+    }
+    block_exclusive_scan_1024(run, warp_tot, &total);
+    const int all_total = total;
+    __syncthreads();
+    const int ex = block_exclusive_scan_1024(kept, warp_tot, &total);
+    if (tid < E) {
+        off[tid] = ex;
+        h[tid] = 0;
+        if (offsets) offsets[tid] = ex;
+    }
+    if (tid == 0) {
+        if (offsets) offsets[E] = total;
+        if (n_dropped) *n_dropped = all_total - total;
+    }
+    __syncthreads();
+    if (tid >= 32) return;
+    const int lane = tid;
+    for (int b = 0; b < n; b += 32) {
+        const int f = b + lane;
+        int e = -1;
+        if (f < n) {
+            e = idx[f];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int rank = 0;
+        if (e >= 0) rank = h[e] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (e >= 0 && lane == 31 - __clz(peers)) h[e] += __popc(peers);
+        __syncwarp();
+        if (f < n) {
+            if (e >= 0 && rank < C) {
+                const int s = off[e] + rank;
+                perm[s] = f;
+                inv[f] = s;
+            } else {
+                inv[f] = -1;
+            }
+        }
+    }
+}
+
 cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long long C,
                             int32_t *hist, int32_t *block_base, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *n_dropped,
                             cudaStream_t st) {
     (void)k;
     const int nblk = dispatch_blocks(n);
+    if (nblk == 1) {
+        dispatch_small_kernel<<<1, 1024, 2 * sizeof(int) * E, st>>>(
+            idx, (int)n, E, C, counts, offsets, perm, inv, n_dropped);
+        note_launch();
+        return cudaGetLastError();
+    }
     if (nblk > 0) {
         dispatch_hist_kernel<<<nblk, 256, sizeof(int) * E, st>>>(idx, n, E, hist);
         note_launch();

@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(512) ec_select_kernel(const float *probsT, int
     __shared__ RadixScratch sc;
     int *warp_tot = sc.warp_tot;
     __shared__ int total;
+    extern __shared__ float colbuf[];
     const int e = blockIdx.x;
     const float *col = probsT + (size_t)e * T;
     if (threadIdx.x == 0) {
@@ -39,6 +40,7 @@ __global__ void __launch_bounds__(512) ec_select_kernel(const float *probsT, int
         for (int t = threadIdx.x; t < T; t += blockDim.x) rowidx[(size_t)e * T + t] = -1;
         return;
     }
+    col = stage_col(col, T, colbuf);
     const float v = radix_select_col(col, T, (long long)(T - Cn), sc);
     // tokens strictly above v
     int above = 0;
@@ -121,7 +123,12 @@ cudaError_t launch_expert_choice(const float *probsT, int T, int E, int Cn, int3
                                  float *row_w, int32_t *rowidx, int32_t *counts,
                                  int32_t *offsets, int32_t *tok_cnt, int32_t *tok_start,
                                  int32_t *tok_rows, int32_t *n_unchosen, cudaStream_t st) {
-    ec_select_kernel<<<E, 512, 0, st>>>(probsT, T, E, Cn, perm, row_w, rowidx, counts, offsets);
+    const size_t smem = stage_col_bytes(T);
+    cudaError_t err = cudaFuncSetAttribute(ec_select_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    ec_select_kernel<<<E, 512, smem, st>>>(probsT, T, E, Cn, perm, row_w, rowidx, counts,
+                                           offsets);
     note_launch();
     const int grid = std::max(1, std::min((T + 255) / 256, 148 * 8));
     if (T > 0) {

@@ -389,12 +389,8 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E,
                                 kRouterParts * dp,
                                 dp, S, s.T * s.E, te, ts, nt, off, part, a.E, 0, st));
-        int planes = S;
-        if (S > 1) {       // a wide kernel adds the planes (same order), streaming
-            MOE_CUDA(launch_sum_planes(part, S, s.T * s.E, a.E, off + 1, s.T, part, st));
-            planes = 1;
-        }
-        MOE_CUDA(launch_router_from_logits(a, part, planes, st));
+        // the softmax kernel adds the S chain planes in plane order as it reads them
+        MOE_CUDA(launch_router_from_logits(a, part, S, st));
     } else {
         MOE_CUDA(launch_router(a, c->dtype, at<float>(ws, L.rt_logits), st));
     }

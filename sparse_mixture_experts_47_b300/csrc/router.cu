@@ -584,6 +584,26 @@ struct RadixScratch {
     unsigned sel[2];
 };
 
+// A column of at most kStageMaxT values is copied to shared memory `buf`
+// first (one coalesced pass, all threads of the block); the selection passes
+// then read it there.  Longer columns are read in place.
+constexpr int kStageMaxT = 16384;
+__device__ const float *stage_col(const float *col, int T, float *buf) {
+    if (T > kStageMaxT) return col;
+    if ((reinterpret_cast<uintptr_t>(col) & 15) == 0) {
+        const int n4 = T / 4;
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n4; i += blockDim.x)
+            reinterpret_cast<float4 *>(buf)[i] = reinterpret_cast<const float4 *>(col)[i];
+        for (int i = 4 * n4 + threadIdx.x; i < T; i += blockDim.x) buf[i] = col[i];
+    } else {
+        for (int i = threadIdx.x; i < T; i += blockDim.x) buf[i] = col[i];
+    }
+    __syncthreads();
+    return buf;
+}
+inline size_t stage_col_bytes(int T) { return T <= kStageMaxT ? sizeof(float) * T : 0; }
+
 // Value of rank r (0-based, ascending) of col[0..T); 512 threads.  Four
 // passes of 8 bits over the fp32 bit patterns (values >= 0, so bit order is
 // value order).
@@ -641,7 +661,8 @@ __global__ void __launch_bounds__(512) quantile_bias_kernel(const float *probsT,
                                                             float *bias_out) {
     __shared__ RadixScratch sc;
     __shared__ unsigned min_gt;
-    const float *col = probsT + (size_t)blockIdx.x * T;
+    extern __shared__ float colbuf[];
+    const float *col = stage_col(probsT + (size_t)blockIdx.x * T, T, colbuf);
     const float v_lo = radix_select_col(col, T, lo, sc);
     float v_hi = v_lo;
     if (lo + 1 < T) {
@@ -830,7 +851,11 @@ cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int
 cudaError_t launch_quantile_bias(const float *probsT, int T, int E, long long lo, float frac,
                                  float *bias_out, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    quantile_bias_kernel<<<E, 512, 0, st>>>(probsT, T, lo, frac, bias_out);
+    const size_t smem = stage_col_bytes(T);
+    cudaError_t err = cudaFuncSetAttribute(quantile_bias_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    quantile_bias_kernel<<<E, 512, smem, st>>>(probsT, T, lo, frac, bias_out);
     note_launch();
     return cudaGetLastError();
 }
