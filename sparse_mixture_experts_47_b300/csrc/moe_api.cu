@@ -155,9 +155,12 @@ FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long lon
     else if (per <= 64 || (per <= 256 && normal_items < kPlanSMs)) p.nt = 64;
     else {
         // 128-row tiles; halve the MMA N when there are too few output tiles
+        // (down projection: fewer than one round of SMs; at the Switch shape
+        // 288 tiles of N = 256 ran in 65 us against 69 us for 576 of N = 128,
+        // and 66 against 89 us with redirected overflow)
         const long long mt = (rows + 127) / 128 + active;
         if (mt * ((F + up_cols - 1) / up_cols) < 2 * kPlanSMs) p.bn_up = 128;
-        if (mt * ((d + 255) / 256) < 2 * kPlanSMs) p.bn_down = 128;
+        if (mt * ((d + 255) / 256) < kPlanSMs) p.bn_down = 128;
         if (per >= kWideMinRows && F >= kWideMinK && p.bn_down == 256) p.mh_down = 2;
         const double pad128 = (double)((per + 127) / 128 * 128) / per;
         const double pad16 = (double)((per + 15) / 16 * 16) / per;
