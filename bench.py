@@ -240,14 +240,29 @@ def run_reference(args, w, T):
     print(json.dumps(line), flush=True)
 
 
+def source_hash(text):
+    """First 16 hex digits of the SHA-256 of a C++ source without its //
+    comments, trailing blanks and blank lines (code edits change it,
+    comment edits do not)."""
+    lines = []
+    for line in text.splitlines():
+        i = line.find("//")
+        if i >= 0:
+            line = line[:i]
+        line = line.rstrip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def traffic_record(kernel_file):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current source of the kernel."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(path):
         return None
-    with open(os.path.join(ROOT, "sparse_mixture_experts_47_b300", "csrc", kernel_file), "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(os.path.join(ROOT, "sparse_mixture_experts_47_b300", "csrc", kernel_file)) as f:
+        h = source_hash(f.read())
     recs = []
     for line in open(path):
         line = line.strip()

@@ -6,7 +6,7 @@
 // deepseekmodel.com: contiguous per-expert rows make one grouped GEMM over
 // all experts possible):
 //   up   SwiGLU: H = silu(A W1_e^T) * (A W3_e^T)    ReLU: H = relu(A W1_e^T)
-//   down O = H W2_e^T  (fp32 out)
+//   down O = H W2_e^T  (fp32, or bf16 expert outputs in a bf16 layer)
 // A [rows, K] and all weights [E*N, K] are K-major bf16, exactly the
 // nn.Linear layout, so both operands are "K-major" for tcgen05.mma.
 //
@@ -21,7 +21,8 @@
 //              K=16 per instruction, fp32 accumulator in TMEM
 //   warp 2     TMEM allocator (512 columns: two 256-column accumulators)
 //   warps 4-7  epilogue: tcgen05.ld of 32 TMEM lanes each, activation,
-//              bf16 (up) or fp32 (down) stores
+//              bf16 (up) stores; down: bf16, fp32, or fp32 rounded to bf16
+//              values (out_mode), fp32 partial sums for a split
 // Small batches (a few rows per expert) run the same pipeline with the
 // operands swapped (NT > 0): 128 weight rows are the MMA's M side and NT = 16,
 // 32 or 64 token rows its N side, so a tile streams 128 rows of W1 (and W3)
