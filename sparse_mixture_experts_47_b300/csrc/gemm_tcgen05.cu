@@ -55,7 +55,8 @@ constexpr int WROWS = 128;           // weight rows of one TMA box
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 256;        // columns of one of the two accumulators
 constexpr int kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KB)
-constexpr int kSmemExtra = 1024 /* alignment slack */ + 256 /* barriers */;
+constexpr int kSmemExtra =
+    1024 /* alignment slack */ + 256 /* barriers */ + 4096 /* epilogue staging */;
 constexpr int kVarRows = 256;        // NT of the per-tile-width geometry
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 
@@ -274,6 +275,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // swapped epilogue: per epilogue warp a [16 tokens][32 features] bf16 block
+    __nv_bfloat16 *epi_stage =
+        reinterpret_cast<__nv_bfloat16 *>(smem + STAGES * G::STAGE_BYTES + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -432,15 +436,41 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int f = c.n0 + quarter * 32 + lane;
                 const bool vf = f < g.N;
                 const bool raw = MODE == GEMM_DOWN || g.k_splits > 1;
+                // bf16 results leave through shared memory: lane = feature
+                // in, 16-byte vectors of 8 features of one token out
+                const bool bf16_out = MODE == GEMM_DOWN ? g.out_mode == kOutBF16 : !raw;
                 const int ncols = G::VARN ? tile_n16<G::ROWS>(c) : NT;
                 float *P = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
                 __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+                __nv_bfloat16 *stg = epi_stage + quarter * (16 * 32);
 #pragma unroll 1
                 for (int j0 = 0; j0 < ncols; j0 += 16) {
                     float a[16], b[16];
                     tmem_ld16(tbase + j0, a);
                     if (MODE == GEMM_UP_SWIGLU) tmem_ld16(tbase + NT + j0, b);
                     tmem_ld_wait();
+                    if (bf16_out) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float v;
+                            if (MODE == GEMM_DOWN) v = a[i];
+                            else if (MODE == GEMM_UP_SWIGLU) v = silu(a[i]) * b[i];
+                            else v = fmaxf(a[i], 0.f);
+                            stg[i * 32 + lane] = __float2bfloat16_rn(v);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const int vi = lane + 32 * q, i = vi >> 2, part = vi & 3;
+                            const int row = c.m0 + j0 + i;
+                            const int fc = c.n0 + quarter * 32 + 8 * part;
+                            if (row < c.mend && fc < g.N)
+                                *reinterpret_cast<uint4 *>(H + (size_t)row * g.ldc + fc) =
+                                    *reinterpret_cast<const uint4 *>(stg + i * 32 + 8 * part);
+                        }
+                        __syncwarp();
+                        continue;
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int row = c.m0 + j0 + i;
