@@ -301,6 +301,35 @@ def pin_bf16_activation_ffn():
     assert not np.allclose(out["y"], exact["y"], atol=1e-6)   # the rounding is visible
 
 
+def pin_bf16_mixture_rounds_each_expert_output():
+    # k = 2 of E = 3 with a shared expert, bf16 storage: each selected expert's
+    # output and the shared expert's output are bf16 tensors (the Expert
+    # modules of [MoE-ch30] s30.6.1 in a bf16 model), combined with the gate
+    # weights in float64; torch rounds every tensor.
+    inp = _rand_layer(11, 16, 3, 24, "swiglu", Fs=20)
+    out = om.moe_forward(inp, 2, "swiglu", act_dtype="bf16")
+    x = torch.tensor(np.asarray(inp["x"], dtype=np.float64))
+
+    def bf(t):
+        return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+    def expert(w1, w3, w2, rows):
+        t = lambda a: torch.tensor(np.asarray(a, dtype=np.float64))
+        h = bf(Fnn.silu(Fnn.linear(rows, t(w1))) * Fnn.linear(rows, t(w3)))
+        return bf(Fnn.linear(h, t(w2)))
+
+    r = out["router"]
+    ref = np.zeros_like(out["y"])
+    for tok in range(x.shape[0]):
+        for j in range(2):
+            e = int(r.idx[tok, j])
+            o = expert(inp["w1"][e], inp["w3"][e], inp["w2"][e], x[tok:tok + 1])
+            ref[tok] += r.w[tok, j] * o[0].numpy()
+    ref += expert(inp["ws1"], inp["ws3"], inp["ws2"], x).numpy()
+    assert np.allclose(out["y"], ref, atol=1e-12)
+    assert np.allclose(out["y_abs"] >= np.abs(out["y"]) - 1e-12, True)
+
+
 def pin_gate_entropy():
     # closed forms: a uniform router over E experts has entropy ln E, a
     # one-hot router 0; a general distribution against scipy.stats.entropy
@@ -474,6 +503,7 @@ PINS = [pin_top2_example, pin_aux_worked_example, pin_selection_bias_example,
         pin_all_experts_is_dense_mixture, pin_shared_expert_added, pin_capacity_cases,
         pin_capacity_switch_workload, pin_dispatch_invariants, pin_quantile_vs_numpy,
         pin_quantile_balance_share, pin_round_to_bf16, pin_bf16_activation_ffn,
+        pin_bf16_mixture_rounds_each_expert_output,
         pin_gate_entropy, pin_expert_output_scale, pin_observe_drop_and_bias,
         pin_reroute_cases, pin_reroute_invariants, pin_expert_choice_case,
         pin_expert_choice_bruteforce, pin_expert_choice_full_capacity_is_dense_mixture]
