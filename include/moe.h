@@ -174,6 +174,27 @@ int moe_dispatch_reroute(const moe_config *cfg, const int32_t *topk_idx,
  * moe_dispatch_reroute), or -1 on an invalid cfg. */
 int64_t moe_reroute_candidates(const moe_config *cfg);
 
+/* How the tensor-core grouped GEMMs of one expert FFN will run for cfg: a
+ * host-only query (no device work, no GPU needed), chosen from the config
+ * alone.  shared = 0: the routed experts; 1: the shared expert.
+ *   rows_per_tile  up projection: 0 = 128 token rows on the MMA's M side;
+ *                  16/32/64 = weights on the M side and that many token rows
+ *                  on the N side (swap-AB, a few rows per expert)
+ *   up_splits, down_splits  reduction split over CTAs (partial sums added in
+ *                  split order)
+ *   up_n, down_n   MMA N of 128-row tiles (256, or 128 with few tiles)
+ *   down_rows_per_tile  as rows_per_tile for the down projection, or 256:
+ *                  up to 256 rows per tile with the MMA N set per tile
+ *   down_halves    1, or 2: 256-row down tiles of two M = 128 MMAs
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG for an invalid cfg, or
+ * MOE_ERR_UNSUPPORTED when the layer does not run on the tensor cores (fp32,
+ * or no shared expert for shared = 1); out untouched then. */
+typedef struct {
+    int32_t rows_per_tile, up_splits, down_splits, up_n, down_n;
+    int32_t down_rows_per_tile, down_halves;
+} moe_ffn_plan_info;
+int moe_ffn_plan(const moe_config *cfg, int32_t shared, moe_ffn_plan_info *out);
+
 /* Expert-choice routing (cfg->routing = MOE_ROUTING_EXPERT_CHOICE).
  * Sources: deepseekmodel.com TopKRouter discussion (each expert picks the
  * top-C tokens for its capacity, so every expert is exactly full);

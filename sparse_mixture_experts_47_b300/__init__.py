@@ -92,6 +92,7 @@ def _load():
     L.moe_dispatch_reroute.restype = I
     L.moe_reroute_candidates.argtypes = [C]; L.moe_reroute_candidates.restype = ctypes.c_int64
     L.moe_expert_choice_rows.argtypes = [C]; L.moe_expert_choice_rows.restype = ctypes.c_int64
+    L.moe_ffn_plan.argtypes = [C, ctypes.c_int32, ctypes.c_void_p]; L.moe_ffn_plan.restype = I
     L.moe_expert_choice.argtypes = [C] + [P] * 9 + [Z, V]; L.moe_expert_choice.restype = I
     L.moe_combine_rows.argtypes = [C] + [P] * 6 + [V]; L.moe_combine_rows.restype = I
     L.moe_expert_ffn.argtypes = [C] + [P] * 8 + [Z, V]; L.moe_expert_ffn.restype = I
@@ -246,6 +247,21 @@ def dispatch_reroute(cfg: MoEConfig, idx, w, cand_idx, cand_w,
         _stream(dev)))
     return {"counts": counts, "offsets": offsets, "perm": perm[:Tk], "inv": inv[:Tk],
             "slot_expert": se[:T], "slot_w": sw[:T], "n_dropped": nd}
+
+
+class _FfnPlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "rows_per_tile", "up_splits", "down_splits", "up_n", "down_n", "down_rows_per_tile",
+        "down_halves")]
+
+
+def ffn_plan(cfg: MoEConfig, shared: bool = False) -> Dict[str, int]:
+    """The grouped-GEMM geometry the library picks for ``cfg`` (host only):
+    see ``moe_ffn_plan`` in moe.h."""
+    info = _FfnPlanInfo()
+    _check("moe_ffn_plan", lib.moe_ffn_plan(ctypes.byref(cfg.c()), 1 if shared else 0,
+                                             ctypes.byref(info)))
+    return {n: int(getattr(info, n)) for n, _ in _FfnPlanInfo._fields_}
 
 
 def expert_choice_rows(cfg: MoEConfig) -> int:

@@ -654,6 +654,23 @@ int64_t moe_reroute_candidates(const moe_config *cfg) {
     return n_candidates(cfg);
 }
 
+int moe_ffn_plan(const moe_config *cfg, int32_t shared, moe_ffn_plan_info *out) {
+    int rc = check_cfg(cfg);
+    if (rc != MOE_OK) return rc;
+    MOE_REQUIRE(out != nullptr);
+    if (cfg->dtype != MOE_DTYPE_BF16 || (shared && cfg->d_ff_shared <= 0))
+        return MOE_ERR_UNSUPPORTED;
+    const FfnPlan p = shared ? shared_plan(cfg) : routed_plan(cfg);
+    out->rows_per_tile = p.nt;
+    out->up_splits = p.s_up;
+    out->down_splits = p.s_down;
+    out->up_n = p.bn_up;
+    out->down_n = p.bn_down;
+    out->down_rows_per_tile = p.nt_down;
+    out->down_halves = p.nt_down ? 1 : p.mh_down;
+    return MOE_OK;
+}
+
 int64_t moe_expert_choice_rows(const moe_config *cfg) {
     if (check_cfg(cfg) != MOE_OK) return -1;
     return ec_rows_per_expert(cfg);

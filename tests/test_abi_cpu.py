@@ -8,6 +8,7 @@ import subprocess
 
 import pytest
 
+import moe_inputs as mi
 import sparse_mixture_experts_47_b300 as moe
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -91,3 +92,37 @@ def test_strerror():
     for s in (0, -1, -2, -3, -4, -5):
         assert moe.lib.moe_strerror(s)
     assert moe.lib.moe_strerror(-99) == b"unknown status"
+
+
+def _plan(name, T, **sizes):
+    w = mi.workload(name)
+    if sizes:
+        w = w.with_sizes(**sizes)
+    return moe.ffn_plan(moe.config_for(w, T))
+
+
+def test_ffn_plan_geometries():
+    """The GEMM geometry follows the rows per expert (host logic, no GPU):
+    the choices behind the measured results of the bench workloads."""
+    big = _plan("mixtral", 16384)            # 4096 rows per expert, reduction 14336 down
+    assert (big["rows_per_tile"], big["up_n"], big["down_n"]) == (0, 256, 256)
+    assert (big["down_rows_per_tile"], big["down_halves"]) == (0, 2)
+    assert big["up_splits"] == big["down_splits"] == 1
+    one = _plan("mixtral", 1)                # 2 rows: swap-AB, split down projection
+    assert one["rows_per_tile"] == 16 and one["down_rows_per_tile"] == 16
+    assert one["up_splits"] == 1 and one["down_splits"] > 1
+    e896 = _plan("e896", 16384)              # about 146 rows per expert
+    assert (e896["rows_per_tile"], e896["down_rows_per_tile"], e896["down_halves"]) == (0, 256, 1)
+    ds = _plan("deepseek", 8192)             # 256 rows per expert, reduction 2048 down
+    assert (ds["rows_per_tile"], ds["down_rows_per_tile"], ds["down_halves"]) == (0, 0, 1)
+    sw = _plan("switch", 8192)               # 288 down tiles of N = 256: one round of SMs
+    assert (sw["rows_per_tile"], sw["down_n"]) == (0, 256)
+    shared = moe.ffn_plan(moe.config_for(mi.workload("deepseek"), 8192), shared=True)
+    assert shared["rows_per_tile"] == 0 and shared["down_halves"] == 1
+
+
+def test_ffn_plan_rejects_fp32_and_missing_shared_expert():
+    with pytest.raises(moe.MoEError):
+        moe.ffn_plan(moe.config_for(mi.workload("tiny"), 64))             # fp32 layer
+    with pytest.raises(moe.MoEError):
+        moe.ffn_plan(moe.config_for(mi.workload("mixtral"), 64), shared=True)
