@@ -121,6 +121,23 @@ def test_ffn_plan_geometries():
     assert shared["rows_per_tile"] == 0 and shared["down_halves"] == 1
 
 
+@pytest.mark.parametrize("name,T,rows,splits", [
+    ("mixtral", 16, 16, (1, 1)),      # 4 rows per expert
+    ("mixtral", 1, 16, (1, 2)),       # 64 down tiles: the reduction split in two
+    ("switch", 1, 16, (2, 8)),        # one row, one expert: both reductions split
+    ("deepseek", 128, 16, (1, 1)),    # 4 rows per expert over 256 experts
+    ("e896", 4096, 64, (1, 1)),       # 36 rows per expert
+])
+def test_ffn_plan_swapped_tiles_for_few_rows(name, T, rows, splits):
+    """A few rows per expert: weights on the MMA's M side, the token rows on
+    its N side, and the reduction split only while the tiles do not fill the
+    SMs once."""
+    p = _plan(name, T)
+    assert p["rows_per_tile"] == rows and p["down_rows_per_tile"] == rows
+    assert (p["up_splits"], p["down_splits"]) == splits
+    assert p["down_halves"] == 1
+
+
 def test_ffn_plan_rejects_fp32_and_missing_shared_expert():
     with pytest.raises(moe.MoEError):
         moe.ffn_plan(moe.config_for(mi.workload("tiny"), 64))             # fp32 layer
