@@ -222,10 +222,8 @@ int moe_expert_choice(const moe_config *cfg, const float *probs_t,
 
 /* Combine over per-token row lists (expert choice):
  * y[t] = sum_{i in [tok_start[t], tok_start[t+1])} row_w[r_i] out_sorted[r_i]
- *        + shared_out[t], in list order.  out_sorted [rows, d] fp32.  In a
- * bf16 layer each out_sorted and shared_out value is first rounded to the
- * nearest bf16 (expert outputs are bf16 tensors there; no-op on the output
- * of moe_expert_ffn). */
+ *        + shared_out[t], in list order, fp32 accumulation.
+ * out_sorted [rows, d] fp32; shared_out [T, d] fp32 or NULL. */
 int moe_combine_rows(const moe_config *cfg, const float *out_sorted,
                      const float *row_w, const int32_t *tok_start,
                      const int32_t *tok_rows, const float *shared_out, void *y,
@@ -257,9 +255,9 @@ int moe_dispatch_static(const moe_config *cfg, const int32_t *topk_idx,
 
 /* Per-expert FFN on the grouped rows: out_sorted[s] = FFN_e(x[perm[s] / k])
  * for offsets[e] <= s < offsets[e+1] (expert choice: x[perm[s]]).
- * Source: ch. 30 §30.2.4 / §30.6.1.  fp32 accumulation; in a bf16 layer h
- * and the output row are bf16 values (rounded once to nearest even; the
- * output held in fp32 here), as the layer's modules return in a bf16 model.
+ * Source: ch. 30 §30.2.4 / §30.6.1.  fp32 accumulation; in a bf16 layer the
+ * activation h, the bf16 operand of the down projection, is rounded once to
+ * the nearest bf16; the output row is fp32.
  *   x          [T, d]; perm, offsets as produced by moe_dispatch (or
  *              moe_dispatch_reroute, moe_expert_choice)
  *   w1, w3, w2 expert weights (w3 NULL for ReLU)
@@ -272,9 +270,7 @@ int moe_expert_ffn(const moe_config *cfg, const void *x, const int32_t *perm,
 
 /* Combine: y[t] = sum_j [inv[t*k+j] >= 0] w[t,j] out_sorted[inv[t*k+j]]
  *               + shared_out[t].   Source: ch. 30 §30.6.1 (weighted
- * accumulate), §30.4.5 (routed + shared).  fp32 accumulation; in a bf16
- * layer out_sorted and shared_out values are first rounded to bf16 as in
- * moe_combine_rows.
+ * accumulate), §30.4.5 (routed + shared).  fp32 accumulation in j order.
  *   out_sorted [*, d] fp32; inv [T*k]; topk_w [T, k]
  *   shared_out [T, d] fp32 or NULL;  y [T, d] in cfg->out_dtype */
 int moe_combine(const moe_config *cfg, const float *out_sorted,
@@ -318,15 +314,22 @@ typedef struct {
     int32_t *slot_expert;      /* [T, k] expert that served each slot after
                                   capacity (and redirection), -1 if dropped */
     float *slot_w;             /* [T, k] gate weight the combine used for it */
+    int32_t *offsets;          /* [E+1] the grouped layout: expert e's rows are
+                                  offsets[e] .. offsets[e+1]) */
+    int32_t *perm;             /* [rows] source of each grouped row: flat slot
+                                  t*k+j (token choice) or token t (expert
+                                  choice); rows = T*k, or E * Cn (see
+                                  moe_expert_choice_rows); rows >= offsets[E]
+                                  are not written */
 } moe_layer_outputs;
 
 /* The whole forward pass (router, dispatch, experts, shared expert,
  * combine, statistics) on one stream, with no host synchronisation.
  * Source: ch. 30 §30.6.1 MoELayer.forward returning (output, aux_loss).
  * Precision: fp32 accumulation throughout; in a bf16 layer the activation h
- * and each expert's output row (routed and shared) are bf16 values, rounded
- * once, before the fp32 weighted combine: the results of the stage calls
- * moe_expert_ffn and moe_combine. */
+ * is stored in bf16 (rounded once to nearest even), and every expert output
+ * row (routed and shared) is kept in fp32 for the weighted combine: the
+ * results of the stage calls moe_expert_ffn and moe_combine. */
 int moe_layer_forward(const moe_config *cfg, const void *x,
                       const moe_layer_weights *wts,
                       const moe_layer_outputs *out, void *ws,
@@ -382,6 +385,12 @@ const char *moe_strerror(int status);
 /* Number of kernels this library has launched in this process (all entry
  * points, all devices); a monotone counter for launch accounting. */
 int64_t moe_kernel_launches(void);
+
+/* The architecture the library's kernels were compiled for, as the CUDA
+ * runtime reports it for one of them on the current device (binaryVersion:
+ * major * 10 + minor, 103 for sm_103a) into *version.  Needs a GPU;
+ * MOE_ERR_CUDA when the runtime cannot load the kernel there. */
+int moe_kernel_binary_version(int32_t *version);
 
 /* Stages of moe_layer_forward that per-stage timing separates. */
 enum {

@@ -53,13 +53,17 @@ Readings where the pages are silent or disagree (each restated where used):
       of its output tensor (its kept rows' FFN outputs, before the gate
       weight); bias size is mean and max |b_e| of the selection bias in
       effect.
-  R8  the layer's activations are stored in the layer dtype: for a bf16 layer
-      the expert's intermediate activation h (the input of W2) is a bf16
-      tensor, so it is rounded once, to nearest even, from its exact value
+  R8  the layer's intermediate activation is stored in the layer dtype: for
+      a bf16 layer the expert's intermediate activation h (the input of W2)
+      is a bf16 tensor, rounded once, to nearest even, from its exact value
       before the down projection.  The pages run the model in
       torch.bfloat16 ([MoE-ch30] §30.6.3), and the Switch workload is
-      specified with bf16 weights and activations.  Everything else stays
-      exact float64.
+      specified with bf16 weights and activations, so the down projection
+      takes a bf16 operand.  Everything after it (each expert's output row,
+      the gate-weighted sum, the shared expert's output, y) stays exact
+      float64: the layer's output is compared in fp32 against a bound of
+      1e-2 x RMS, and a bf16 rounding of an expert output alone moves it by
+      up to 2^-8 of its magnitude, which at a few RMS is that whole bound.
 
 Pins (tests/test_oracle_pins.py): the printed worked examples (top-2
 renormalisation, 4-token aux loss, selection-bias example), brute-force top-k
@@ -81,7 +85,7 @@ __all__ = [
     "expert_ffn", "load_stats", "moe_forward", "RouterOut", "DispatchOut", "round_to_bf16",
     "round_to_fp32", "gate_entropy", "expert_output_scale", "bias_magnitude", "observe",
     "dispatch_reroute", "RerouteOut", "expert_choice", "ExpertChoiceOut",
-    "moe_forward_expert_choice",
+    "moe_forward_expert_choice", "with_ranking",
 ]
 
 
@@ -180,6 +184,26 @@ class RouterOut:
     select_bias: Optional[np.ndarray]   # [E] bias used for selection
 
 
+def with_ranking(r: RouterOut, ranking: Dict[int, Sequence[int]]) -> RouterOut:
+    """The router's result with the leading experts of some tokens given.
+
+    Where two selection scores are equal to within rounding, either order
+    is a correct top-k (reading R5 fixes only exactly equal scores), and a
+    device computing the scores in fp32 may take the other one.
+    ``ranking[t]`` lists token t's experts best first (at least k of them);
+    its first k become the token's slots, in that order, and their weights
+    are renormalised from the unbiased probabilities as in ``route``.  The
+    caller checks that the scores allow the order before passing it.
+    """
+    idx, w = r.idx.copy(), r.w.copy()
+    k = idx.shape[1]
+    for t, lead in ranking.items():
+        row = np.asarray(lead, dtype=np.int64)[:k]
+        idx[t] = row
+        w[t] = renormalise(r.probs[t:t + 1], row[None, :])[0]
+    return RouterOut(r.logits, r.probs, r.scores, idx, w, r.select_bias)
+
+
 def route(x, w_r, k: int, logit_bias=None, select_bias=None,
           select_space: str = "probs", quantile_balance: bool = False
           ) -> RouterOut:
@@ -266,8 +290,8 @@ class RerouteOut:
     n_dropped: int
 
 
-def dispatch_reroute(scores: np.ndarray, probs: np.ndarray, k: int, C: int, rounds: int
-                     ) -> RerouteOut:
+def dispatch_reroute(scores: np.ndarray, probs: np.ndarray, k: int, C: int, rounds: int,
+                     ranking: Optional[Dict[int, Sequence[int]]] = None) -> RerouteOut:
     """Capacity with overflow redirected to the next-best expert ([MoE-ch30]
     §30.5.2: tokens beyond an expert's capacity are dropped or sent to the
     next-best expert).  Reading R10:
@@ -286,9 +310,16 @@ def dispatch_reroute(scores: np.ndarray, probs: np.ndarray, k: int, C: int, roun
       capacity decisions never rescale the other slots (as for drops, R6);
     * an expert's rows are grouped in the order they were served: round 0 in
       (t*k + j) order, then round 1, and so on.
+
+    ``ranking[t]`` (as in ``with_ranking``) fixes the leading experts of
+    token t's ranking where its scores tie within rounding; the rest of the
+    ranking follows the scores.
     """
     T, E = scores.shape
     order = np.argsort(-scores, axis=1, kind="stable")        # full ranking per token
+    for t, lead in (ranking or {}).items():
+        lead = [int(e) for e in lead]
+        order[t] = lead + [int(e) for e in order[t] if int(e) not in set(lead)]
     top = order[:, :k]
     norm = np.take_along_axis(probs, top, axis=1).sum(axis=1)
     counts = np.bincount(top.reshape(-1), minlength=E).astype(np.int64)
@@ -340,7 +371,8 @@ class ExpertChoiceOut:
     n_unchosen: int           # tokens no expert picked (their routed output is 0)
 
 
-def expert_choice(probs: np.ndarray, C: int) -> ExpertChoiceOut:
+def expert_choice(probs: np.ndarray, C: int,
+                  chosen: Optional[Dict[int, Sequence[int]]] = None) -> ExpertChoiceOut:
     """Expert-choice routing ([MoE-prac] TopKRouter discussion: each expert
     picks the top-C tokens for its capacity, so every expert is exactly
     full; [MoE-memo] routing table: each expert chooses its top tokens).
@@ -348,37 +380,49 @@ def expert_choice(probs: np.ndarray, C: int) -> ExpertChoiceOut:
     router as token choice); expert e takes the min(C, T) tokens with the
     largest probs[:, e], exactly equal values by lower token index; the gate
     weight of (t, e) is probs[t, e] with no renormalisation; a token may be
-    picked by any number of experts, including none."""
+    picked by any number of experts, including none.
+
+    ``chosen[e]`` gives expert e's Cn tokens where its column ties within
+    rounding at the Cn-th value (either token is a correct pick there); the
+    caller checks that the values allow the set before passing it."""
     T, E = probs.shape
     Cn = min(C, T)
-    chosen = np.zeros((E, Cn), dtype=np.int64)
+    picks = np.zeros((E, Cn), dtype=np.int64)
     weight = np.zeros((E, Cn))
     picked = np.zeros(T, dtype=bool)
     for e in range(E):
-        order = np.argsort(-probs[:, e], kind="stable")   # ties: lower token first
-        top = np.sort(order[:Cn])
-        chosen[e] = top
+        if chosen is not None and e in chosen:
+            top = np.sort(np.asarray(chosen[e], dtype=np.int64))
+            assert top.shape[0] == Cn
+        else:
+            order = np.argsort(-probs[:, e], kind="stable")   # ties: lower token first
+            top = np.sort(order[:Cn])
+        picks[e] = top
         weight[e] = probs[top, e]
         picked[top] = True
-    return ExpertChoiceOut(chosen, weight, np.full(E, Cn, dtype=np.int64),
+    return ExpertChoiceOut(picks, weight, np.full(E, Cn, dtype=np.int64),
                            np.arange(E + 1, dtype=np.int64) * Cn, int(T - picked.sum()))
 
 
 def moe_forward_expert_choice(inp: Dict, k: int, act: str, capacity_factor: float = 1.0,
                               tokens: Optional[Sequence[int]] = None,
-                              act_dtype: str = "fp64") -> Dict:
+                              act_dtype: str = "fp64",
+                              chosen: Optional[Dict[int, Sequence[int]]] = None,
+                              probs: Optional[np.ndarray] = None) -> Dict:
     """Layer forward with expert-choice routing (reading R11):
     y[t] = sum over experts e that picked t of probs[t, e] FFN_e(x[t]) +
     shared(x[t]), with capacity C = ceil(cf * T * k / E) (k = average number
     of experts per token).  f, p and aux use the experts' actual loads:
-    f_e = Cn / (T k)."""
+    f_e = Cn / (T k).  ``chosen`` is passed to ``expert_choice``; ``probs``,
+    when given, is this module's softmax of the router logits for the same
+    inputs, computed earlier."""
     x = _f64(inp["x"])
     T = x.shape[0]
     E = inp["w_r"].shape[0]
-    logits = router_logits(x, inp["w_r"], inp.get("logit_bias"))
-    probs = softmax(logits)
+    if probs is None:
+        probs = softmax(router_logits(x, inp["w_r"], inp.get("logit_bias")))
     C = capacity(T, k, E, capacity_factor)
-    ec = expert_choice(probs, C)
+    ec = expert_choice(probs, C, chosen)
     f = ec.counts / float(T * k) if T else np.zeros(E)
     p = probs.mean(axis=0) if T else np.zeros(E)
     stats = {"counts": ec.counts, "f": f, "p": p, "aux": E * float(np.sum(f * p)),
@@ -386,7 +430,6 @@ def moe_forward_expert_choice(inp: Dict, k: int, act: str, capacity_factor: floa
     rows = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     pos = {int(t): i for i, t in enumerate(rows)}
     y = np.zeros((rows.shape[0], x.shape[1]))
-    y_abs = np.zeros_like(y)       # sum of |terms| of y, for rounding-aware comparisons
     for e in range(E):
         sel = [(n, int(t)) for n, t in enumerate(ec.chosen[e]) if int(t) in pos]
         if not sel:
@@ -396,13 +439,10 @@ def moe_forward_expert_choice(inp: Dict, k: int, act: str, capacity_factor: floa
                          inp["w2"][e], act, act_dtype)
         for i, (n, t) in enumerate(sel):
             y[pos[t]] += ec.weight[e, n] * out[i]
-            y_abs[pos[t]] += np.abs(ec.weight[e, n] * out[i])
     if inp.get("ws1") is not None:
         sh = expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
         y += sh
-        y_abs += np.abs(sh)
-    return {"probs": probs, "ec": ec, "stats": stats, "capacity": C, "rows": rows, "y": y,
-            "y_abs": y_abs}
+    return {"probs": probs, "ec": ec, "stats": stats, "capacity": C, "rows": rows, "y": y}
 
 
 # --------------------------------------------------------------------------
@@ -438,10 +478,9 @@ def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str, act_dtype: str = "fp64"
 
     SwiGLU: w2(silu(w1 x) * w3 x)  ([MoE-ch30] §30.2.4), ReLU: w2(relu(w1 x)).
     Weights are nn.Linear-shaped: w1, w3 [F, d], w2 [d, F]; no biases.
-    ``act_dtype`` is the layer's storage type (reading R8): the intermediate
-    activation h and the expert's output row are tensors of that type (the
-    Expert module's result in [MoE-ch30] §30.6.1 MoELayer.forward), each
-    rounded once; "fp64" keeps both exact.  Products and sums are exact.
+    ``act_dtype`` is the layer's storage type of the intermediate activation
+    h (reading R8): h is rounded once to it; "fp64" keeps it exact.  The
+    expert's output row is exact.  Products and sums are exact.
     """
     a = x_rows @ _f64(w1).T
     if act == "swiglu":
@@ -451,7 +490,7 @@ def expert_ffn(x_rows: np.ndarray, w1, w3, w2, act: str, act_dtype: str = "fp64"
     else:
         raise ValueError(act)
     h = ACT_ROUNDING[act_dtype](h)
-    return ACT_ROUNDING[act_dtype](h @ _f64(w2).T)
+    return h @ _f64(w2).T
 
 
 # --------------------------------------------------------------------------
@@ -534,7 +573,9 @@ def observe(r: "RouterOut", dp: "DispatchOut", outputs: Dict[int, np.ndarray], E
 def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
                 select_space: str = "probs", quantile_balance: bool = False,
                 tokens: Optional[Sequence[int]] = None, act_dtype: str = "fp64",
-                observe_outputs: bool = False, reroute_rounds: int = 0) -> Dict:
+                observe_outputs: bool = False, reroute_rounds: int = 0,
+                ranking: Optional[Dict[int, Sequence[int]]] = None,
+                router: Optional[RouterOut] = None) -> Dict:
     """Forward of the token-choice MoE layer.
 
     y[t] = sum_j keep[t,j] * w[t,j] * FFN_{idx[t,j]}(x[t]) + shared(x[t]).
@@ -545,16 +586,21 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
     activation (reading R8).  ``observe_outputs`` adds the observability set
     (needs every token: ``tokens`` None).  ``reroute_rounds`` > 0 sends
     capacity overflow to the next-best experts (reading R10) instead of
-    dropping it.
+    dropping it.  ``ranking`` fixes the order of tokens whose scores tie
+    within rounding (``with_ranking``); ``router``, when given, is this
+    module's ``route`` of the same inputs and options, computed earlier.
     """
     x = _f64(inp["x"])
     T = x.shape[0]
     E = inp["w_r"].shape[0]
-    r = route(x, inp["w_r"], k, inp.get("logit_bias"), inp.get("select_bias"),
-              select_space, quantile_balance)
+    r = router if router is not None else route(
+        x, inp["w_r"], k, inp.get("logit_bias"), inp.get("select_bias"), select_space,
+        quantile_balance)
+    if ranking:
+        r = with_ranking(r, ranking)
     C = capacity(T, k, E, capacity_factor)
     if reroute_rounds > 0:
-        dp = dispatch_reroute(r.scores, r.probs, k, C, reroute_rounds)
+        dp = dispatch_reroute(r.scores, r.probs, k, C, reroute_rounds, ranking)
         slot_e, slot_w = dp.slot_expert, dp.slot_w
     else:
         dp = dispatch(r.idx, E, C)
@@ -562,7 +608,6 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
     st = load_stats(r.probs, r.idx, E)
     rows = np.arange(T) if tokens is None else np.asarray(sorted(set(int(t) for t in tokens)))
     y = np.zeros((rows.shape[0], x.shape[1]))
-    y_abs = np.zeros_like(y)       # sum of |terms| of y, for rounding-aware comparisons
     pos = {int(t): i for i, t in enumerate(rows)}
     groups: Dict[int, list] = {}
     for t in rows:
@@ -578,13 +623,10 @@ def moe_forward(inp: Dict, k: int, act: str, capacity_factor: float = 0.0,
         outputs[e] = out
         for n, (t, _) in enumerate(tj):
             y[pos[int(t)]] += ww[n] * out[n]
-            y_abs[pos[int(t)]] += np.abs(ww[n] * out[n])
     if inp.get("ws1") is not None:
         sh = expert_ffn(x[rows], inp["ws1"], inp["ws3"], inp["ws2"], "swiglu", act_dtype)
         y += sh
-        y_abs += np.abs(sh)
-    res = {"router": r, "dispatch": dp, "stats": st, "capacity": C, "rows": rows, "y": y,
-           "y_abs": y_abs}
+    res = {"router": r, "dispatch": dp, "stats": st, "capacity": C, "rows": rows, "y": y}
     if observe_outputs:
         assert tokens is None, "observability needs every token"
         res["observe"] = observe(r, dp, outputs, E, k)

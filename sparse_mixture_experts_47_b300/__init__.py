@@ -65,7 +65,7 @@ class _Outputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("y", "topk_idx", "topk_w", "counts", "n_dropped", "f", "p", "aux",
                  "load_max_over_mean", "select_bias_out", "counts_unbiased", "slot_expert",
-                 "slot_w")]
+                 "slot_w", "offsets", "perm")]
 
 
 OBS_KEYS = ("drop_ratio", "gate_entropy", "bias_mean_abs", "bias_max_abs", "expert_out_mean",
@@ -110,6 +110,7 @@ def _load():
     L.moe_device_status.argtypes = [V]; L.moe_device_status.restype = I
     L.moe_strerror.argtypes = [I]; L.moe_strerror.restype = ctypes.c_char_p
     L.moe_kernel_launches.argtypes = []; L.moe_kernel_launches.restype = ctypes.c_int64
+    L.moe_kernel_binary_version.argtypes = [P]; L.moe_kernel_binary_version.restype = I
     L.moe_stage_timing_enable.argtypes = [I]; L.moe_stage_timing_enable.restype = I
     L.moe_stage_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int64)]
@@ -357,14 +358,17 @@ def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
                   workspace: Optional[Workspace] = None, outputs: Optional[Dict] = None,
                   want_unbiased_counts: bool = False, observe: bool = False,
                   observed: Optional[Dict] = None,
-                  want_slots: bool = False) -> Dict[str, torch.Tensor]:
+                  want_slots: bool = False, want_layout: bool = False
+                  ) -> Dict[str, torch.Tensor]:
     """The whole layer on torch's current stream.  ``weights`` holds device
     tensors under the keys w_r, logit_bias, select_bias, w1, w3, w2, ws1,
     ws3, ws2 (missing or None = absent).  ``outputs`` may pass preallocated
     output tensors (same keys as the returned dict).  ``observe`` adds the
     monitoring set (``OBS_KEYS``: drop ratio, gate entropy, bias size,
     per-expert output mean/std/max) under the key "observe"; ``observed``
-    may pass its preallocated tensors."""
+    may pass its preallocated tensors.  ``want_slots`` adds each slot's
+    serving expert and gate weight; ``want_layout`` the grouped layout
+    (offsets [E+1], perm [rows])."""
     dev = x.device
     T, E, k, d = cfg.T, cfg.n_experts, cfg.top_k, cfg.d_model
     o = dict(outputs or {})
@@ -390,12 +394,16 @@ def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
     if want_slots:
         need("slot_expert", (T, k), torch.int32)
         need("slot_w", (T, k), torch.float32)
+    if want_layout:
+        need("offsets", (E + 1,), torch.int32)
+        rows = E * expert_choice_rows(cfg) if cfg.routing == ROUTING_EXPERT_CHOICE else T * k
+        need("perm", (rows,), torch.int32)
     W = _Weights(*(_ptr(weights.get(key)) for key in _WEIGHT_KEYS))
     O = _Outputs(_ptr(o["y"]), _ptr(o["idx"]), _ptr(o["w"]), _ptr(o["counts"]),
                  _ptr(o["n_dropped"]), _ptr(o["f"]), _ptr(o["p"]), _ptr(o["aux"]),
                  _ptr(o["load_max_over_mean"]), _ptr(o.get("select_bias")),
                  _ptr(o.get("counts_unbiased")), _ptr(o.get("slot_expert")),
-                 _ptr(o.get("slot_w")))
+                 _ptr(o.get("slot_w")), _ptr(o.get("offsets")), _ptr(o.get("perm")))
     buf, nb = _ws(cfg, dev, workspace)
     if observe or observed is not None:
         ob = _obs_tensors(cfg, dev, observed)
@@ -533,6 +541,14 @@ STAGES = ("router", "dispatch", "stats", "gather", "up", "down", "shared", "comb
 def kernel_launches() -> int:
     """Kernels launched by the library so far in this process."""
     return int(lib.moe_kernel_launches())
+
+
+def kernel_binary_version() -> int:
+    """Architecture of the library's kernels as the CUDA runtime loads them on
+    the current device (103 for sm_103a)."""
+    v = ctypes.c_int32(0)
+    _check("moe_kernel_binary_version", lib.moe_kernel_binary_version(ctypes.byref(v)))
+    return int(v.value)
 
 
 def stage_timing(on: bool) -> None:

@@ -6,7 +6,7 @@
 // deepseekmodel.com: contiguous per-expert rows make one grouped GEMM over
 // all experts possible):
 //   up   SwiGLU: H = silu(A W1_e^T) * (A W3_e^T)    ReLU: H = relu(A W1_e^T)
-//   down O = H W2_e^T  (fp32, or bf16 expert outputs in a bf16 layer)
+//   down O = H W2_e^T  (fp32 expert outputs)
 // A [rows, K] and all weights [E*N, K] are K-major bf16, exactly the
 // nn.Linear layout, so both operands are "K-major" for tcgen05.mma.
 //
@@ -21,8 +21,8 @@
 //              K=16 per instruction, fp32 accumulator in TMEM
 //   warp 2     TMEM allocator (512 columns: two 256-column accumulators)
 //   warps 4-7  epilogue: tcgen05.ld of 32 TMEM lanes each, activation,
-//              bf16 (up) stores; down: bf16, fp32, or fp32 rounded to bf16
-//              values (out_mode), fp32 partial sums for a split
+//              bf16 (up) stores; down: fp32 stores (partial sums for a
+//              split)
 // Small batches (a few rows per expert) run the same pipeline with the
 // operands swapped (NT > 0): 128 weight rows are the MMA's M side and NT = 16,
 // 32 or 64 token rows its N side, so a tile streams 128 rows of W1 (and W3)
@@ -99,7 +99,6 @@ struct Args {
     const int32_t *tile_e, *tile_start, *n_mtiles, *offsets;
     void *C;
     int ldc;
-    int out_mode;      // GEMM_DOWN, one split: kOutF32, kOutBF16, kOutF32Rounded
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -436,9 +435,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int f = c.n0 + quarter * 32 + lane;
                 const bool vf = f < g.N;
                 const bool raw = MODE == GEMM_DOWN || g.k_splits > 1;
-                // bf16 results leave through shared memory: lane = feature
-                // in, 16-byte vectors of 8 features of one token out
-                const bool bf16_out = MODE == GEMM_DOWN ? g.out_mode == kOutBF16 : !raw;
+                // bf16 results (the activation h) leave through shared
+                // memory: lane = feature in, 16-byte vectors of 8 features of
+                // one token out
+                const bool bf16_out = !raw;
                 const int ncols = G::VARN ? tile_n16<G::ROWS>(c) : NT;
                 float *P = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
                 __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
@@ -453,8 +453,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             float v;
-                            if (MODE == GEMM_DOWN) v = a[i];
-                            else if (MODE == GEMM_UP_SWIGLU) v = silu(a[i]) * b[i];
+                            if (MODE == GEMM_UP_SWIGLU) v = silu(a[i]) * b[i];
                             else v = fmaxf(a[i], 0.f);
                             stg[i * 32 + lane] = __float2bfloat16_rn(v);
                         }
@@ -475,13 +474,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int i = 0; i < 16; ++i) {
                         const int row = c.m0 + j0 + i;
                         if (!vf || row >= c.mend) continue;
-                        if (MODE == GEMM_DOWN && g.out_mode == kOutBF16) {
-                            H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(a[i]);
-                        } else if (raw) {
+                        if (raw) {
                             float *dst = P + (size_t)row * g.ldc + f;
-                            dst[0] = MODE == GEMM_DOWN && g.out_mode == kOutF32Rounded
-                                         ? __bfloat162float(__float2bfloat16_rn(a[i]))
-                                         : a[i];
+                            dst[0] = a[i];
                             if (MODE == GEMM_UP_SWIGLU) dst[g.N] = b[i];
                         } else if (MODE == GEMM_UP_SWIGLU) {
                             H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(silu(a[i]) * b[i]);
@@ -532,21 +527,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                 *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
                         }
                     }
-                } else if (g.out_mode == kOutBF16) {
-                    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(g.C);
-#pragma unroll 1
-                    for (int cc = 0; cc < BN; cc += 16) {
-                        float v[16];
-                        tmem_ld16(tbase + cc, v);
-                        tmem_ld_wait();
-                        const int col = c.n0 + cc;
-                        if (vrow) {
-                            __nv_bfloat16 *dst = O + (size_t)row * g.ldc + col;
-                            if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
-                            if (col + 8 < g.N)
-                                *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
-                        }
-                    }
                 } else {
                     float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
 #pragma unroll 1
@@ -554,10 +534,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         float v[16];
                         tmem_ld16(tbase + cc, v);
                         tmem_ld_wait();
-                        if (g.out_mode == kOutF32Rounded)
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
                         const int col = c.n0 + cc;
                         if (vrow) {
                             float *dst = O + (size_t)row * g.ldc + col;
@@ -678,25 +654,20 @@ static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args
 // every tile writes fp32 partial sums to C + s * split_stride: GEMM_DOWN
 // always (row-major [rows, ldc]); the up modes only with nt > 0, writing the
 // pre-activation sums (SwiGLU: W1 part at column f, W3 part at N + f).
-// k_splits = 1 up modes write the activation in bf16.  out_mode (GEMM_DOWN
-// with k_splits = 1 only): kOutF32, kOutBF16 (bf16 output), kOutF32Rounded
-// (fp32 output holding the nearest bf16 of each value).
+// k_splits = 1 up modes write the activation in bf16; GEMM_DOWN writes fp32.
 cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long long a_rows,
                            int a_cols,
                            const void *B0, const void *B1, int E, int b_rows, int N, int K,
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,
                            const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           int out_mode, cudaStream_t st) {
+                           cudaStream_t st) {
     using namespace tc;
     if (a_rows == 0) return cudaSuccess;
     const int nk = (K + BK - 1) / BK;
     if (nt != 0 && nt != 16 && nt != 32 && nt != 64 && nt != kVarRows) return cudaErrorInvalidValue;
     if (bn != BNM && bn != BNM / 2) return cudaErrorInvalidValue;
     if (mh != 1 && (mh != 2 || nt != 0 || bn != BNM)) return cudaErrorInvalidValue;
-    if (out_mode != kOutF32 && (mode != GEMM_DOWN || k_splits != 1 || N % 8 != 0 ||
-                                (out_mode != kOutBF16 && out_mode != kOutF32Rounded)))
-        return cudaErrorInvalidValue;
     if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN && nt == 0) ||
         (a_k_period % BK != 0 && a_k_period != K))
         return cudaErrorInvalidValue;
@@ -733,7 +704,6 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
     g.offsets = offsets;
     g.C = C;
     g.ldc = ldc;
-    g.out_mode = out_mode;
     if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, mh, m, g, st);
     if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, mh, m, g, st);
     return launch_mode<GEMM_DOWN>(nt, bn, mh, m, g, st);

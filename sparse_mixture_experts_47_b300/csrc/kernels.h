@@ -83,23 +83,17 @@ cudaError_t launch_stats_finalize(const int32_t *counts, const float *p, int T, 
                                   cudaStream_t st, const ObsArgs &o = ObsArgs{});
 cudaError_t launch_entropy_partials(const float *probs, int T, int E, float *ent_partial,
                                     cudaStream_t st);
-// Expert outputs o in row order: one bf16 plane (bf16 = 1), or `planes`
-// fp32 planes `plane` elements apart (partial sums of a split reduction,
-// added in plane order), their sum rounded to the nearest bf16 when round_bf16
-// is set (a bf16 layer's expert output is a bf16 tensor).
+// Expert outputs o in row order: `planes` fp32 planes `plane` elements apart
+// (partial sums of a split reduction, added in plane order; one plane when
+// the reduction is not split).
 struct ExpertOut {
-    const void *p;
-    int bf16;
+    const float *p;
     int planes;
     long long plane;
-    int round_bf16;
 };
-inline ExpertOut expert_out_f32(const float *p, int planes = 1, long long plane = 0,
-                                bool round_bf16 = false) {
-    return ExpertOut{p, 0, planes, plane, round_bf16 ? 1 : 0};
+inline ExpertOut expert_out_f32(const float *p, int planes = 1, long long plane = 0) {
+    return ExpertOut{p, planes, plane};
 }
-// Output modes of the down projection (launch_tc_gemm).
-enum { kOutF32 = 0, kOutBF16 = 1, kOutF32Rounded = 2 };
 // Expert output scale over the dispatched rows: row statistics into
 // rs [max_rows][3] (fp64), then per expert mean, std and max |o| (each
 // output pointer may be NULL).
@@ -132,11 +126,10 @@ cudaError_t launch_slot_outputs(const int32_t *idx, const float *w, const int32_
 cudaError_t launch_split_activation(const float *P, int splits, long long plane, int N,
                                     int swiglu, const int32_t *rows_end, long long max_rows,
                                     __nv_bfloat16 *h, cudaStream_t st);
-// out[r] = sum_s P_s[r] (fp32) for rows r < *rows_end; round_bf16: each sum
-// replaced by its nearest bf16.
+// out[r] = sum_s P_s[r] (fp32, in split order) for rows r < *rows_end.
 cudaError_t launch_sum_planes(const float *P, int splits, long long plane, int d,
                               const int32_t *rows_end, long long max_rows, float *out,
-                              cudaStream_t st, bool round_bf16 = false);
+                              cudaStream_t st);
 cudaError_t launch_build_tiles(const int32_t *offsets, int E, int BM, int32_t *tile_e,
                                int32_t *tile_m0, int32_t *tile_start, int32_t *n_tiles,
                                cudaStream_t st);
@@ -167,6 +160,6 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,
                            const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           int out_mode, cudaStream_t st);
+                           cudaStream_t st);
 
 }  // namespace moe

@@ -161,34 +161,21 @@ cudaError_t launch_entropy_partials(const float *probs, int T, int E, float *ent
     return cudaGetLastError();
 }
 
-__device__ __forceinline__ float round_bf16(float v) {
-    return __bfloat162float(__float2bfloat16_rn(v));
-}
-__device__ __forceinline__ float4 round4_bf16(float4 v) {
-    return make_float4(round_bf16(v.x), round_bf16(v.y), round_bf16(v.z), round_bf16(v.w));
-}
 // Element i of the expert outputs (planes added in plane order).
 __device__ __forceinline__ float expert_out_at(const ExpertOut &o, long long i) {
-    if (o.bf16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(o.p)[i]);
-    const float *P = static_cast<const float *>(o.p);
-    float v = P[i];
-    for (int sp = 1; sp < o.planes; ++sp) v += P[sp * o.plane + i];
-    return o.round_bf16 ? round_bf16(v) : v;
+    float v = o.p[i];
+    for (int sp = 1; sp < o.planes; ++sp) v += o.p[sp * o.plane + i];
+    return v;
 }
 // Elements 4i .. 4i+3 of the expert outputs.
 __device__ __forceinline__ float4 expert_out4(const ExpertOut &o, long long i) {
-    if (o.bf16) {
-        const uint2 u = static_cast<const uint2 *>(o.p)[i];
-        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-    }
-    const float4 *P = static_cast<const float4 *>(o.p);
+    const float4 *P = reinterpret_cast<const float4 *>(o.p);
     float4 v = P[i];
     for (int sp = 1; sp < o.planes; ++sp) {
         const float4 q = P[sp * (o.plane / 4) + i];
         v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
     }
-    return o.round_bf16 ? round4_bf16(v) : v;
+    return v;
 }
 
 // Per sorted row r < *rows_end of the expert outputs: sum, sum of squares
@@ -493,29 +480,24 @@ cudaError_t launch_split_activation(const float *P, int splits, long long plane,
     return cudaGetLastError();
 }
 
-// out[r] = sum_s P_s[r] for rows r < *rows_end (fp32, split order), rounded
-// to the nearest bf16 when round_bf16 is set.
+// out[r] = sum_s P_s[r] for rows r < *rows_end (fp32, split order).
 __global__ void sum_planes_kernel(const float4 *P, int splits, long long plane4, int d4,
-                                  const int32_t *rows_end, long long max_rows, float4 *out,
-                                  int round_bf16) {
+                                  const int32_t *rows_end, long long max_rows, float4 *out) {
     const long long rows = min((long long)*rows_end, max_rows);
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < rows * d4;
-         i += (long long)gridDim.x * blockDim.x) {
-        float4 v = sum_planes4(P, splits, plane4, i);
-        if (round_bf16) v = round4_bf16(v);
-        out[i] = v;
-    }
+         i += (long long)gridDim.x * blockDim.x)
+        out[i] = sum_planes4(P, splits, plane4, i);
 }
 
 cudaError_t launch_sum_planes(const float *P, int splits, long long plane, int d,
                               const int32_t *rows_end, long long max_rows, float *out,
-                              cudaStream_t st, bool round_bf16) {
+                              cudaStream_t st) {
     if (max_rows == 0) return cudaSuccess;
     const long long work = max_rows * (d / 4);
     const int grid = (int)std::min<long long>((work + 255) / 256, 148 * 8);
     sum_planes_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4 *>(P), splits,
                                             plane / 4, d / 4, rows_end, max_rows,
-                                            reinterpret_cast<float4 *>(out), round_bf16 ? 1 : 0);
+                                            reinterpret_cast<float4 *>(out));
     note_launch();
     return cudaGetLastError();
 }

@@ -391,7 +391,7 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
         MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E,
                                 kRouterParts * dp,
-                                dp, S, s.T * s.E, te, ts, nt, off, part, a.E, 0, st));
+                                dp, S, s.T * s.E, te, ts, nt, off, part, a.E, st));
         // the softmax kernel adds the S chain planes in plane order as it reads them
         MOE_CUDA(launch_router_from_logits(a, part, S, st));
     } else {
@@ -421,11 +421,10 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
 // Up and down projections of one grouped FFN on the tensor cores: rows of A
 // (x_sorted, or x itself for the shared expert) grouped by `offsets` into
 // `groups` experts; h gets the activation in bf16; the down projection's
-// output goes to `out`: plan.s_down fp32 planes of rows*d elements, or with
-// one split the format out_mode names (kOutF32, kOutBF16, kOutF32Rounded).
+// output goes to `out`: plan.s_down fp32 planes of rows*d elements.
 int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void *A,
                long long rows, int groups, int F, const int32_t *offsets, const void *w1,
-               const void *w3, const void *w2, void *h, float *up_part, void *out, int out_mode,
+               const void *w3, const void *w2, void *h, float *up_part, float *out,
                int32_t *tile_e, int32_t *tile_start, int32_t *ntiles, int up_stage,
                int down_stage, cudaStream_t st) {
     const int d = c->d_model;
@@ -438,13 +437,13 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
         MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, 1, A, rows, d, w1, w3, groups, F, F, d,
                                 d, plan.s_up,
                                 rows * upw * F, tile_e, tile_start, ntiles, offsets, up_part,
-                                upw * F, 0, st));
+                                upw * F, st));
         MOE_CUDA(launch_split_activation(up_part, plan.s_up, rows * upw * F, F,
                                          up_mode == GEMM_UP_SWIGLU, offsets + groups, rows,
                                          static_cast<__nv_bfloat16 *>(h), st));
     } else {
         MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, 1, A, rows, d, w1, w3, groups, F, F, d,
-                                d, 1, 0, tile_e, tile_start, ntiles, offsets, h, F, 0, st));
+                                d, 1, 0, tile_e, tile_start, ntiles, offsets, h, F, st));
     }
     if (up_stage >= 0) {
         stage_end(up_stage, ev, st);
@@ -456,22 +455,20 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
                                     tile_e, nullptr, tile_start, ntiles, st));
     MOE_CUDA(launch_tc_gemm(GEMM_DOWN, plan.nt_down, plan.bn_down, mh_down, h, rows, F, w2, nullptr,
                             groups, d, d, F, F, plan.s_down, rows * d, tile_e, tile_start, ntiles,
-                            offsets, out, d, plan.s_down == 1 ? out_mode : kOutF32, st));
+                            offsets, out, d, st));
     if (down_stage >= 0) stage_end(down_stage, ev, st);
     return MOE_OK;
 }
 
 // Grouped expert FFN over the dispatched rows; out_sorted fp32 (plan.s_down
-// planes of R*d elements), or with one split the format out_mode names
-// (bf16 layers only for kOutBF16 and kOutF32Rounded).  bf16: gather the rows into x_sorted, tcgen05
-// up (+activation) into h, tcgen05 down into out_sorted.  fp32: SIMT GEMMs
-// reading x through perm directly.
+// planes of R*d elements).  bf16: gather the rows into x_sorted, tcgen05 up
+// (+activation, h in bf16) into h, tcgen05 down into out_sorted.  fp32: SIMT
+// GEMMs reading x through perm directly.
 int run_experts(const moe_config *c, const void *x, const int32_t *perm, const int32_t *offsets,
-                const void *w1, const void *w3, const void *w2, void *out_sorted,
-                int out_mode, void *ws, const Layout &L, cudaStream_t st) {
+                const void *w1, const void *w3, const void *w2, float *out_sorted, void *ws,
+                const Layout &L, cudaStream_t st) {
     const Sizes s = sizes(c);
     if (s.R == 0) return MOE_OK;
-    if (out_mode != kOutF32 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
     const int gk = expert_choice(c) ? 1 : (int)s.k;   // perm holds t*k+j, or t itself
     int32_t *tile_e = at<int32_t>(ws, L.tile_e), *tile_m0 = at<int32_t>(ws, L.tile_m0);
     int32_t *tile_start = at<int32_t>(ws, L.tile_start), *ntiles = at<int32_t>(ws, L.ntiles);
@@ -482,7 +479,7 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
         MOE_CUDA(launch_gather_rows(x, 2, (int)s.d, perm, offsets + s.E, gk, s.R, xs, st));
         stage_end(MOE_STAGE_GATHER, ev, st);
         return run_tc_ffn(c, routed_plan(c), up_mode, xs, s.R, (int)s.E, (int)s.F, offsets, w1,
-                          w3, w2, h, at<float>(ws, L.up_part), out_sorted, out_mode, tile_e,
+                          w3, w2, h, at<float>(ws, L.up_part), out_sorted, tile_e,
                           tile_start, ntiles, MOE_STAGE_UP, MOE_STAGE_DOWN, st);
     }
     cudaEvent_t ev = stage_begin(st);
@@ -508,10 +505,10 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
 }
 
 // Shared expert (SwiGLU) on all T rows -> sh_out: shared_plan.s_down fp32
-// planes of T*d elements, or one bf16 plane (out_mode kOutBF16, one split):
-// the same grouped kernels with one group {0, T} and x read in place.
+// planes of T*d elements: the same grouped kernels with one group {0, T} and
+// x read in place.
 int run_shared(const moe_config *c, const void *x, const void *ws1, const void *ws3,
-               const void *ws2, int out_mode, void *ws, const Layout &L, cudaStream_t st) {
+               const void *ws2, void *ws, const Layout &L, cudaStream_t st) {
     const Sizes s = sizes(c);
     if (s.T == 0) return MOE_OK;
     int32_t *off = at<int32_t>(ws, L.sh_offsets);
@@ -524,7 +521,7 @@ int run_shared(const moe_config *c, const void *x, const void *ws1, const void *
     float *o = at<float>(ws, L.sh_out);
     if (c->dtype == MOE_DTYPE_BF16)
         return run_tc_ffn(c, shared_plan(c), GEMM_UP_SWIGLU, x, s.T, 1, (int)s.Fs, off, ws1, ws3,
-                          ws2, h, at<float>(ws, L.sh_up_part), o, out_mode, te, ts, nt, -1,
+                          ws2, h, at<float>(ws, L.sh_up_part), o, te, ts, nt, -1,
                           -1, st);
     MOE_CUDA(launch_build_tiles(off, 1, kSimtBM, te, tm, nullptr, nt, st));
     GroupedGemmArgs up;
@@ -702,9 +699,8 @@ int moe_combine_rows(const moe_config *cfg, const float *out_sorted, const float
     if (cfg->T == 0) return MOE_OK;
     MOE_PTR(out_sorted); MOE_PTR(row_w); MOE_PTR(tok_start); MOE_PTR(tok_rows); MOE_PTR(y);
     MOE_OPT_PTR(shared_out);
-    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
-    MOE_CUDA(launch_combine_rows(expert_out_f32(out_sorted, 1, 0, bf16), tok_start, tok_rows,
-                                 row_w, expert_out_f32(shared_out, 1, 0, bf16),
+    MOE_CUDA(launch_combine_rows(expert_out_f32(out_sorted), tok_start, tok_rows,
+                                 row_w, expert_out_f32(shared_out),
                                  cfg->T, cfg->d_model, cfg->out_dtype, y, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -741,20 +737,16 @@ int moe_expert_ffn(const moe_config *cfg, const void *x, const int32_t *perm,
     const Layout L = layout(cfg);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     const FfnPlan plan = routed_plan(cfg);
-    // a bf16 layer's expert outputs are bf16 values (held here in fp32)
-    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
     if (plan.s_down == 1)
-        return run_experts(cfg, x, perm, offsets, w1, w3, w2, out_sorted,
-                           bf16 ? kOutF32Rounded : kOutF32, ws, L, (cudaStream_t)stream);
+        return run_experts(cfg, x, perm, offsets, w1, w3, w2, out_sorted, ws, L,
+                           (cudaStream_t)stream);
     // split reduction: partial planes in the workspace, summed into out_sorted
     float *planes = at<float>(ws, L.out_sorted);
-    rc = run_experts(cfg, x, perm, offsets, w1, w3, w2, planes, kOutF32, ws, L,
-                     (cudaStream_t)stream);
+    rc = run_experts(cfg, x, perm, offsets, w1, w3, w2, planes, ws, L, (cudaStream_t)stream);
     if (rc != MOE_OK) return rc;
     const long long R = sizes(cfg).R;
     MOE_CUDA(launch_sum_planes(planes, plan.s_down, R * cfg->d_model, cfg->d_model,
-                               offsets + cfg->n_experts, R, out_sorted, (cudaStream_t)stream,
-                               bf16));
+                               offsets + cfg->n_experts, R, out_sorted, (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -764,9 +756,8 @@ int moe_combine(const moe_config *cfg, const float *out_sorted, const int32_t *i
     if (rc != MOE_OK) return rc;
     if (cfg->T == 0) return MOE_OK;
     MOE_PTR(out_sorted); MOE_PTR(inv); MOE_PTR(topk_w); MOE_PTR(y); MOE_OPT_PTR(shared_out);
-    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
-    MOE_CUDA(launch_combine(expert_out_f32(out_sorted, 1, 0, bf16), inv, topk_w,
-                            expert_out_f32(shared_out, 1, 0, bf16), cfg->T, cfg->top_k,
+    MOE_CUDA(launch_combine(expert_out_f32(out_sorted), inv, topk_w,
+                            expert_out_f32(shared_out), cfg->T, cfg->top_k,
                             cfg->d_model, cfg->out_dtype, y, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -864,6 +855,7 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     MOE_OPT_PTR(out->n_dropped); MOE_OPT_PTR(out->f); MOE_OPT_PTR(out->p); MOE_OPT_PTR(out->aux);
     MOE_OPT_PTR(out->load_max_over_mean); MOE_OPT_PTR(out->select_bias_out);
     MOE_OPT_PTR(out->counts_unbiased); MOE_OPT_PTR(out->slot_expert); MOE_OPT_PTR(out->slot_w);
+    MOE_OPT_PTR(out->offsets); MOE_OPT_PTR(out->perm);
     if (obs) {
         MOE_OPT_PTR(obs->drop_ratio); MOE_OPT_PTR(obs->gate_entropy);
         MOE_OPT_PTR(obs->bias_mean_abs); MOE_OPT_PTR(obs->bias_max_abs);
@@ -881,21 +873,15 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     int32_t *counts = out->counts ? out->counts : at<int32_t>(ws, L.counts);
     int32_t *ndrop = out->n_dropped ? out->n_dropped : at<int32_t>(ws, L.ndrop);
     float *sbias = out->select_bias_out ? out->select_bias_out : at<float>(ws, L.sbias);
-    int32_t *offsets = at<int32_t>(ws, L.offsets);
-    int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
-    // Expert outputs: one bf16 plane for bf16 layers whose down projection is
-    // not split (half the bytes written by the down projection and read by
-    // the combine); fp32 planes otherwise.
-    // (a bf16 layer's expert outputs are bf16 tensors: split planes are
-    // rounded after their sum)
-    void *out_sorted = at<void>(ws, L.out_sorted);
-    const bool bf16 = cfg->dtype == MOE_DTYPE_BF16;
+    int32_t *offsets = out->offsets ? out->offsets : at<int32_t>(ws, L.offsets);
+    int32_t *perm = out->perm ? out->perm : at<int32_t>(ws, L.perm);
+    int32_t *inv = at<int32_t>(ws, L.inv);
+    // Expert outputs: fp32 planes (one per split of the down projection's
+    // reduction, added in split order by their readers), routed and shared.
+    float *out_sorted = at<float>(ws, L.out_sorted);
     const FfnPlan rplan = routed_plan(cfg), splan = shared_plan(cfg);
-    const bool o_bf16 = bf16 && rplan.s_down == 1;
-    const ExpertOut eo{out_sorted, o_bf16 ? 1 : 0, rplan.s_down, s.R * s.d,
-                       (bf16 && !o_bf16) ? 1 : 0};
-    const bool sh_bf16 = bf16 && splan.s_down == 1;
-    ExpertOut sh{nullptr, sh_bf16 ? 1 : 0, splan.s_down, s.T * s.d, (bf16 && !sh_bf16) ? 1 : 0};
+    const ExpertOut eo = expert_out_f32(out_sorted, rplan.s_down, s.R * s.d);
+    ExpertOut sh = expert_out_f32(nullptr, splan.s_down, s.T * s.d);
 
     const bool biased = cfg->quantile_balance || wts->select_bias != nullptr;
     const bool want_unb = out->counts_unbiased != nullptr;
@@ -972,8 +958,7 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
                                          obs->expert_out_std, obs->expert_out_max_abs, st));
         return MOE_OK;
     }
-    rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted,
-                     o_bf16 ? kOutBF16 : kOutF32, ws, L, st);
+    rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted, ws, L, st);
     if (rc != MOE_OK) return rc;
     if (want_scale)
         MOE_CUDA(launch_expert_scale(eo, (int)s.d, offsets, (int)s.E, s.R,
@@ -982,11 +967,10 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
                                      obs->expert_out_max_abs, st));
     if (s.Fs > 0) {
         ev = stage_begin(st);
-        rc = run_shared(cfg, x, wts->ws1, wts->ws3, wts->ws2, sh_bf16 ? kOutBF16 : kOutF32, ws,
-                        L, st);
+        rc = run_shared(cfg, x, wts->ws1, wts->ws3, wts->ws2, ws, L, st);
         if (rc != MOE_OK) return rc;
         stage_end(MOE_STAGE_SHARED, ev, st);
-        sh.p = at<void>(ws, L.sh_out);
+        sh.p = at<float>(ws, L.sh_out);
     }
     ev = stage_begin(st);
     if (ec)
@@ -1013,6 +997,17 @@ int moe_device_status(moe_stream_t stream) {
 
 int64_t moe_kernel_launches(void) {
     return __atomic_load_n(&g_kernel_launches, __ATOMIC_RELAXED);
+}
+
+int moe_kernel_binary_version(int32_t *version) {
+    if (!version) return MOE_ERR_INVALID_ARG;
+    cudaFuncAttributes a{};
+    if (cudaFuncGetAttributes(&a, set_pair_kernel) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    *version = a.binaryVersion;
+    return MOE_OK;
 }
 
 int moe_stage_timing_enable(int on) {

@@ -10,7 +10,7 @@ import oracle.moe_oracle as om
 import sparse_mixture_experts_47_b300 as moe
 from tests.conftest import load_golden
 from tests.parity import (FP_ATOL, W_ATOL, act_dtype, compare_y, full_check, gpu_layer,
-                          oracle_layer, weights_dict, y_allow)
+                          oracle_layer, weights_dict, y_tol)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -86,12 +86,11 @@ def test_bf16_output_matches_fp32_output():
 def test_batch_invariance(name, T):
     """A token's routing does not depend on the batch it comes in (the
     pages' batch=1 vs batch=64 check): indices and gate weights are
-    bit-identical, outputs agree within the tolerance (GEMM tiling differs)."""
+    bit-identical, outputs agree within the layer's y tolerance (GEMM tiling
+    differs)."""
     w, _ = SMALL[name]
     inp = mi.generate(w, T, DEV)
     big = gpu_layer(w, T, inp)
-    # magnitude of y's terms for the rounding allowance of both runs
-    y_abs = oracle_layer(w, inp, tokens=range(16))["y_abs"]
     rms = float(np.sqrt(np.mean(big["y"].astype(np.float64) ** 2)))
     for t in (1, 16):
         sub = dict(inp)
@@ -99,7 +98,7 @@ def test_batch_invariance(name, T):
         small = gpu_layer(w, t, sub)
         assert np.array_equal(small["idx"], big["idx"][:t])
         assert np.array_equal(small["w"], big["w"][:t])
-        assert np.all(np.abs(small["y"] - big["y"][:t]) <= y_allow(w, rms, y_abs[:t]))
+        assert np.max(np.abs(small["y"] - big["y"][:t])) <= y_tol(w) * rms
 
 
 def test_layer_graph_and_pipeline_match_eager():
@@ -265,7 +264,8 @@ def test_expert_ffn_and_combine_stages(name):
         ref[a:b] = om.expert_ffn(x[rows], inp["w1"][e], None if inp["w3"] is None else inp["w3"][e],
                                  inp["w2"][e], w.act, act_dtype(w))
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    assert np.all(np.abs(got - ref) <= y_allow(w, rms, np.abs(ref)))
+    err = float(np.max(np.abs(got - ref)))
+    assert err <= y_tol(w) * rms, (err / rms, y_tol(w))
     # combine with the oracle's expert outputs (rounded to fp32) and weights
     shared = None
     if w.d_ff_shared:
@@ -276,3 +276,7 @@ def test_expert_ffn_and_combine_stages(name):
                     torch.tensor(orc["router"].w, dtype=torch.float32, device=DEV), shared)
     yo = orc["y"]
     assert np.max(np.abs(y.cpu().numpy() - yo)) <= 1e-5 * float(np.sqrt(np.mean(yo ** 2)))
+
+
+def test_kernels_loaded_for_sm_103a():
+    assert moe.kernel_binary_version() == 103

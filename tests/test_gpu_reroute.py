@@ -11,7 +11,7 @@ import moe_inputs as mi
 import oracle.moe_oracle as om
 import sparse_mixture_experts_47_b300 as moe
 from tests.conftest import load_golden
-from tests.parity import full_check, gpu_layer, sample_tokens, tie_mask
+from tests.parity import full_check, sample_tokens
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -95,18 +95,15 @@ SMALL = {
 def test_layer_reroute_small_full_oracle(name):
     w, T = SMALL[name]
     inp = mi.generate(w, T, DEV)
-    rep, gpu, orc = full_check(w, T, inp)
+    rep, gpu, orc = full_check(w, T, inp, want_slots=True)
     print(name, rep)
     plain = om.moe_forward(inp, w.top_k, w.act, w.capacity_factor, "probs", False, [0],
                            "bf16")
     assert orc["dispatch"].n_dropped < plain["dispatch"].n_dropped   # redirection helps
     assert (orc["dispatch"].slot_round > 0).any()
-    # the served expert of every slot, on tokens before the first tie
-    g = gpu_layer(w, T, inp, want_slots=True)
-    ties, _ = tie_mask(orc["router"], w.top_k)
-    first = int(np.nonzero(ties)[0].min()) if ties.any() else T
-    assert np.array_equal(g["slot_expert"][:first], orc["dispatch"].slot_expert[:first])
-    assert np.max(np.abs(g["slot_w"][:first] - orc["dispatch"].slot_w[:first])) <= 1e-5
+    # the served expert and weight of every slot
+    assert np.array_equal(gpu["slot_expert"], orc["dispatch"].slot_expert)
+    assert np.max(np.abs(gpu["slot_w"] - orc["dispatch"].slot_w)) <= 1e-5
 
 
 def test_layer_reroute_full_size():

@@ -283,29 +283,42 @@ def pin_round_to_bf16():
     assert om.round_to_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -30]))[0] == 1 + 2.0 ** -7
 
 
+def pin_round_to_fp32():
+    # nearest even at 24 significant bits, checked on values built from their
+    # binary expansion (spacing 2^-23 on [1, 2)) and against torch's
+    # float64 -> float32 conversion of random values over a wide range
+    assert om.round_to_fp32(np.array([1 + 2.0 ** -24]))[0] == 1.0
+    assert om.round_to_fp32(np.array([1 + 3 * 2.0 ** -24]))[0] == 1 + 2.0 ** -22
+    assert om.round_to_fp32(np.array([1 + 2.0 ** -24 + 2.0 ** -40]))[0] == 1 + 2.0 ** -23
+    assert om.round_to_fp32(np.array([-(2 + 2.0 ** -23)]))[0] == -2.0
+    v = RNG.normal(size=4000) * np.exp(RNG.uniform(-60, 60, size=4000))
+    ref = torch.tensor(v, dtype=torch.float64).to(torch.float32).to(torch.float64).numpy()
+    assert np.array_equal(om.round_to_fp32(v), ref)
+
+
 def pin_bf16_activation_ffn():
-    # E = 1 with bf16 storage: the page's Expert in a bf16 model stores h in
-    # bf16 before w2 and returns its output as a bf16 tensor (gate weight 1
-    # here); torch.nn.functional in float64 with both tensors rounded by torch.
+    # E = 1 with bf16 storage of the intermediate activation (reading R8):
+    # h is a bf16 tensor before w2, the output row stays exact (gate weight 1
+    # here); torch.nn.functional in float64 with h rounded by torch.
     inp = _rand_layer(13, 16, 1, 24, "swiglu")
     out = om.moe_forward(inp, 1, "swiglu", act_dtype="bf16")
     x, w1, w3, w2 = (torch.tensor(np.asarray(a, dtype=np.float64))
                      for a in (inp["x"], inp["w1"][0], inp["w3"][0], inp["w2"][0]))
     h = Fnn.silu(Fnn.linear(x, w1)) * Fnn.linear(x, w3)
-    h = h.to(torch.float32).to(torch.bfloat16).to(torch.float64)
-    o = Fnn.linear(h, w2)
-    ref = o.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    hb = h.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    ref = Fnn.linear(hb, w2).numpy()
     assert np.allclose(out["y"], ref, atol=1e-12)
-    assert not np.allclose(ref, o.numpy(), atol=1e-6)   # the output rounding is visible
+    # the output is not rounded: some element lies off the bf16 grid
+    assert not np.array_equal(om.round_to_bf16(out["y"]), out["y"])
     exact = om.moe_forward(inp, 1, "swiglu")
-    assert not np.allclose(out["y"], exact["y"], atol=1e-6)   # the rounding is visible
+    assert np.allclose(exact["y"], Fnn.linear(h, w2).numpy(), atol=1e-12)
+    assert not np.allclose(out["y"], exact["y"], atol=1e-6)   # h's rounding is visible
 
 
-def pin_bf16_mixture_rounds_each_expert_output():
-    # k = 2 of E = 3 with a shared expert, bf16 storage: each selected expert's
-    # output and the shared expert's output are bf16 tensors (the Expert
-    # modules of [MoE-ch30] s30.6.1 in a bf16 model), combined with the gate
-    # weights in float64; torch rounds every tensor.
+def pin_bf16_mixture_exact_expert_outputs():
+    # k = 2 of E = 3 with a shared expert, bf16 storage: each expert rounds
+    # its h to bf16 (torch), and the expert outputs, the gate-weighted sum
+    # and the shared expert's output are exact float64.
     inp = _rand_layer(11, 16, 3, 24, "swiglu", Fs=20)
     out = om.moe_forward(inp, 2, "swiglu", act_dtype="bf16")
     x = torch.tensor(np.asarray(inp["x"], dtype=np.float64))
@@ -316,7 +329,7 @@ def pin_bf16_mixture_rounds_each_expert_output():
     def expert(w1, w3, w2, rows):
         t = lambda a: torch.tensor(np.asarray(a, dtype=np.float64))
         h = bf(Fnn.silu(Fnn.linear(rows, t(w1))) * Fnn.linear(rows, t(w3)))
-        return bf(Fnn.linear(h, t(w2)))
+        return Fnn.linear(h, t(w2))
 
     r = out["router"]
     ref = np.zeros_like(out["y"])
@@ -327,7 +340,100 @@ def pin_bf16_mixture_rounds_each_expert_output():
             ref[tok] += r.w[tok, j] * o[0].numpy()
     ref += expert(inp["ws1"], inp["ws3"], inp["ws2"], x).numpy()
     assert np.allclose(out["y"], ref, atol=1e-12)
-    assert np.allclose(out["y_abs"] >= np.abs(out["y"]) - 1e-12, True)
+
+
+def _logit_layer(logits, F):
+    """A layer whose router logits are ``logits`` exactly: x = logits,
+    W_r = I (d = E), random experts of width F."""
+    T, E = logits.shape
+    return {"x": logits, "w_r": np.eye(E),
+            "w1": RNG.normal(size=(E, F, E)) / math.sqrt(E),
+            "w3": RNG.normal(size=(E, F, E)) / math.sqrt(E),
+            "w2": RNG.normal(size=(E, E, F)) / math.sqrt(F)}
+
+
+def pin_ranking_of_tied_tokens():
+    # Token 0 has two experts with exactly equal scores: the plain rule puts
+    # the lower index first (R5).  Giving the other order through ``ranking``
+    # must equal routing on scores nudged to prefer it (the nudge is far below
+    # every other gap and moves the weights by ~1e-12), for the top-k, the
+    # capacity drops, the statistics and y; tokens not named keep the plain
+    # order.
+    lg = RNG.normal(size=(12, 4))
+    lg[0, 1] = lg[0, 2] = lg[0].max() + 0.5              # experts 1 and 2 tie on token 0
+    inp = _logit_layer(lg, 10)
+    plain = om.moe_forward(inp, 1, "swiglu", capacity_factor=0.7)
+    assert plain["router"].idx[0, 0] == 1
+    alt = om.moe_forward(inp, 1, "swiglu", capacity_factor=0.7, ranking={0: [2]})
+    nudged = dict(inp, x=lg.copy())
+    nudged["x"][0, 2] += 1e-12
+    ref = om.moe_forward(nudged, 1, "swiglu", capacity_factor=0.7)
+    assert alt["router"].idx[0, 0] == 2
+    assert alt["router"].idx.tolist() == ref["router"].idx.tolist()
+    assert np.allclose(alt["router"].w, ref["router"].w, atol=1e-12)
+    assert alt["dispatch"].perm.tolist() == ref["dispatch"].perm.tolist()
+    assert alt["stats"]["counts"].tolist() == ref["stats"]["counts"].tolist()
+    assert np.allclose(alt["y"], ref["y"], atol=1e-9)
+    assert not np.allclose(alt["y"][0], plain["y"][0], atol=1e-6)
+    # k = 2, with and without redirection: the given order of token 0 leads
+    # its ranking, the rest of its ranking follows the scores
+    lg2 = RNG.normal(size=(10, 5))
+    lg2[0, 3] = lg2[0, 4] = lg2[0].max() + 1.0
+    inp2 = _logit_layer(lg2, 8)
+    n2 = dict(inp2, x=lg2.copy())
+    n2["x"][0, 4] += 1e-12
+    for rounds in (0, 1):
+        a = om.moe_forward(inp2, 2, "swiglu", capacity_factor=0.6, reroute_rounds=rounds,
+                           ranking={0: [4, 3]})
+        b = om.moe_forward(n2, 2, "swiglu", capacity_factor=0.6, reroute_rounds=rounds)
+        assert a["router"].idx.tolist() == b["router"].idx.tolist()
+        assert np.allclose(a["router"].w, b["router"].w, atol=1e-12)
+        assert a["dispatch"].perm.tolist() == b["dispatch"].perm.tolist()
+        assert a["dispatch"].n_dropped == b["dispatch"].n_dropped
+        assert np.allclose(a["y"], b["y"], atol=1e-9)
+    # a selection bias makes experts 3 and 4 tie in score at the k-th place
+    # of token 0 while their probabilities differ: the given order swaps
+    # which one is selected, and its weights come from the probabilities
+    lg3 = RNG.normal(size=(6, 5))
+    lg3[0] = [3.0, -1.0, -2.0, 1.0, 0.5]
+    inp3 = _logit_layer(lg3, 8)
+    p0 = om.softmax(lg3)[0]
+    b4 = p0[3] - p0[4]
+    for _ in range(8):
+        if p0[4] + b4 == p0[3]:
+            break
+        b4 = np.nextafter(b4, np.inf if p0[4] + b4 < p0[3] else -np.inf)
+    assert p0[4] + b4 == p0[3]
+    bias = np.array([0.0, 0.0, 0.0, 0.0, b4])
+    inp3["select_bias"] = bias
+    plain3 = om.moe_forward(inp3, 2, "swiglu")
+    assert plain3["router"].idx[0].tolist() == [0, 3]
+    a3 = om.moe_forward(inp3, 2, "swiglu", ranking={0: [0, 4]})
+    n3 = dict(inp3, select_bias=bias + np.array([0, 0, 0, 0, 1e-15]))
+    b3 = om.moe_forward(n3, 2, "swiglu")
+    assert a3["router"].idx.tolist() == b3["router"].idx.tolist()
+    assert np.array_equal(a3["router"].w, b3["router"].w)
+    assert np.allclose(a3["y"], b3["y"], atol=1e-12)
+    assert not np.allclose(a3["router"].w[0], plain3["router"].w[0], atol=1e-3)
+
+
+def pin_expert_choice_given_set():
+    # Expert 0's column ties exactly at its C-th value between tokens 2 and 5;
+    # the lower token wins (R11).  Giving the other token through ``chosen``
+    # equals expert choice on a column nudged to prefer it.
+    T, E, C = 8, 3, 3
+    probs = om.softmax(RNG.normal(size=(T, E)))
+    col = np.array([0.9, 0.1, 0.5, 0.2, 0.8, 0.5, 0.05, 0.3])
+    probs[:, 0] = col
+    plain = om.expert_choice(probs, C)
+    assert plain.chosen[0].tolist() == [0, 2, 4]
+    alt = om.expert_choice(probs, C, chosen={0: [5, 0, 4]})
+    nudged = probs.copy()
+    nudged[5, 0] += 1e-15
+    ref = om.expert_choice(nudged, C)
+    assert alt.chosen.tolist() == ref.chosen.tolist()
+    assert np.allclose(alt.weight, ref.weight, atol=1e-14)
+    assert alt.n_unchosen == ref.n_unchosen
 
 
 def pin_gate_entropy():
@@ -502,8 +608,9 @@ PINS = [pin_top2_example, pin_aux_worked_example, pin_selection_bias_example,
         pin_router_logits_layout, pin_single_expert_is_dense_ffn, pin_identical_experts,
         pin_all_experts_is_dense_mixture, pin_shared_expert_added, pin_capacity_cases,
         pin_capacity_switch_workload, pin_dispatch_invariants, pin_quantile_vs_numpy,
-        pin_quantile_balance_share, pin_round_to_bf16, pin_bf16_activation_ffn,
-        pin_bf16_mixture_rounds_each_expert_output,
+        pin_quantile_balance_share, pin_round_to_bf16, pin_round_to_fp32,
+        pin_bf16_activation_ffn, pin_bf16_mixture_exact_expert_outputs,
+        pin_ranking_of_tied_tokens, pin_expert_choice_given_set,
         pin_gate_entropy, pin_expert_output_scale, pin_observe_drop_and_bias,
         pin_reroute_cases, pin_reroute_invariants, pin_expert_choice_case,
         pin_expert_choice_bruteforce, pin_expert_choice_full_capacity_is_dense_mixture]
@@ -599,10 +706,37 @@ def _mut_round_truncate(a):
     return np.trunc(a / q) * q                      # truncation instead of nearest-even
 
 
-def _mut_ffn_output_unrounded(x_rows, w1, w3, w2, act, act_dtype="fp64"):
+def _mut_ffn_output_rounded(x_rows, w1, w3, w2, act, act_dtype="fp64"):
     a = x_rows @ om._f64(w1).T
     h = om._silu(a) * (x_rows @ om._f64(w3).T) if act == "swiglu" else np.maximum(a, 0.0)
-    return om.ACT_ROUNDING[act_dtype](h) @ om._f64(w2).T   # output row left unrounded
+    h = om.ACT_ROUNDING[act_dtype](h)
+    return om.ACT_ROUNDING[act_dtype](h @ om._f64(w2).T)   # output row rounded too
+
+
+def _mut_ffn_h_unrounded(x_rows, w1, w3, w2, act, act_dtype="fp64"):
+    a = x_rows @ om._f64(w1).T
+    h = om._silu(a) * (x_rows @ om._f64(w3).T) if act == "swiglu" else np.maximum(a, 0.0)
+    return h @ om._f64(w2).T                                # h left at full precision
+
+
+def _mut_round_fp32_truncate(a):
+    v = np.asarray(a, dtype=np.float64)
+    f = v.astype(np.float32).astype(np.float64)
+    over = np.abs(f) > np.abs(v)                            # rounded away from zero
+    return np.where(over, np.nextafter(f.astype(np.float32), np.float32(0)).astype(np.float64), f)
+
+
+_ORIG_WITH_RANKING = om.with_ranking
+
+
+def _mut_ranking_keeps_weights(r, ranking):
+    out = _ORIG_WITH_RANKING(r, ranking)
+    out.w = r.w.copy()                                      # weights not renormalised
+    return out
+
+
+def _mut_ranking_ignored(r, ranking):
+    return r
 
 
 def _mut_capacity_floor(T, k, E, cf):
@@ -700,7 +834,11 @@ MUTATIONS = [
     ("topk_desc", _mut_topk_ascending),
     ("topk_desc", _mut_topk_unstable_ties),
     ("expert_ffn", _mut_silu_on_w3),
-    ("expert_ffn", _mut_ffn_output_unrounded),
+    ("expert_ffn", _mut_ffn_output_rounded),
+    ("expert_ffn", _mut_ffn_h_unrounded),
+    ("round_to_fp32", _mut_round_fp32_truncate),
+    ("with_ranking", _mut_ranking_keeps_weights),
+    ("with_ranking", _mut_ranking_ignored),
     ("router_logits", _mut_router_reversed_experts),
     ("router_logits", _mut_router_sign),
     ("dispatch", _mut_drop_last),
