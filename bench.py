@@ -419,7 +419,8 @@ def run_ours(args, w, T):
     tc_peak = peaks["bf16_tflops_sustained"] * 1e12
     tc_burst = peaks["bf16_tflops"] * 1e12
     hbm = peaks["hbm_gbs"] * 1e9
-    roof_s = max(flops / tc_peak, bytes_ / hbm)
+    roof_s = max(flops / tc_burst, bytes_ / hbm)
+    roof_sus_s = max(flops / tc_peak, bytes_ / hbm)
     up_ms = stage_ms["up"] / max(calls, 1)
     up_tflops = up_flops / (up_ms / 1e3) / 1e12
     up_gbs = up_bytes / (up_ms / 1e3) / 1e9
@@ -427,12 +428,16 @@ def run_ours(args, w, T):
             if r.get("workload") == w.name and not args.n_experts]
     exact = [r for r in recs if r.get("T") == T]
     tr = exact[0] if exact else (recs[-1] if recs else None)
-    up_tensor_bound = up_flops / tc_peak >= up_bytes / hbm
+    # The dominant kernel is timed per launch inside short graph replays, a
+    # burst window: its tensor-bound fraction is quoted against the measured
+    # burst bf16 peak; the sustained peak (a seconds-long loop under the
+    # power cap) is reported beside it.
+    up_tensor_bound = up_flops / tc_burst >= up_bytes / hbm
     if up_tensor_bound:
-        roof = {"bound": "tensor", "achieved": up_tflops, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": up_tflops / peaks["bf16_tflops_sustained"],
-                "frac_of_burst": up_tflops * 1e12 / tc_burst,
-                "peak_source": f"{src} bf16_tflops_sustained"}
+        roof = {"bound": "tensor", "achieved": up_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": up_tflops * 1e12 / tc_burst,
+                "frac_of_sustained": up_tflops * 1e12 / tc_peak,
+                "peak_source": f"{src} bf16_tflops (burst)"}
     else:
         roof = {"bound": "hbm", "achieved": up_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": up_gbs / peaks["hbm_gbs"], "peak_source": f"{src} hbm_gbs"}
@@ -448,7 +453,13 @@ def run_ours(args, w, T):
             # the row traffic (x_sorted in, h out) grows with T
             rows = tr["dram_bytes_per_launch"] - tr["weight_bytes"]
             roof["traffic"] = tr["weight_bytes"] + rows * T / tr["T"]
-        roof["traffic_source"] = f"ncu capture at T={tr.get('T')}"
+        roof["traffic_source"] = (
+            f"not measured in this run: dram__bytes_read.sum + dram__bytes_write.sum of one "
+            f"ncu capture at T={tr.get('T')} of the same kernel source (hash "
+            f"{tr.get('source_sha256_16')}), recorded in profiles/ncu_traffic.md"
+            + ("" if tr.get("T") == T else f", scaled to T={T} by its row traffic"))
+    else:
+        roof["traffic_source"] = "no ncu record of the current kernel source"
 
     if rank != 0:
         return
@@ -476,8 +487,10 @@ def run_ours(args, w, T):
         "roofline": roof,
         "layer_roofline": {"flops": flops, "bytes": bytes_, "roofline_ms": roof_s * 1e3,
                            "frac": roof_s / step_s,
-                           "bound": "tensor" if flops / tc_peak > bytes_ / hbm else "hbm",
-                           "peaks": f"{src}: {peaks['bf16_tflops_sustained']} TF/s sustained, "
+                           "frac_of_sustained": roof_sus_s / step_s,
+                           "bound": "tensor" if flops / tc_burst > bytes_ / hbm else "hbm",
+                           "peaks": f"{src}: {peaks['bf16_tflops']} TF/s burst "
+                                    f"({peaks['bf16_tflops_sustained']} sustained), "
                                     f"{peaks['hbm_gbs']} GB/s"},
         "stage_ms": {k: v / max(calls, 1) for k, v in stage_ms.items()},
         "e2e": {"value": job_throughput(world, T, args.steps, e2e_ms), "unit": "tokens/s",
