@@ -321,6 +321,10 @@ typedef struct {
                                   choice); rows = T*k, or E * Cn (see
                                   moe_expert_choice_rows); rows >= offsets[E]
                                   are not written */
+    int32_t *cand_idx;         /* [T, nc] with redirection (reroute_rounds > 0):
+                                  each token's experts ranked after its top k,
+                                  best first, nc = moe_reroute_candidates(cfg);
+                                  not written otherwise */
 } moe_layer_outputs;
 
 /* The whole forward pass (router, dispatch, experts, shared expert,
@@ -385,6 +389,19 @@ const char *moe_strerror(int status);
 /* Number of kernels this library has launched in this process (all entry
  * points, all devices); a monotone counter for launch accounting. */
 int64_t moe_kernel_launches(void);
+
+/* Test hook of the failure detection (no counterpart on the pages): every
+ * mbarrier wait in the tensor-core GEMM is bounded, and on expiry the kernel
+ * sets the error word that moe_device_status returns as
+ * MOE_ERR_DEVICE_TIMEOUT, lets its issued copies and MMAs finish, frees its
+ * tensor memory and returns.  This sets, on the current device, the limit of
+ * the main-loop waits (default 2e9 ns; the waits that drain an aborted CTA
+ * keep 2 s) and, with stall_mma = 1, makes the MMA issuer of every GEMM CTA
+ * first wait on a barrier phase that nothing completes, so the bounded wait
+ * runs out without any fault.  Synchronous; call it with no library work in
+ * flight and restore (2000000000, 0) afterwards.  MOE_ERR_INVALID_ARG for a
+ * zero limit or stall_mma outside {0, 1}. */
+int moe_debug_set_wait_hooks(uint64_t main_loop_limit_ns, int32_t stall_mma);
 
 /* The architecture the library's kernels were compiled for, as the CUDA
  * runtime reports it for one of them on the current device (binaryVersion:

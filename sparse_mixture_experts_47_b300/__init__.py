@@ -65,7 +65,7 @@ class _Outputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("y", "topk_idx", "topk_w", "counts", "n_dropped", "f", "p", "aux",
                  "load_max_over_mean", "select_bias_out", "counts_unbiased", "slot_expert",
-                 "slot_w", "offsets", "perm")]
+                 "slot_w", "offsets", "perm", "cand_idx")]
 
 
 OBS_KEYS = ("drop_ratio", "gate_entropy", "bias_mean_abs", "bias_max_abs", "expert_out_mean",
@@ -111,6 +111,8 @@ def _load():
     L.moe_strerror.argtypes = [I]; L.moe_strerror.restype = ctypes.c_char_p
     L.moe_kernel_launches.argtypes = []; L.moe_kernel_launches.restype = ctypes.c_int64
     L.moe_kernel_binary_version.argtypes = [P]; L.moe_kernel_binary_version.restype = I
+    L.moe_debug_set_wait_hooks.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+    L.moe_debug_set_wait_hooks.restype = I
     L.moe_stage_timing_enable.argtypes = [I]; L.moe_stage_timing_enable.restype = I
     L.moe_stage_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int64)]
@@ -367,7 +369,8 @@ def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
     monitoring set (``OBS_KEYS``: drop ratio, gate entropy, bias size,
     per-expert output mean/std/max) under the key "observe"; ``observed``
     may pass its preallocated tensors.  ``want_slots`` adds each slot's
-    serving expert and gate weight; ``want_layout`` the grouped layout
+    serving expert and gate weight (with redirection also each token's
+    candidate experts after its top k); ``want_layout`` the grouped layout
     (offsets [E+1], perm [rows])."""
     dev = x.device
     T, E, k, d = cfg.T, cfg.n_experts, cfg.top_k, cfg.d_model
@@ -394,6 +397,8 @@ def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
     if want_slots:
         need("slot_expert", (T, k), torch.int32)
         need("slot_w", (T, k), torch.float32)
+        if cfg.reroute_rounds > 0:
+            need("cand_idx", (T, max(reroute_candidates(cfg), 1)), torch.int32)
     if want_layout:
         need("offsets", (E + 1,), torch.int32)
         rows = E * expert_choice_rows(cfg) if cfg.routing == ROUTING_EXPERT_CHOICE else T * k
@@ -403,7 +408,8 @@ def layer_forward(cfg: MoEConfig, x, weights: Dict[str, Optional[torch.Tensor]],
                  _ptr(o["n_dropped"]), _ptr(o["f"]), _ptr(o["p"]), _ptr(o["aux"]),
                  _ptr(o["load_max_over_mean"]), _ptr(o.get("select_bias")),
                  _ptr(o.get("counts_unbiased")), _ptr(o.get("slot_expert")),
-                 _ptr(o.get("slot_w")), _ptr(o.get("offsets")), _ptr(o.get("perm")))
+                 _ptr(o.get("slot_w")), _ptr(o.get("offsets")), _ptr(o.get("perm")),
+                 _ptr(o.get("cand_idx")))
     buf, nb = _ws(cfg, dev, workspace)
     if observe or observed is not None:
         ob = _obs_tensors(cfg, dev, observed)
@@ -549,6 +555,14 @@ def kernel_binary_version() -> int:
     v = ctypes.c_int32(0)
     _check("moe_kernel_binary_version", lib.moe_kernel_binary_version(ctypes.byref(v)))
     return int(v.value)
+
+
+def debug_set_wait_hooks(main_loop_limit_ns: int = 2_000_000_000, stall_mma: bool = False
+                         ) -> None:
+    """Test hook of the GEMM's bounded waits on the current device (see
+    moe_debug_set_wait_hooks); the defaults restore normal operation."""
+    _check("moe_debug_set_wait_hooks",
+           lib.moe_debug_set_wait_hooks(int(main_loop_limit_ns), int(bool(stall_mma))))
 
 
 def stage_timing(on: bool) -> None:

@@ -60,6 +60,14 @@ constexpr int kSmemExtra =
 constexpr int kVarRows = 256;        // NT of the per-tile-width geometry
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 
+// Failure-detection test hooks (moe_debug_set_wait_hooks).  The limit of the
+// main-loop waits (producer, MMA issuer, epilogue); the drain waits after an
+// abort keep kWaitLimitNs.  g_stall_mma != 0 makes the MMA issuer first wait
+// on a barrier phase that nothing completes, so that its bounded wait runs
+// out and the abort path runs.
+__device__ unsigned long long g_main_wait_limit_ns = kWaitLimitNs;
+__device__ int g_stall_mma = 0;
+
 // Tile geometry of one kernel instantiation.  NT = 0: token rows on the M
 // side (A = 128 activation rows, B = 256 weight rows).  NT > 0: weight rows on
 // the M side (A = 128 rows of W1, plus 128 rows of W3 for SwiGLU), token rows
@@ -127,12 +135,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
+    const uint64_t limit = g_main_wait_limit_ns;
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit) {
             flag_error(kErrTimeout);
             *abort_flag = 1;
             return false;
@@ -312,7 +321,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------ TMA producer
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t issued = 0;   // stages with a load in flight or unconsumed
+        uint32_t issued = 0;       // stages that received a load
+        uint32_t issued_par = 0;   // bit s: phase parity of stage s's last load
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
             const TileCoord c = decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk);
@@ -350,16 +360,20 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (!G::SWAP || MODE == GEMM_UP_SWIGLU)
                     tma_load_2d(sb + G::BOX * BK * 2, &tmB1, kb * BK, b1, fb);
                 issued |= 1u << stage;
+                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
         }
         if (!ok) {
-            // Let the copies already issued land before the CTA can exit.
+            // Let the copies already issued land before the CTA can exit: the
+            // last load into stage s completes the full barrier's phase of
+            // parity issued_par[s] (only this thread arrives on it, so that
+            // phase stays the last completed one).
             for (int s = 0; s < STAGES; ++s) {
                 if (!(issued >> s & 1u)) continue;
+                const uint32_t par = issued_par >> s & 1u;
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(full0 + 8 * s, 0) && !mbar_try_wait(full0 + 8 * s, 1) &&
-                       globaltimer() - t0 < kWaitLimitNs) {
+                while (!mbar_try_wait(full0 + 8 * s, par) && globaltimer() - t0 < kWaitLimitNs) {
                 }
             }
         }
@@ -371,6 +385,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
+        // test hook: done_bar's first phase completes only at the commit
+        // below, so this wait can only run out
+        if (g_stall_mma && !mbar_wait(done_bar, 0, abort_flag)) ok = false;
         for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
             // The K range depends on the split alone; only the per-tile
             // width (NT = 256) needs the tile table here.
@@ -594,6 +611,14 @@ static bool make_map(CUtensorMap *m, const void *base, long long rows, long long
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
+}
+
+// moe_debug_set_wait_hooks: the current device's copies of the test hooks.
+cudaError_t set_wait_hooks(unsigned long long main_limit_ns, int stall_mma) {
+    cudaError_t e = cudaMemcpyToSymbol(tc::g_main_wait_limit_ns, &main_limit_ns,
+                                       sizeof(main_limit_ns));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(tc::g_stall_mma, &stall_mma, sizeof(stall_mma));
 }
 
 static int num_sms() {

@@ -161,5 +161,11 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
                            const int32_t *tile_e, const int32_t *tile_start,
                            const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
                            cudaStream_t st);
+namespace tc {
+// Test hooks of the grouped GEMM's bounded waits on the current device: the
+// main-loop wait limit in ns and a stall of the MMA issuer (see
+// moe_debug_set_wait_hooks).
+cudaError_t set_wait_hooks(unsigned long long main_limit_ns, int stall_mma);
+}  // namespace tc
 
 }  // namespace moe

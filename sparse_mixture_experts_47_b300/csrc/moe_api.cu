@@ -356,7 +356,7 @@ void stage_end(int stage, cudaEvent_t a, cudaStream_t st) {
 int run_router(const moe_config *c, const void *x, const float *w_r, const float *logit_bias,
                const float *select_bias, int32_t *idx, float *w, float *probs, float *p_out,
                float *sbias_out, bool want_probsT, void *ws, const Layout &L, cudaStream_t st,
-               float *entropy_out = nullptr) {
+               float *entropy_out = nullptr, int32_t *cand_out = nullptr) {
     const Sizes s = sizes(c);
     RouterArgs a{};
     a.x = x; a.w_r = w_r; a.logit_bias = logit_bias;
@@ -374,7 +374,7 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
     a.p_partial = at<float>(ws, L.p_partial);
     a.ent_partial = entropy_out ? at<float>(ws, L.ent_partial) : nullptr;
     a.n_cand = (int)n_candidates(c);
-    a.cand_idx = at<int32_t>(ws, L.cand_idx);
+    a.cand_idx = cand_out ? cand_out : at<int32_t>(ws, L.cand_idx);
     a.cand_w = at<float>(ws, L.cand_w);
     if (tc_router(c)) {
         const int dp = (int)router_dp(c);
@@ -855,7 +855,7 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     MOE_OPT_PTR(out->n_dropped); MOE_OPT_PTR(out->f); MOE_OPT_PTR(out->p); MOE_OPT_PTR(out->aux);
     MOE_OPT_PTR(out->load_max_over_mean); MOE_OPT_PTR(out->select_bias_out);
     MOE_OPT_PTR(out->counts_unbiased); MOE_OPT_PTR(out->slot_expert); MOE_OPT_PTR(out->slot_w);
-    MOE_OPT_PTR(out->offsets); MOE_OPT_PTR(out->perm);
+    MOE_OPT_PTR(out->offsets); MOE_OPT_PTR(out->perm); MOE_OPT_PTR(out->cand_idx);
     if (obs) {
         MOE_OPT_PTR(obs->drop_ratio); MOE_OPT_PTR(obs->gate_entropy);
         MOE_OPT_PTR(obs->bias_mean_abs); MOE_OPT_PTR(obs->bias_max_abs);
@@ -876,6 +876,8 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     int32_t *offsets = out->offsets ? out->offsets : at<int32_t>(ws, L.offsets);
     int32_t *perm = out->perm ? out->perm : at<int32_t>(ws, L.perm);
     int32_t *inv = at<int32_t>(ws, L.inv);
+    int32_t *cand = out->cand_idx && cfg->reroute_rounds > 0 ? out->cand_idx
+                                                             : at<int32_t>(ws, L.cand_idx);
     // Expert outputs: fp32 planes (one per split of the down projection's
     // reduction, added in split order by their readers), routed and shared.
     float *out_sorted = at<float>(ws, L.out_sorted);
@@ -890,7 +892,8 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     cudaEvent_t ev = stage_begin(st);
     if (s.T > 0) {
         rc = run_router(cfg, x, wts->w_r, wts->logit_bias, wts->select_bias, idx, w, nullptr, p,
-                        sbias, want_unb && biased, ws, L, st, obs ? obs->gate_entropy : nullptr);
+                        sbias, want_unb && biased, ws, L, st, obs ? obs->gate_entropy : nullptr,
+                        cand);
         if (rc != MOE_OK) return rc;
     } else if (obs && obs->gate_entropy) {
         MOE_CUDA(cudaMemsetAsync(obs->gate_entropy, 0, sizeof(float), st));
@@ -908,7 +911,7 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
                                       at<int32_t>(ws, L.ec_tok_rows), ndrop, st));
     } else if (cfg->reroute_rounds > 0) {
         float *sw = out->slot_w ? out->slot_w : at<float>(ws, L.slot_w);
-        MOE_CUDA(launch_dispatch_reroute(idx, w, at<int32_t>(ws, L.cand_idx),
+        MOE_CUDA(launch_dispatch_reroute(idx, w, cand,
                                          at<float>(ws, L.cand_w), (int)n_candidates(cfg), s.T,
                                          (int)s.k, (int)s.E, capacity_of(cfg),
                                          cfg->reroute_rounds, reroute_work(ws, L), counts,
@@ -997,6 +1000,15 @@ int moe_device_status(moe_stream_t stream) {
 
 int64_t moe_kernel_launches(void) {
     return __atomic_load_n(&g_kernel_launches, __ATOMIC_RELAXED);
+}
+
+int moe_debug_set_wait_hooks(uint64_t main_loop_limit_ns, int32_t stall_mma) {
+    if (main_loop_limit_ns == 0 || stall_mma < 0 || stall_mma > 1) return MOE_ERR_INVALID_ARG;
+    if (tc::set_wait_hooks(main_loop_limit_ns, stall_mma) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
 
 int moe_kernel_binary_version(int32_t *version) {
