@@ -425,7 +425,7 @@ def run_ours(args, w, T):
     up_tflops = up_flops / (up_ms / 1e3) / 1e12
     up_gbs = up_bytes / (up_ms / 1e3) / 1e9
     recs = [r for r in traffic_record("gemm_tcgen05.cu") or []
-            if r.get("workload") == w.name and not args.n_experts]
+            if r.get("workload") == w.name and not args.n_experts and not args.d_ff]
     exact = [r for r in recs if r.get("T") == T]
     tr = exact[0] if exact else (recs[-1] if recs else None)
     # The dominant kernel is timed per launch inside short graph replays, a
@@ -522,11 +522,17 @@ def main():
     ap.add_argument("--n-experts", type=int, default=None,
                     help="override the workload's expert count (a reduced case for profiler "
                          "captures; with --T scaled alike it keeps the rows per expert)")
+    ap.add_argument("--d-ff", type=int, default=None,
+                    help="override the routed experts' width (a reduced case for profiler "
+                         "captures of the router and the row kernels, whose work does not "
+                         "depend on it)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     w = mi.workload(args.workload)
     if args.n_experts:
         w = w.with_sizes(n_experts=args.n_experts)
+    if args.d_ff:
+        w = w.with_sizes(d_ff=args.d_ff)
     T = args.T or max(w.tokens)
     if args.impl == "reference":
         run_reference(args, w, T)

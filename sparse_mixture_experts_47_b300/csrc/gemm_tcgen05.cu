@@ -33,6 +33,12 @@
 // MMA's N chosen per tile: a tile holds up to 256 of one expert's rows and
 // its MMA N is that count rounded up to 16, so an expert with 146 rows costs
 // a 160-wide tile instead of two 128-row tiles.
+// GEMM_LOGITS (NT = 0, N = 256): the router's logits x W_r^T over a long
+// reduction cut into chains of equal K ranges (the tensor core's fp32
+// accumulation loses precision along one long chain).  Chain 0 of a tile
+// accumulates into TMEM columns 0-255 (S), every later chain into columns
+// 256-511 (A); after each later chain the epilogue adds A into S in TMEM
+// (tcgen05.ld / st), so S = ((c0 + c1) + c2) + ..., and stores S once.
 // MH = 2 (NT = 0, N = 256): tiles of 256 token rows, two M = 128 MMAs per
 // K step sharing the weight tile, so a 64 KB stage feeds twice the MMA work
 // of a 48 KB one; the 256 x 256 fp32 accumulator fills TMEM, so there is one
@@ -55,8 +61,14 @@ constexpr int WROWS = 128;           // weight rows of one TMA box
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 256;        // columns of one of the two accumulators
 constexpr int kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KB)
-constexpr int kSmemExtra =
-    1024 /* alignment slack */ + 256 /* barriers */ + 4096 /* epilogue staging */;
+constexpr int kSmemBase = 1024 /* alignment slack */ + 256 /* barriers */;
+// Epilogue staging per CTA (4 epilogue warps).  Swapped geometries: a
+// [16 tokens][32 features] bf16 block per warp.  NT = 0 fp32 outputs: a
+// [32 rows][32 columns] fp32 block per warp, rows kEpiRowStride floats apart
+// (16-byte aligned rows; a quarter-warp's float4 accesses hit distinct banks).
+constexpr int kEpiRowStride = 36;
+constexpr int kEpiSwapBytes = 4 * 16 * 32 * 2;
+constexpr int kEpiF32Bytes = 4 * 32 * kEpiRowStride * 4;
 constexpr int kVarRows = 256;        // NT of the per-tile-width geometry
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 
@@ -85,13 +97,16 @@ template <int MODE, int NT, int BN, int MH> struct Geo {
     static constexpr int ACT_BYTES = ROWS * BK * 2;
     static constexpr int W_BYTES = SWAP ? WT * WROWS * BK * 2 : BN * BK * 2;
     static constexpr int STAGE_BYTES = ACT_BYTES + W_BYTES;
-    static constexpr int FIT = (kSmemLimit - kSmemExtra) / STAGE_BYTES;
+    static constexpr int EPI =
+        SWAP ? kEpiSwapBytes : ((MODE == GEMM_DOWN || MODE == GEMM_LOGITS) ? kEpiF32Bytes : 0);
+    static constexpr int EXTRA = kSmemBase + EPI;
+    static constexpr int FIT = (kSmemLimit - EXTRA) / STAGE_BYTES;
     static constexpr int STAGES =
         SWAP ? (FIT < 8 ? FIT : 8) : MH == 2 ? 3 : (BN == BNM ? 4 : 6);
     static constexpr int NACC = MH == 2 ? 1 : 2;                 // accumulator buffers
     // output columns (features) of one tile
     static constexpr int OUTC = SWAP ? WROWS : (MODE == GEMM_UP_SWIGLU ? BN / 2 : BN);
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + kSmemExtra;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EXTRA;
 };
 
 struct Args {
@@ -107,6 +122,7 @@ struct Args {
     const int32_t *tile_e, *tile_start, *n_mtiles, *offsets;
     void *C;
     int ldc;
+    int chain_kb;      // GEMM_LOGITS: K blocks per chain (a split holds whole chains)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -197,6 +213,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 32 TMEM lanes x 16 consecutive 32-bit columns; thread i writes lane base+i.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32"
+        " [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+          "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+          "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+          "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+          "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+          "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes in 8-row (1024-byte) atoms.  Fields: start address >> 4 (bits
@@ -222,8 +254,12 @@ struct TileCoord {
 
 // Work item L -> (split, expert, row tile, output-column tile, K-block
 // range).  Splits are outermost so that the CTAs in flight work on the same K
-// slice.  ROWS = activation rows per tile, OUTC = output columns per tile.
-template <int ROWS, int OUTC>
+// slice.  Inside an expert, output-column tiles are outer and row tiles inner
+// (the CTAs in flight share a weight tile); with ROWS_OUTER the other way
+// round (they share the activation rows: the router's logits, whose split
+// spans all of x's columns and whose weights stay in L2).  ROWS = activation
+// rows per tile, OUTC = output columns per tile.
+template <int ROWS, int OUTC, bool ROWS_OUTER = false>
 __device__ __forceinline__ TileCoord decode_tile(const Args &g, int L, int tiles, int nk) {
     const int split = L / tiles;
     L -= split * tiles;
@@ -232,7 +268,8 @@ __device__ __forceinline__ TileCoord decode_tile(const Args &g, int L, int tiles
     const int st = g.tile_start[e];
     const int mt_e = g.tile_start[e + 1] - st;
     const int local = L - st * g.n_ntiles;
-    const int nt = local / mt_e, mt = local - nt * mt_e;
+    const int nt = ROWS_OUTER ? local % g.n_ntiles : local / mt_e;
+    const int mt = ROWS_OUTER ? local / g.n_ntiles : local - nt * mt_e;
     TileCoord c;
     c.e = e;
     c.m0 = g.offsets[e] + mt * ROWS;
@@ -325,7 +362,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t issued_par = 0;   // bit s: phase parity of stage s's last load
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
-            const TileCoord c = decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk);
+            const TileCoord c = decode_tile<G::ROWS, G::OUTC, MODE == GEMM_LOGITS>(g, L, tiles, nk);
             int b0, b1;
             if (G::SWAP) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
             else if (MODE == GEMM_UP_SWIGLU) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
@@ -388,47 +425,85 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         // test hook: done_bar's first phase completes only at the commit
         // below, so this wait can only run out
         if (g_stall_mma && !mbar_wait(done_bar, 0, abort_flag)) ok = false;
-        for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
-            // The K range depends on the split alone; only the per-tile
-            // width (NT = 256) needs the tile table here.
-            const int kb0 = (L / tiles) * g.kb_per_split;
-            const int kb1 = min(nk, kb0 + g.kb_per_split);
-            uint32_t idesc = idesc_fixed;
-            if (G::VARN)
-                idesc = idesc_bf16(
-                    WROWS, tile_n16<G::ROWS>(decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk)));
-            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t sa = smem_u32(smem + stage * G::STAGE_BYTES);
-                const uint32_t sb = sa + G::ACT_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
-                    if (G::SWAP) {
-                        // weights (M side) x tokens (N side)
-                        tc_mma(d_tmem, desc_sw128(sb + kk * 32), desc_sw128(sa + kk * 32), idesc,
-                               accum);
-                        if (MODE == GEMM_UP_SWIGLU)
-                            tc_mma(d_tmem + NT, desc_sw128(sb + WROWS * BK * 2 + kk * 32),
-                                   desc_sw128(sa + kk * 32), idesc, accum);
-                    } else {
-                        tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
-                               accum);
-                        if (MH == 2)    // rows 128..255 of the tile into columns 256..511
-                            tc_mma(d_tmem + BN, desc_sw128(sa + BM * BK * 2 + kk * 32),
-                                   desc_sw128(sb + kk * 32), idesc, accum);
+        if constexpr (MODE == GEMM_LOGITS) {
+            // a work item is a tile and a split of whole chains; chain 0 of
+            // an item into S (columns 0-255), later chains into A (256-511);
+            // sp, ap: uses of S and A so far (wait parities)
+            uint32_t sp = 0, ap = 0;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                const int kbs = (L / tiles) * g.kb_per_split;
+                const int kbe = min(nk, kbs + g.kb_per_split);
+                const int nch = (kbe - kbs + g.chain_kb - 1) / g.chain_kb;
+                for (int ch = 0; ch < nch; ++ch) {
+                    const int slot = ch == 0 ? 0 : 1;
+                    if (!mbar_wait(tempty0 + 8 * slot, (slot ? ap : sp) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    if (slot) ap ^= 1; else sp ^= 1;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + slot * ACC_COLS;
+                    const int kb0 = kbs + ch * g.chain_kb, kb1 = min(kbe, kb0 + g.chain_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(smem + stage * G::STAGE_BYTES);
+                        const uint32_t sb = sa + G::ACT_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32),
+                                   idesc_fixed, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        tc_commit(empty0 + 8 * stage);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    // A's commit also covers chain 0's MMAs into S
+                    if (slot || nch == 1) tc_commit(tfull0 + 8 * slot);
                 }
-                tc_commit(empty0 + 8 * stage);
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
-            if (!ok) break;
-            tc_commit(tfull0 + 8 * acc);
-            if (++acc == G::NACC) { acc = 0; acc_phase ^= 1; }
+        } else {
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                // The K range depends on the split alone; only the per-tile
+                // width (NT = 256) needs the tile table here.
+                const int kb0 = (L / tiles) * g.kb_per_split;
+                const int kb1 = min(nk, kb0 + g.kb_per_split);
+                uint32_t idesc = idesc_fixed;
+                if (G::VARN)
+                    idesc = idesc_bf16(
+                        WROWS, tile_n16<G::ROWS>(decode_tile<G::ROWS, G::OUTC, MODE == GEMM_LOGITS>(g, L, tiles, nk)));
+                if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * G::STAGE_BYTES);
+                    const uint32_t sb = sa + G::ACT_BYTES;
+    #pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+                        if (G::SWAP) {
+                            // weights (M side) x tokens (N side)
+                            tc_mma(d_tmem, desc_sw128(sb + kk * 32), desc_sw128(sa + kk * 32), idesc,
+                                   accum);
+                            if (MODE == GEMM_UP_SWIGLU)
+                                tc_mma(d_tmem + NT, desc_sw128(sb + WROWS * BK * 2 + kk * 32),
+                                       desc_sw128(sa + kk * 32), idesc, accum);
+                        } else {
+                            tc_mma(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), idesc,
+                                   accum);
+                            if (MH == 2)    // rows 128..255 of the tile into columns 256..511
+                                tc_mma(d_tmem + BN, desc_sw128(sa + BM * BK * 2 + kk * 32),
+                                       desc_sw128(sb + kk * 32), idesc, accum);
+                        }
+                    }
+                    tc_commit(empty0 + 8 * stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit(tfull0 + 8 * acc);
+                if (++acc == G::NACC) { acc = 0; acc_phase ^= 1; }
+            }
         }
         // All MMAs of this thread complete before TMEM can be freed.
         tc_commit(done_bar);
@@ -438,136 +513,217 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
         const int quarter = warp - 4;                     // TMEM lanes 32*quarter..
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int L = blockIdx.x; L < total; L += gridDim.x) {
-            const TileCoord c = decode_tile<G::ROWS, G::OUTC>(g, L, tiles, nk);
-            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
-            tc_fence_after();
-            const uint32_t tbase0 =
-                tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
-            if (G::SWAP) {
-                const uint32_t tbase = tbase0;
-                // TMEM lane = output feature f, column = token row m0 + j.
-                const int f = c.n0 + quarter * 32 + lane;
-                const bool vf = f < g.N;
-                const bool raw = MODE == GEMM_DOWN || g.k_splits > 1;
-                // bf16 results (the activation h) leave through shared
-                // memory: lane = feature in, 16-byte vectors of 8 features of
-                // one token out
-                const bool bf16_out = !raw;
-                const int ncols = G::VARN ? tile_n16<G::ROWS>(c) : NT;
-                float *P = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
-                __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
-                __nv_bfloat16 *stg = epi_stage + quarter * (16 * 32);
-#pragma unroll 1
-                for (int j0 = 0; j0 < ncols; j0 += 16) {
-                    float a[16], b[16];
-                    tmem_ld16(tbase + j0, a);
-                    if (MODE == GEMM_UP_SWIGLU) tmem_ld16(tbase + NT + j0, b);
-                    tmem_ld_wait();
-                    if (bf16_out) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float v;
-                            if (MODE == GEMM_UP_SWIGLU) v = silu(a[i]) * b[i];
-                            else v = fmaxf(a[i], 0.f);
-                            stg[i * 32 + lane] = __float2bfloat16_rn(v);
-                        }
-                        __syncwarp();
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int vi = lane + 32 * q, i = vi >> 2, part = vi & 3;
-                            const int row = c.m0 + j0 + i;
-                            const int fc = c.n0 + quarter * 32 + 8 * part;
-                            if (row < c.mend && fc < g.N)
-                                *reinterpret_cast<uint4 *>(H + (size_t)row * g.ldc + fc) =
-                                    *reinterpret_cast<const uint4 *>(stg + i * 32 + 8 * part);
-                        }
-                        __syncwarp();
-                        continue;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int row = c.m0 + j0 + i;
-                        if (!vf || row >= c.mend) continue;
-                        if (raw) {
-                            float *dst = P + (size_t)row * g.ldc + f;
-                            dst[0] = a[i];
-                            if (MODE == GEMM_UP_SWIGLU) dst[g.N] = b[i];
-                        } else if (MODE == GEMM_UP_SWIGLU) {
-                            H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(silu(a[i]) * b[i]);
-                        } else {
-                            H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(fmaxf(a[i], 0.f));
-                        }
-                    }
+        if constexpr (MODE == GEMM_LOGITS) {
+            uint32_t sf = 0, af = 0;   // fills of S and A seen so far (wait parities)
+            float *stg = reinterpret_cast<float *>(epi_stage) + quarter * (32 * kEpiRowStride);
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                const TileCoord c = decode_tile<G::ROWS, G::OUTC, MODE == GEMM_LOGITS>(g, L, tiles, nk);
+                const int nch = (c.kb1 - c.kb0 + g.chain_kb - 1) / g.chain_kb;
+                float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
+                const uint32_t tS = tmem_base + ((uint32_t)(quarter * 32) << 16);
+                const uint32_t tA = tS + ACC_COLS;
+                if (nch == 1) {
+                    if (!mbar_wait(tfull0, sf, abort_flag)) break;
+                    sf ^= 1;
+                    tc_fence_after();
                 }
-            } else {
-#pragma unroll 1
-              for (int hh = 0; hh < MH; ++hh) {    // 128-row halves (MH = 2)
-                const int row = c.m0 + hh * BM + quarter * 32 + lane;
-                const bool vrow = row < c.mend;
-                const uint32_t tbase = tbase0 + hh * BN;
-                if (MODE == GEMM_UP_SWIGLU) {
-                    __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
-#pragma unroll 1
-                    for (int cc = 0; cc < BN / 2; cc += 16) {
-                        float gt[16], up[16];
-                        tmem_ld16(tbase + cc, gt);
-                        tmem_ld16(tbase + BN / 2 + cc, up);
-                        tmem_ld_wait();
-                        float h[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) h[i] = silu(gt[i]) * up[i];
-                        const int col = c.n0 + cc;
-                        if (vrow) {
-                            __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
-                            if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(h);
-                            if (col + 8 < g.N)
-                                *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(h + 8);
-                        }
-                    }
-                } else if (MODE == GEMM_UP_RELU) {
-                    __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+                // S += A after every later chain, in chain order
+                for (int ch = 1; ch < nch; ++ch) {
+                    if (!mbar_wait(tfull0 + 8, af, abort_flag)) { ok = false; break; }
+                    af ^= 1;
+                    tc_fence_after();
 #pragma unroll 1
                     for (int cc = 0; cc < BN; cc += 16) {
-                        float v[16];
-                        tmem_ld16(tbase + cc, v);
+                        float a[16], b[16];
+                        tmem_ld16(tS + cc, a);
+                        tmem_ld16(tA + cc, b);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
-                        const int col = c.n0 + cc;
-                        if (vrow) {
-                            __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
-                            if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
-                            if (col + 8 < g.N)
-                                *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
+                        for (int i = 0; i < 16; ++i) a[i] += b[i];
+                        tmem_st16(tS + cc, a);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty0 + 8);
+                }
+                if (!ok) break;
+                // S out as fp32 row segments through the staging block (as in
+                // the fp32 epilogue of the other modes)
+                const int row0 = c.m0 + quarter * 32;
+#pragma unroll 1
+                for (int cc = 0; cc < BN; cc += 32) {
+                    float v[32];
+                    tmem_ld16(tS + cc, v);
+                    tmem_ld16(tS + cc + 16, v + 16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4 *>(stg + lane * kEpiRowStride + 4 * q) =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    __syncwarp();
+                    const int col = c.n0 + cc + 4 * (lane & 7);
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int r = 4 * it + (lane >> 3);
+                        const float4 q = *reinterpret_cast<const float4 *>(
+                            stg + r * kEpiRowStride + 4 * (lane & 7));
+                        if (row0 + r < c.mend && col < g.N)
+                            *reinterpret_cast<float4 *>(O + (size_t)(row0 + r) * g.ldc + col) = q;
+                    }
+                    __syncwarp();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0);
+            }
+        } else {
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int L = blockIdx.x; L < total; L += gridDim.x) {
+                const TileCoord c = decode_tile<G::ROWS, G::OUTC, MODE == GEMM_LOGITS>(g, L, tiles, nk);
+                if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t tbase0 =
+                    tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+                if (G::SWAP) {
+                    const uint32_t tbase = tbase0;
+                    // TMEM lane = output feature f, column = token row m0 + j.
+                    const int f = c.n0 + quarter * 32 + lane;
+                    const bool vf = f < g.N;
+                    const bool raw = MODE == GEMM_DOWN || g.k_splits > 1;
+                    // bf16 results (the activation h) leave through shared
+                    // memory: lane = feature in, 16-byte vectors of 8 features of
+                    // one token out
+                    const bool bf16_out = !raw;
+                    const int ncols = G::VARN ? tile_n16<G::ROWS>(c) : NT;
+                    float *P = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
+                    __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+                    __nv_bfloat16 *stg = epi_stage + quarter * (16 * 32);
+    #pragma unroll 1
+                    for (int j0 = 0; j0 < ncols; j0 += 16) {
+                        float a[16], b[16];
+                        tmem_ld16(tbase + j0, a);
+                        if (MODE == GEMM_UP_SWIGLU) tmem_ld16(tbase + NT + j0, b);
+                        tmem_ld_wait();
+                        if (bf16_out) {
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                float v;
+                                if (MODE == GEMM_UP_SWIGLU) v = silu(a[i]) * b[i];
+                                else v = fmaxf(a[i], 0.f);
+                                stg[i * 32 + lane] = __float2bfloat16_rn(v);
+                            }
+                            __syncwarp();
+    #pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                const int vi = lane + 32 * q, i = vi >> 2, part = vi & 3;
+                                const int row = c.m0 + j0 + i;
+                                const int fc = c.n0 + quarter * 32 + 8 * part;
+                                if (row < c.mend && fc < g.N)
+                                    *reinterpret_cast<uint4 *>(H + (size_t)row * g.ldc + fc) =
+                                        *reinterpret_cast<const uint4 *>(stg + i * 32 + 8 * part);
+                            }
+                            __syncwarp();
+                            continue;
+                        }
+    #pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int row = c.m0 + j0 + i;
+                            if (!vf || row >= c.mend) continue;
+                            if (raw) {
+                                float *dst = P + (size_t)row * g.ldc + f;
+                                dst[0] = a[i];
+                                if (MODE == GEMM_UP_SWIGLU) dst[g.N] = b[i];
+                            } else if (MODE == GEMM_UP_SWIGLU) {
+                                H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(silu(a[i]) * b[i]);
+                            } else {
+                                H[(size_t)row * g.ldc + f] = __float2bfloat16_rn(fmaxf(a[i], 0.f));
+                            }
                         }
                     }
                 } else {
-                    float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
-#pragma unroll 1
-                    for (int cc = 0; cc < BN; cc += 16) {
-                        float v[16];
-                        tmem_ld16(tbase + cc, v);
-                        tmem_ld_wait();
-                        const int col = c.n0 + cc;
-                        if (vrow) {
-                            float *dst = O + (size_t)row * g.ldc + col;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (col + 4 * q < g.N)
-                                    *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(
-                                        v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    #pragma unroll 1
+                  for (int hh = 0; hh < MH; ++hh) {    // 128-row halves (MH = 2)
+                    const int row = c.m0 + hh * BM + quarter * 32 + lane;
+                    const bool vrow = row < c.mend;
+                    const uint32_t tbase = tbase0 + hh * BN;
+                    if (MODE == GEMM_UP_SWIGLU) {
+                        __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+    #pragma unroll 1
+                        for (int cc = 0; cc < BN / 2; cc += 16) {
+                            float gt[16], up[16];
+                            tmem_ld16(tbase + cc, gt);
+                            tmem_ld16(tbase + BN / 2 + cc, up);
+                            tmem_ld_wait();
+                            float h[16];
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) h[i] = silu(gt[i]) * up[i];
+                            const int col = c.n0 + cc;
+                            if (vrow) {
+                                __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                                if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(h);
+                                if (col + 8 < g.N)
+                                    *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(h + 8);
+                            }
+                        }
+                    } else if (MODE == GEMM_UP_RELU) {
+                        __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+    #pragma unroll 1
+                        for (int cc = 0; cc < BN; cc += 16) {
+                            float v[16];
+                            tmem_ld16(tbase + cc, v);
+                            tmem_ld_wait();
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
+                            const int col = c.n0 + cc;
+                            if (vrow) {
+                                __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                                if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
+                                if (col + 8 < g.N)
+                                    *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
+                            }
+                        }
+                    } else {
+                        // fp32 outputs: each warp stages a 32-row x 32-column block
+                        // (lane = row) in shared memory, then stores it as 128-byte
+                        // row segments (8 lanes per row, 4 rows per instruction)
+                        float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
+                        float *stg = reinterpret_cast<float *>(epi_stage) +
+                                     quarter * (32 * kEpiRowStride);
+                        const int row0 = c.m0 + hh * BM + quarter * 32;
+    #pragma unroll 1
+                        for (int cc = 0; cc < BN; cc += 32) {
+                            float v[32];
+                            tmem_ld16(tbase + cc, v);
+                            tmem_ld16(tbase + cc + 16, v + 16);
+                            tmem_ld_wait();
+    #pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                *reinterpret_cast<float4 *>(stg + lane * kEpiRowStride + 4 * q) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            __syncwarp();
+                            const int col = c.n0 + cc + 4 * (lane & 7);
+    #pragma unroll
+                            for (int it = 0; it < 8; ++it) {
+                                const int r = 4 * it + (lane >> 3);
+                                const float4 q = *reinterpret_cast<const float4 *>(
+                                    stg + r * kEpiRowStride + 4 * (lane & 7));
+                                if (row0 + r < c.mend && col < g.N)
+                                    *reinterpret_cast<float4 *>(O + (size_t)(row0 + r) * g.ldc + col) = q;
+                            }
+                            __syncwarp();
                         }
                     }
+                  }
                 }
-              }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+                if (++acc == G::NACC) { acc = 0; acc_phase ^= 1; }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-            if (++acc == G::NACC) { acc = 0; acc_phase ^= 1; }
+    
         }
     }
 
@@ -680,23 +836,31 @@ static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args
 // always (row-major [rows, ldc]); the up modes only with nt > 0, writing the
 // pre-activation sums (SwiGLU: W1 part at column f, W3 part at N + f).
 // k_splits = 1 up modes write the activation in bf16; GEMM_DOWN writes fp32.
+// GEMM_LOGITS (nt = 0, bn = 256, mh = 1): the reduction is cut into chains of
+// chain_kb K blocks, and k_splits splits of whole chains; each split sums its
+// chains on chip in chain order and writes one fp32 plane.
 cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long long a_rows,
                            int a_cols,
                            const void *B0, const void *B1, int E, int b_rows, int N, int K,
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,
                            const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           cudaStream_t st) {
+                           cudaStream_t st, int chain_kb) {
     using namespace tc;
     if (a_rows == 0) return cudaSuccess;
     const int nk = (K + BK - 1) / BK;
     if (nt != 0 && nt != 16 && nt != 32 && nt != 64 && nt != kVarRows) return cudaErrorInvalidValue;
     if (bn != BNM && bn != BNM / 2) return cudaErrorInvalidValue;
     if (mh != 1 && (mh != 2 || nt != 0 || bn != BNM)) return cudaErrorInvalidValue;
-    if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN && nt == 0) ||
+    if (mode == GEMM_LOGITS && (nt != 0 || bn != BNM || mh != 1 || chain_kb < 1))
+        return cudaErrorInvalidValue;
+    if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN && mode != GEMM_LOGITS && nt == 0) ||
         (a_k_period % BK != 0 && a_k_period != K))
         return cudaErrorInvalidValue;
-    const int kbps = (nk + k_splits - 1) / k_splits;
+    // GEMM_LOGITS: a split holds whole chains of chain_kb K blocks
+    const int chains = mode == GEMM_LOGITS ? (nk + chain_kb - 1) / chain_kb : nk;
+    const int unit = mode == GEMM_LOGITS ? chain_kb : 1;
+    const int kbps = (chains + k_splits - 1) / k_splits * unit;
     k_splits = (nk + kbps - 1) / kbps;          // every split gets at least one K block
     const bool var = nt == kVarRows;
     if (var && mode != GEMM_DOWN) return cudaErrorInvalidValue;
@@ -729,8 +893,10 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
     g.offsets = offsets;
     g.C = C;
     g.ldc = ldc;
+    g.chain_kb = chain_kb;
     if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, mh, m, g, st);
     if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, mh, m, g, st);
+    if (mode == GEMM_LOGITS) return launch_geo<GEMM_LOGITS, 0, BNM>(m, g, st);
     return launch_mode<GEMM_DOWN>(nt, bn, mh, m, g, st);
 }
 

@@ -23,11 +23,19 @@ struct RouterArgs {
 };
 
 // router.cu
-// E <= 32: the logits are computed in slices of kRouterSlice columns of d,
-// written as partial planes [slices][T][E] (caller's buffer) and added in
-// slice order by the softmax kernel.
+// E <= 32: the logits are computed in slices of d, written as partial planes
+// [slices][T][E] (caller's buffer) and added in slice order by the softmax
+// kernel.  E <= 8: a slice is 32 lanes x one 16-byte vector of x (256 bf16
+// or 128 fp32 columns), its W_r columns held in registers; 8 < E <= 32:
+// kRouterSlice columns, its W_r columns staged in shared memory.
 constexpr int kRouterSlice = 512;
-inline int router_slices(int d) { return (d + kRouterSlice - 1) / kRouterSlice; }
+inline int router_slice_cols(int E, int dtype) {
+    return E <= 8 ? 32 * (dtype == MOE_DTYPE_BF16 ? 8 : 4) : kRouterSlice;
+}
+inline int router_slices(int d, int E, int dtype) {
+    const int c = router_slice_cols(E, dtype);
+    return (d + c - 1) / c;
+}
 int router_blocks(int T, int E, int dtype);
 size_t router_smem_bytes(int E, int dtype);
 cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStream_t st);
@@ -137,7 +145,10 @@ inline long long max_tiles(long long rows, int E, int BM) { return (rows + BM - 
 
 // ffn_simt.cu: SIMT grouped GEMM (fp32 accumulate) for the fp32 workloads.
 constexpr int kSimtBM = 64, kSimtBN = 64;
-enum { GEMM_UP_SWIGLU = 0, GEMM_UP_RELU = 1, GEMM_DOWN = 2 };
+// GEMM_LOGITS: fp32 C = A B^T over K in chains of chain_kb K blocks, each
+// split of whole chains summed on chip in chain order into its own plane (the
+// tensor-core router).
+enum { GEMM_UP_SWIGLU = 0, GEMM_UP_RELU = 1, GEMM_DOWN = 2, GEMM_LOGITS = 3 };
 struct GroupedGemmArgs {
     const void *A;               // rows of A: [rows, K] (K contiguous)
     const int32_t *a_gather;     // NULL, or A row of sorted row s = a_gather[s] / gather_k
@@ -160,7 +171,7 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
                            int a_k_period, int k_splits, long long split_stride,
                            const int32_t *tile_e, const int32_t *tile_start,
                            const int32_t *n_mtiles, const int32_t *offsets, void *C, int ldc,
-                           cudaStream_t st);
+                           cudaStream_t st, int chain_kb = 0);
 namespace tc {
 // Test hooks of the grouped GEMM's bounded waits on the current device: the
 // main-loop wait limit in ns and a stall of the MMA issuer (see

@@ -79,21 +79,32 @@ Sizes sizes(const moe_config *c) {
 // core's fp32 accumulation loses a little with every step of a long chain
 // (measured on B300: logit error up to 1.3e-4 over one 192-block chain, 1e-5
 // over chains of about 20 blocks, where the fp32 CUDA-core router reaches
-// 1.4e-5), so the reduction is cut into S chains of at most 16 K blocks, each
-// written as an fp32 partial plane and summed in fixed order.  S depends on
-// d only, so a token's logits do not depend on the batch it comes in (batch
-// invariance).
+// 1.4e-5), so the reduction is cut into S chains of at most 16 K blocks.
+// Groups of 4 chains are summed on chip in chain order (GEMM_LOGITS), each
+// group into its own fp32 plane, and the softmax adds the planes in group
+// order.  Chains and groups depend on d only, so a token's logits do not
+// depend on the batch it comes in (batch invariance).
 bool tc_router(const moe_config *c) {
     return c->dtype == MOE_DTYPE_BF16 && c->n_experts > 32 && c->n_experts % 4 == 0;
 }
 long long router_dp(const moe_config *c) { return (c->d_model + 63) / 64 * 64; }
 constexpr int kRouterChainBlocks = 16;
 constexpr int kRouterParts = 2;
-int router_splits(const moe_config *c) {
+constexpr int kRouterGroupChains = 4;
+// Chains: S equal K ranges of at most kRouterChainBlocks K blocks.
+int router_chain_kb(const moe_config *c) {
     const long long nk = kRouterParts * router_dp(c) / 64;
     const long long S = (nk + kRouterChainBlocks - 1) / kRouterChainBlocks;
-    const long long kbps = (nk + S - 1) / S;
-    return (int)((nk + kbps - 1) / kbps);
+    return (int)((nk + S - 1) / S);
+}
+// Groups of up to kRouterGroupChains consecutive chains: one work item per
+// group and tile, one fp32 plane per group (summed in group order by the
+// softmax).  Both depend on d only.
+int router_groups(const moe_config *c) {
+    const long long nk = kRouterParts * router_dp(c) / 64;
+    const long long kb = router_chain_kb(c);
+    const long long chains = (nk + kb - 1) / kb;
+    return (int)((chains + kRouterGroupChains - 1) / kRouterGroupChains);
 }
 // How the grouped GEMMs of one expert FFN run.  nt = 0: 128 token rows per
 // tile on the MMA's M side.  nt = 16/32/64: weights on the M side and nt
@@ -235,7 +246,7 @@ Layout layout(const moe_config *c) {
     const bool rt = tc_router(c);
     L.rt_wsplit = take(rt ? 2 * s.E * kRouterParts * router_dp(c) : 0);
     const long long planes =
-        rt ? router_splits(c) : (s.E <= 32 ? router_slices((int)s.d) : 0);
+        rt ? router_groups(c) : (s.E <= 32 ? router_slices((int)s.d, (int)s.E, c->dtype) : 0);
     L.rt_logits = take(sizeof(float) * planes * s.T * s.E);
     L.rt_offsets = take(sizeof(int32_t) * 2);
     L.rt_tile_e = take(sizeof(int32_t) * max_tiles(s.T, 1, kTcBM));
@@ -378,7 +389,7 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
     a.cand_w = at<float>(ws, L.cand_w);
     if (tc_router(c)) {
         const int dp = (int)router_dp(c);
-        const int S = router_splits(c);
+        const int G = router_groups(c);
         __nv_bfloat16 *wsplit = at<__nv_bfloat16>(ws, L.rt_wsplit);
         float *part = at<float>(ws, L.rt_logits);
         int32_t *off = at<int32_t>(ws, L.rt_offsets);
@@ -389,11 +400,12 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         note_launch();
         MOE_CUDA(cudaGetLastError());
         MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
-        MOE_CUDA(launch_tc_gemm(GEMM_DOWN, 0, 256, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E, a.E,
-                                kRouterParts * dp,
-                                dp, S, s.T * s.E, te, ts, nt, off, part, a.E, st));
-        // the softmax kernel adds the S chain planes in plane order as it reads them
-        MOE_CUDA(launch_router_from_logits(a, part, S, st));
+        // chains of router_chain_kb K blocks summed on chip in chain order,
+        // one plane per group of chains; the softmax adds the G planes in order
+        MOE_CUDA(launch_tc_gemm(GEMM_LOGITS, 0, 256, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E,
+                                a.E, kRouterParts * dp, dp, G, s.T * s.E, te, ts, nt, off, part,
+                                a.E, st, router_chain_kb(c)));
+        MOE_CUDA(launch_router_from_logits(a, part, G, st));
     } else {
         MOE_CUDA(launch_router(a, c->dtype, at<float>(ws, L.rt_logits), st));
     }

@@ -28,10 +28,27 @@ namespace moe {
 // holds TPW = 32/EP tokens x EP (padded) experts; lanes split the slice into
 // 16-byte vectors, accumulate all TPW*EP = 32 partial logits, and a
 // reduce-scatter butterfly leaves lane L with the slice's logit of
-// (token L / EP, expert L % EP).  The W_r slice is staged in shared memory.
-// Each token's arithmetic is the same whatever the batch size, so a token's
-// routing does not depend on the batch it comes in.
+// (token L / EP, expert L % EP).  The W_r slice is staged in shared memory
+// once per CTA; the CTAs of a slice then stride over the token groups, so
+// W_r is read from L2 about three times per SM instead of once per 8 x TPW
+// tokens.  Each token's arithmetic is the same whatever the batch size and
+// grid, so a token's routing does not depend on the batch it comes in.
 // --------------------------------------------------------------------------
+// The values of 16 bytes of x, widened to fp32.
+template <typename TX> __device__ __forceinline__ void widen16(const uint4 &u, float *v);
+template <> __device__ __forceinline__ void widen16<float>(const uint4 &u, float *v) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+}
+template <> __device__ __forceinline__ void widen16<__nv_bfloat16>(const uint4 &u, float *v) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 template <typename TX, int EP>
 __global__ void __launch_bounds__(256) router_partial_kernel(RouterArgs a, float *part) {
     constexpr int VN = Vec<TX>::N;
@@ -40,7 +57,6 @@ __global__ void __launch_bounds__(256) router_partial_kernel(RouterArgs a, float
     extern __shared__ __align__(16) float wsm[];   // [EP][DS]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tok0 = (blockIdx.x * 8 + warp) * TPW;
     const int c0 = blockIdx.y * DS, clen = min(DS, a.d - c0);
     const TX *x = static_cast<const TX *>(a.x);
 
@@ -53,65 +69,163 @@ __global__ void __launch_bounds__(256) router_partial_kernel(RouterArgs a, float
     }
     __syncthreads();
 
-    float acc[TPW][EP];
+    // A token group's x (TPW tokens x this lane's NJ 16-byte vectors) is
+    // loaded raw, and the next group's is in flight while this one is used.
+    constexpr int NJ = DS / (32 * VN);
+    const int tok_step = gridDim.x * 8 * TPW;
+    auto load_group = [&](int tk, uint4 (&r)[NJ][TPW]) {
 #pragma unroll
-    for (int t = 0; t < TPW; ++t)
-#pragma unroll
-        for (int e = 0; e < EP; ++e) acc[t][e] = 0.f;
-
-#pragma unroll
-    for (int j = 0; j < DS / (32 * VN); ++j) {
-        const int c = (j * 32 + lane) * VN;
-        if (c < clen) {
-            float xv[TPW][VN];
+        for (int j = 0; j < NJ; ++j)
 #pragma unroll
             for (int t = 0; t < TPW; ++t) {
-                if (tok0 + t < a.T) {
-                    load16_f32(x + (size_t)(tok0 + t) * a.d + c0 + c, xv[t]);
-                } else {
+                const int c = (j * 32 + lane) * VN;
+                r[j][t] = (c < clen && tk + t < a.T)
+                              ? *reinterpret_cast<const uint4 *>(x + (size_t)(tk + t) * a.d + c0 + c)
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+    };
+    uint4 cur[NJ][TPW], nxt[NJ][TPW];
+    int tok0 = (blockIdx.x * 8 + warp) * TPW;
+    if (tok0 < a.T) load_group(tok0, cur);
+#pragma unroll 1
+    for (; tok0 < a.T; tok0 += tok_step) {
+        if (tok0 + tok_step < a.T) load_group(tok0 + tok_step, nxt);
+        float acc[TPW][EP];
 #pragma unroll
-                    for (int i = 0; i < VN; ++i) xv[t][i] = 0.f;
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+            for (int e = 0; e < EP; ++e) acc[t][e] = 0.f;
+
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int c = (j * 32 + lane) * VN;
+            if (c < clen) {
+                float xv[TPW][VN];
+#pragma unroll
+                for (int t = 0; t < TPW; ++t) widen16<TX>(cur[j][t], xv[t]);
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    if (e < a.E) {
+                        float wv[VN];
+#pragma unroll
+                        for (int i = 0; i < VN; i += 4) {
+                            const float4 q = *reinterpret_cast<const float4 *>(wsm + e * DS + c + i);
+                            wv[i] = q.x; wv[i + 1] = q.y; wv[i + 2] = q.z; wv[i + 3] = q.w;
+                        }
+#pragma unroll
+                        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+                            for (int i = 0; i < VN; ++i) acc[t][e] = fmaf(xv[t][i], wv[i], acc[t][e]);
+                    }
                 }
             }
+        }
+
+        // Reduce-scatter: afterwards v[0] of lane L holds the sum over lanes of
+        // the flattened accumulator entry L.
+        float v[32];
+#pragma unroll
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+            for (int e = 0; e < EP; ++e) v[t * EP + e] = acc[t][e];
+#pragma unroll
+        for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < n / 2; ++i) {
+                const float send = up ? v[i] : v[i + n / 2];
+                const float keep = up ? v[i + n / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+        const int ge = lane % EP;
+        const int t = tok0 + lane / EP;
+        if (ge < a.E && t < a.T)
+            part[(size_t)blockIdx.y * a.T * a.E + (size_t)t * a.E + ge] = v[0];
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+#pragma unroll
+            for (int t = 0; t < TPW; ++t) cur[j][t] = nxt[j][t];
+    }
+}
+
+// --------------------------------------------------------------------------
+// E <= 8: the same partial logits with each lane's W_r columns in registers.
+// A slice is 32 lanes x VN columns (one 16-byte vector of x per token and
+// lane); lane l holds W_r[e][c .. c+VN) for all 8 (padded) experts, so the
+// FMAs read no shared memory (staging W_r in shared memory and reading it
+// back for every 4 tokens made the kernel bound by shared-memory bandwidth).
+// A warp takes TPW = 4 tokens at a time, the next 4 tokens' x in flight;
+// per (token, expert) the lane's VN products are summed in column order, the
+// same reduce-scatter butterfly leaves lane L with (token L / 8, expert
+// L % 8), and the softmax kernel adds the slices in order: fixed by d alone.
+// --------------------------------------------------------------------------
+template <typename TX>
+__global__ void __launch_bounds__(256, 2) router_partial_w8_kernel(RouterArgs a, float *part) {
+    constexpr int VN = Vec<TX>::N;
+    constexpr int EP = 8, TPW = 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = (blockIdx.y * 32 + lane) * VN;     // this lane's first column
+    const bool cv = c < a.d;                         // d is a multiple of VN
+    const TX *x = static_cast<const TX *>(a.x);
+
+    float wr[EP][VN];
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+#pragma unroll
+        for (int i = 0; i < VN; i += 4) {
+            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < a.E && cv)
+                q = *reinterpret_cast<const float4 *>(a.w_r + (size_t)e * a.d + c + i);
+            wr[e][i] = q.x; wr[e][i + 1] = q.y; wr[e][i + 2] = q.z; wr[e][i + 3] = q.w;
+        }
+
+    const int tok_step = gridDim.x * 8 * TPW;
+    auto load_group = [&](int tk, uint4 (&r)[TPW]) {
+#pragma unroll
+        for (int t = 0; t < TPW; ++t)
+            r[t] = (cv && tk + t < a.T)
+                       ? *reinterpret_cast<const uint4 *>(x + (size_t)(tk + t) * a.d + c)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    };
+    uint4 cur[TPW], nxt[TPW];
+    int tok0 = (blockIdx.x * 8 + warp) * TPW;
+    if (tok0 < a.T) load_group(tok0, cur);
+#pragma unroll 1
+    for (; tok0 < a.T; tok0 += tok_step) {
+        if (tok0 + tok_step < a.T) load_group(tok0 + tok_step, nxt);
+        float v[32];
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+            float xv[VN];
+            widen16<TX>(cur[t], xv);
 #pragma unroll
             for (int e = 0; e < EP; ++e) {
-                if (e < a.E) {
-                    float wv[VN];
+                float s = 0.f;
 #pragma unroll
-                    for (int i = 0; i < VN; i += 4) {
-                        const float4 q = *reinterpret_cast<const float4 *>(wsm + e * DS + c + i);
-                        wv[i] = q.x; wv[i + 1] = q.y; wv[i + 2] = q.z; wv[i + 3] = q.w;
-                    }
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t)
-#pragma unroll
-                        for (int i = 0; i < VN; ++i) acc[t][e] = fmaf(xv[t][i], wv[i], acc[t][e]);
-                }
+                for (int i = 0; i < VN; ++i) s = fmaf(xv[i], wr[e][i], s);
+                v[t * EP + e] = s;
             }
         }
-    }
-
-    // Reduce-scatter: afterwards v[0] of lane L holds the sum over lanes of
-    // the flattened accumulator entry L.
-    float v[32];
+        // Reduce-scatter: afterwards v[0] of lane L holds the sum over lanes
+        // of the flattened entry L.
 #pragma unroll
-    for (int t = 0; t < TPW; ++t)
+        for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+            const bool up = (lane & off) != 0;
 #pragma unroll
-        for (int e = 0; e < EP; ++e) v[t * EP + e] = acc[t][e];
-#pragma unroll
-    for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
-        const bool up = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-            const float send = up ? v[i] : v[i + n / 2];
-            const float keep = up ? v[i + n / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            for (int i = 0; i < n / 2; ++i) {
+                const float send = up ? v[i] : v[i + n / 2];
+                const float keep = up ? v[i + n / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
         }
+        const int ge = lane % EP;
+        const int t = tok0 + lane / EP;
+        if (ge < a.E && t < a.T)
+            part[(size_t)blockIdx.y * a.T * a.E + (size_t)t * a.E + ge] = v[0];
+#pragma unroll
+        for (int t2 = 0; t2 < TPW; ++t2) cur[t2] = nxt[t2];
     }
-    const int ge = lane % EP;
-    const int t = tok0 + lane / EP;
-    if (ge < a.E && t < a.T)
-        part[(size_t)blockIdx.y * a.T * a.E + (size_t)t * a.E + ge] = v[0];
 }
 
 // --------------------------------------------------------------------------
@@ -742,6 +856,30 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const float *probs, co
 // --------------------------------------------------------------------------
 // Host launchers
 // --------------------------------------------------------------------------
+// Grid of the partial-logit kernels: about `per_sm` resident CTAs per SM
+// over all slices, each striding over the token groups of its slice.
+static dim3 partial_grid(const void *kern, size_t smem, int S, int tok_per_cta, int T) {
+    int dev = 0, sms = 148, per_sm = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int groups = (T + tok_per_cta - 1) / tok_per_cta;
+    return dim3(std::max(1, std::min(groups, (sms * per_sm + S - 1) / S)), S);
+}
+
+template <typename TX>
+static cudaError_t launch_partial_w8(const RouterArgs &a, float *part, cudaStream_t st) {
+    auto kern = router_partial_w8_kernel<TX>;
+    const int dtype = sizeof(TX) == 2 ? MOE_DTYPE_BF16 : MOE_DTYPE_FP32;
+    const dim3 grid = partial_grid(reinterpret_cast<const void *>(kern), 0,
+                                   router_slices(a.d, a.E, dtype), 8 * 4, a.T);
+    kern<<<grid, 256, 0, st>>>(a, part);
+    note_launch();
+    return cudaGetLastError();
+}
+
 template <typename TX, int EP>
 static cudaError_t launch_partial(const RouterArgs &a, float *part, cudaStream_t st) {
     constexpr int TPW = 32 / EP;
@@ -749,8 +887,9 @@ static cudaError_t launch_partial(const RouterArgs &a, float *part, cudaStream_t
     auto kern = router_partial_kernel<TX, EP>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    const int tok_per_cta = 8 * TPW;
-    dim3 grid((a.T + tok_per_cta - 1) / tok_per_cta, router_slices(a.d));
+    const int dtype = sizeof(TX) == 2 ? MOE_DTYPE_BF16 : MOE_DTYPE_FP32;
+    const dim3 grid = partial_grid(reinterpret_cast<const void *>(kern), smem,
+                                   router_slices(a.d, a.E, dtype), 8 * TPW, a.T);
     kern<<<grid, 256, smem, st>>>(a, part);
     note_launch();
     return cudaGetLastError();
@@ -792,11 +931,11 @@ size_t router_smem_bytes(int E, int dtype) {
 template <typename TX>
 static cudaError_t launch_router_t(const RouterArgs &a, float *part, cudaStream_t st) {
     if (a.E <= 32) {
-        cudaError_t err = a.E <= 8    ? launch_partial<TX, 8>(a, part, st)
+        cudaError_t err = a.E <= 8    ? launch_partial_w8<TX>(a, part, st)
                           : a.E <= 16 ? launch_partial<TX, 16>(a, part, st)
                                       : launch_partial<TX, 32>(a, part, st);
         if (err != cudaSuccess) return err;
-        const int S = router_slices(a.d);
+        const int S = router_slices(a.d, a.E, sizeof(TX) == 2 ? MOE_DTYPE_BF16 : MOE_DTYPE_FP32);
         return a.E <= 8    ? launch_small_epilogue<8>(a, part, S, st)
                : a.E <= 16 ? launch_small_epilogue<16>(a, part, S, st)
                            : launch_small_epilogue<32>(a, part, S, st);
