@@ -64,11 +64,8 @@ constexpr int kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KB)
 constexpr int kSmemBase = 1024 /* alignment slack */ + 256 /* barriers */;
 // Epilogue staging per CTA (4 epilogue warps).  Swapped geometries: a
 // [16 tokens][32 features] bf16 block per warp.  NT = 0 fp32 outputs: a
-// [32 rows][32 columns] fp32 block per warp, rows kEpiRowStride floats apart
-// (16-byte aligned rows; a quarter-warp's float4 accesses hit distinct banks).
-constexpr int kEpiRowStride = 36;
+// [32 rows][32 or 16 columns] fp32 block per warp (Geo::EPI_COLS).
 constexpr int kEpiSwapBytes = 4 * 16 * 32 * 2;
-constexpr int kEpiF32Bytes = 4 * 32 * kEpiRowStride * 4;
 constexpr int kVarRows = 256;        // NT of the per-tile-width geometry
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 
@@ -97,8 +94,14 @@ template <int MODE, int NT, int BN, int MH> struct Geo {
     static constexpr int ACT_BYTES = ROWS * BK * 2;
     static constexpr int W_BYTES = SWAP ? WT * WROWS * BK * 2 : BN * BK * 2;
     static constexpr int STAGE_BYTES = ACT_BYTES + W_BYTES;
+    // fp32 epilogue staging: [32 rows][EPI_COLS] per warp, rows EPI_STRIDE
+    // floats apart (16-byte aligned; a quarter-warp's float4 writes hit
+    // distinct banks)
+    static constexpr int EPI_COLS = 32;
+    static constexpr int EPI_STRIDE = EPI_COLS + 4;
     static constexpr int EPI =
-        SWAP ? kEpiSwapBytes : ((MODE == GEMM_DOWN || MODE == GEMM_LOGITS) ? kEpiF32Bytes : 0);
+        SWAP ? kEpiSwapBytes
+             : ((MODE == GEMM_DOWN || MODE == GEMM_LOGITS) ? 4 * 32 * EPI_STRIDE * 4 : 0);
     static constexpr int EXTRA = kSmemBase + EPI;
     static constexpr int FIT = (kSmemLimit - EXTRA) / STAGE_BYTES;
     static constexpr int STAGES =
@@ -298,6 +301,37 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
         w[i] = *reinterpret_cast<uint32_t *>(&b);
     }
     return u;
+}
+
+// fp32 results of this warp's 32 TMEM lanes (rows row0 .. row0 + 31) and BNT
+// columns from taddr, stored to O [rows, ldc] through the warp's staging
+// block stg [32][EC + 4]: lane = row in, EC/4 lanes per row out, so that a
+// warp store writes whole EC*4-byte row segments of 32/(EC/4) rows.
+template <int EC, int BNT>
+__device__ __forceinline__ void store_f32_rows(uint32_t taddr, float *stg, int lane, float *O,
+                                               int ldc, int row0, int mend, int n0, int N) {
+    constexpr int ES = EC + 4, LPR = EC / 4, RPI = 32 / LPR;
+#pragma unroll 1
+    for (int cc = 0; cc < BNT; cc += EC) {
+        float v[EC];
+#pragma unroll
+        for (int h = 0; h < EC; h += 16) tmem_ld16(taddr + cc + h, v + h);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < EC / 4; ++q)
+            *reinterpret_cast<float4 *>(stg + lane * ES + 4 * q) =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        __syncwarp();
+        const int col = n0 + cc + 4 * (lane % LPR);
+#pragma unroll
+        for (int it = 0; it < 32 / RPI; ++it) {
+            const int r = RPI * it + lane / LPR;
+            const float4 q = *reinterpret_cast<const float4 *>(stg + r * ES + 4 * (lane % LPR));
+            if (row0 + r < mend && col < N)
+                *reinterpret_cast<float4 *>(O + (size_t)(row0 + r) * ldc + col) = q;
+        }
+        __syncwarp();
+    }
 }
 
 template <int MODE, int NT, int BN, int MH>
@@ -515,7 +549,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const int quarter = warp - 4;                     // TMEM lanes 32*quarter..
         if constexpr (MODE == GEMM_LOGITS) {
             uint32_t sf = 0, af = 0;   // fills of S and A seen so far (wait parities)
-            float *stg = reinterpret_cast<float *>(epi_stage) + quarter * (32 * kEpiRowStride);
+            float *stg = reinterpret_cast<float *>(epi_stage) + quarter * (32 * G::EPI_STRIDE);
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
                 const TileCoord c = decode_tile<G::ROWS, G::OUTC, MODE == GEMM_LOGITS>(g, L, tiles, nk);
@@ -549,31 +583,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     if (lane == 0) mbar_arrive(tempty0 + 8);
                 }
                 if (!ok) break;
-                // S out as fp32 row segments through the staging block (as in
-                // the fp32 epilogue of the other modes)
-                const int row0 = c.m0 + quarter * 32;
-#pragma unroll 1
-                for (int cc = 0; cc < BN; cc += 32) {
-                    float v[32];
-                    tmem_ld16(tS + cc, v);
-                    tmem_ld16(tS + cc + 16, v + 16);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<float4 *>(stg + lane * kEpiRowStride + 4 * q) =
-                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    __syncwarp();
-                    const int col = c.n0 + cc + 4 * (lane & 7);
-#pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int r = 4 * it + (lane >> 3);
-                        const float4 q = *reinterpret_cast<const float4 *>(
-                            stg + r * kEpiRowStride + 4 * (lane & 7));
-                        if (row0 + r < c.mend && col < g.N)
-                            *reinterpret_cast<float4 *>(O + (size_t)(row0 + r) * g.ldc + col) = q;
-                    }
-                    __syncwarp();
-                }
+                // S out as fp32 row segments through the staging block
+                store_f32_rows<G::EPI_COLS, BN>(tS, stg, lane, O, g.ldc, c.m0 + quarter * 32,
+                                                c.mend, c.n0, g.N);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty0);
@@ -686,35 +698,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                             }
                         }
                     } else {
-                        // fp32 outputs: each warp stages a 32-row x 32-column block
-                        // (lane = row) in shared memory, then stores it as 128-byte
-                        // row segments (8 lanes per row, 4 rows per instruction)
+                        // fp32 outputs: each warp stores its 32 rows as whole row
+                        // segments through its staging block
                         float *O = static_cast<float *>(g.C) + (size_t)c.split * g.split_stride;
                         float *stg = reinterpret_cast<float *>(epi_stage) +
-                                     quarter * (32 * kEpiRowStride);
-                        const int row0 = c.m0 + hh * BM + quarter * 32;
-    #pragma unroll 1
-                        for (int cc = 0; cc < BN; cc += 32) {
-                            float v[32];
-                            tmem_ld16(tbase + cc, v);
-                            tmem_ld16(tbase + cc + 16, v + 16);
-                            tmem_ld_wait();
-    #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                *reinterpret_cast<float4 *>(stg + lane * kEpiRowStride + 4 * q) =
-                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                            __syncwarp();
-                            const int col = c.n0 + cc + 4 * (lane & 7);
-    #pragma unroll
-                            for (int it = 0; it < 8; ++it) {
-                                const int r = 4 * it + (lane >> 3);
-                                const float4 q = *reinterpret_cast<const float4 *>(
-                                    stg + r * kEpiRowStride + 4 * (lane & 7));
-                                if (row0 + r < c.mend && col < g.N)
-                                    *reinterpret_cast<float4 *>(O + (size_t)(row0 + r) * g.ldc + col) = q;
-                            }
-                            __syncwarp();
-                        }
+                                     quarter * (32 * G::EPI_STRIDE);
+                        store_f32_rows<G::EPI_COLS, BN>(tbase, stg, lane, O, g.ldc,
+                                                        c.m0 + hh * BM + quarter * 32, c.mend,
+                                                        c.n0, g.N);
                     }
                   }
                 }
