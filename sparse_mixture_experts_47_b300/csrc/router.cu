@@ -696,12 +696,7 @@ struct RadixScratch {
     int warp_tot[16];
     int total;
     unsigned sel[2];
-    int part[2][kRadixWarps];   // bisection: per-warp counts, two alternating slots
 };
-
-// Columns of at most 512 * kSelPer values are selected by bisection on the
-// bit pattern with the values in registers (kSelPer per thread).
-constexpr int kSelPer = 32;
 
 // A column of at most kStageMaxT values is copied to shared memory `buf`
 // first (one coalesced pass, all threads of the block); the selection passes
@@ -723,41 +718,13 @@ __device__ const float *stage_col(const float *col, int T, float *buf) {
 }
 inline size_t stage_col_bytes(int T) { return T <= kStageMaxT ? sizeof(float) * T : 0; }
 
-// Value of rank r (0-based, ascending) of col[0..T); 512 threads; values >= 0,
-// so the order of the fp32 bit patterns is the order of the values.
-// T <= 512 * kSelPer: thread tid holds elements tid + 512 j in registers
-// (missing ones 0xffffffff, above every pattern of a value >= 0); for bit b
-// from 30 down to 0 the block counts the values below prefix | 2^b, and if
-// no more than r are below it the rank-r value has bit b set.  One warp
-// reduction and one barrier per bit, no atomics.
-// Longer columns: four passes of 8-bit radix digits with per-warp histograms.
+// Value of rank r (0-based, ascending) of col[0..T); 512 threads.  Four
+// passes of 8 bits over the fp32 bit patterns (values >= 0, so bit order is
+// value order), per-warp histograms.  After the first pass only the values
+// that share the selected prefix are counted, and a warp none of whose values
+// does skips the histogram update.
 __device__ float radix_select_col(const float *col, int T, long long r, RadixScratch &sc) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (T <= 512 * kSelPer) {
-        unsigned v[kSelPer];
-#pragma unroll
-        for (int j = 0; j < kSelPer; ++j) {
-            const int i = tid + 512 * j;
-            v[j] = i < T ? __float_as_uint(col[i]) : 0xffffffffu;
-        }
-        unsigned prefix = 0;
-#pragma unroll 1
-        for (int b = 30; b >= 0; --b) {
-            const unsigned cand = prefix | (1u << b);
-            int cnt = 0;
-#pragma unroll
-            for (int j = 0; j < kSelPer; ++j) cnt += v[j] < cand ? 1 : 0;
-            cnt = __reduce_add_sync(0xffffffffu, cnt);
-            const int slot = b & 1;
-            if (lane == 0) sc.part[slot][warp] = cnt;
-            __syncthreads();
-            long long below = 0;
-#pragma unroll
-            for (int w = 0; w < kRadixWarps; ++w) below += sc.part[slot][w];
-            if (below <= r) prefix = cand;
-        }
-        return __uint_as_float(prefix);
-    }
     unsigned prefix = 0, mask = 0;
     unsigned *my_hist = sc.hist[warp];
     for (int shift = 32 - kRadixDigit; shift >= 0; shift -= kRadixDigit) {
@@ -778,8 +745,9 @@ __device__ float radix_select_col(const float *col, int T, long long r, RadixScr
             for (int q = 0; q < kRadixBatch; ++q) {
                 const int i = i0 + q * blockDim.x;
                 if (i0 - tid + q * (int)blockDim.x >= n) break;     // uniform over the block
-                unsigned bin = 0xffffffffu;
-                if (i < T && (v[q] & mask) == prefix) bin = (v[q] >> shift) & (kRadixBins - 1);
+                const bool match = i < T && (v[q] & mask) == prefix;
+                if (!__any_sync(0xffffffffu, match)) continue;          // uniform over the warp
+                const unsigned bin = match ? (v[q] >> shift) & (kRadixBins - 1) : 0xffffffffu;
                 const unsigned peers = __match_any_sync(0xffffffffu, bin);
                 if (bin != 0xffffffffu && lane == __ffs(peers) - 1)
                     atomicAdd(&my_hist[bin], __popc(peers));
