@@ -308,6 +308,8 @@ def stage_pass(moe, cfg, inp, weights, ws, outs, args, use_graph, dev, reps=None
 
 def run_ours(args, w, T):
     import sparse_mixture_experts_47_b300 as moe
+    if args.pair_tiles:
+        moe.debug_set_pair_tiles(args.pair_tiles)
 
     world, rank, local = dist_setup(args)
     dev = torch.device("cuda", local if world > 1 else 0)
@@ -441,7 +443,9 @@ def run_ours(args, w, T):
     else:
         roof = {"bound": "hbm", "achieved": up_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": up_gbs / peaks["hbm_gbs"], "peak_source": f"{src} hbm_gbs"}
-    roof["kernel"] = "grouped_gemm_tc_kernel (up projection)"
+    plan = moe.ffn_plan(cfg) if w.dtype == "bf16" else {}
+    roof["kernel"] = ("grouped_gemm_pair_kernel (up projection, 256-row tiles on SM pairs)"
+                      if plan.get("up_pair") else "grouped_gemm_tc_kernel (up projection)")
     roof["algorithmic_per_launch"] = {"flops": up_flops, "bytes": up_bytes}
     roof["ms_per_launch"] = up_ms
     roof["traffic"] = None
@@ -526,6 +530,9 @@ def main():
                     help="override the routed experts' width (a reduced case for profiler "
                          "captures of the router and the row kernels, whose work does not "
                          "depend on it)")
+    ap.add_argument("--pair-tiles", type=int, default=0, choices=[-1, 0, 1],
+                    help="the library's switch of the 256-row SM-pair GEMM tiles: 0 its own "
+                         "rule (default), -1 never, 1 wherever the geometry allows")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     w = mi.workload(args.workload)

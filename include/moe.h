@@ -186,12 +186,16 @@ int64_t moe_reroute_candidates(const moe_config *cfg);
  *   down_rows_per_tile  as rows_per_tile for the down projection, or 256:
  *                  up to 256 rows per tile with the MMA N set per tile
  *   down_halves    1, or 2: 256-row down tiles of two M = 128 MMAs
+ *   up_pair, down_pair  1: 256-row tiles on a pair of SMs (a cluster of
+ *                  two CTAs running one M = 256 MMA, cta_group::2); the
+ *                  down projection then reports down_halves = 2
  * Returns MOE_OK, MOE_ERR_INVALID_ARG for an invalid cfg, or
  * MOE_ERR_UNSUPPORTED when the layer does not run on the tensor cores (fp32,
  * or no shared expert for shared = 1); out untouched then. */
 typedef struct {
     int32_t rows_per_tile, up_splits, down_splits, up_n, down_n;
     int32_t down_rows_per_tile, down_halves;
+    int32_t up_pair, down_pair;
 } moe_ffn_plan_info;
 int moe_ffn_plan(const moe_config *cfg, int32_t shared, moe_ffn_plan_info *out);
 
@@ -402,6 +406,14 @@ int64_t moe_kernel_launches(void);
  * flight and restore (2000000000, 0) afterwards.  MOE_ERR_INVALID_ARG for a
  * zero limit or stall_mma outside {0, 1}. */
 int moe_debug_set_wait_hooks(uint64_t main_loop_limit_ns, int32_t stall_mma);
+
+/* Tuning and test switch of the 256-row SM-pair tiles (see
+ * moe_ffn_plan_info.up_pair): 0 (default) the library's rule (experts
+ * averaging at least 512 rows), -1 never (128-row or one-SM 256-row tiles
+ * instead), 1 for every projection that runs token rows on the MMA's M side
+ * (rows_per_tile = 0; its N is then 256).  Host-only; it applies to the calls
+ * planned after it, on every device.  MOE_ERR_INVALID_ARG outside {-1, 0, 1}. */
+int moe_debug_set_pair_tiles(int32_t policy);
 
 /* The architecture the library's kernels were compiled for, as the CUDA
  * runtime reports it for one of them on the current device (binaryVersion:

@@ -113,6 +113,8 @@ def _load():
     L.moe_kernel_binary_version.argtypes = [P]; L.moe_kernel_binary_version.restype = I
     L.moe_debug_set_wait_hooks.argtypes = [ctypes.c_uint64, ctypes.c_int32]
     L.moe_debug_set_wait_hooks.restype = I
+    L.moe_debug_set_pair_tiles.argtypes = [ctypes.c_int32]
+    L.moe_debug_set_pair_tiles.restype = I
     L.moe_stage_timing_enable.argtypes = [I]; L.moe_stage_timing_enable.restype = I
     L.moe_stage_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int64)]
@@ -255,7 +257,7 @@ def dispatch_reroute(cfg: MoEConfig, idx, w, cand_idx, cand_w,
 class _FfnPlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "rows_per_tile", "up_splits", "down_splits", "up_n", "down_n", "down_rows_per_tile",
-        "down_halves")]
+        "down_halves", "up_pair", "down_pair")]
 
 
 def ffn_plan(cfg: MoEConfig, shared: bool = False) -> Dict[str, int]:
@@ -563,6 +565,13 @@ def debug_set_wait_hooks(main_loop_limit_ns: int = 2_000_000_000, stall_mma: boo
     moe_debug_set_wait_hooks); the defaults restore normal operation."""
     _check("moe_debug_set_wait_hooks",
            lib.moe_debug_set_wait_hooks(int(main_loop_limit_ns), int(bool(stall_mma))))
+
+
+def debug_set_pair_tiles(policy: int = 0) -> None:
+    """Switch of the 256-row SM-pair GEMM tiles (see moe_debug_set_pair_tiles):
+    0 the library's rule, -1 never, 1 for every projection with token rows on
+    the MMA's M side."""
+    _check("moe_debug_set_pair_tiles", lib.moe_debug_set_pair_tiles(int(policy)))
 
 
 def stage_timing(on: bool) -> None:

@@ -51,6 +51,8 @@
 
 #include <cuda.h>
 
+#include <algorithm>
+
 namespace moe {
 namespace tc {
 
@@ -727,6 +729,317 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
 }
 
+// ---------------------------------------------------------------- SM-pair tiles
+// Tiles of 256 token rows x 256 MMA columns on a cluster of two CTAs (two
+// SMs) with tcgen05.mma.cta_group::2 (M = 256).  CTA r of the pair stages
+// rows m0 + 128 r .. + 127 of A and the r-th 128-row box of the weight tile
+// (SwiGLU: r = 0 the W1 rows, r = 1 the same W3 rows; otherwise weight rows
+// n0 + 128 r ..), so a stage is 32 KB per SM where the one-SM 128 x 256 tile
+// needs 48 KB, and 6 (down) or 7 (up) stages fit.  The MMA reads each CTA's
+// A rows from that CTA's shared memory and the two B boxes from both, and
+// leaves each CTA's 128 rows x 256 columns in that CTA's TMEM, where the
+// CTA's own epilogue reads them.  Two accumulators of 256 columns: a tile's
+// epilogue overlaps the next tile's MMAs.
+//   rank 0 (even CTA): the MMA issuer for both; its full barriers collect
+//     both CTAs' TMA bytes; its commits arrive on both CTAs' barriers
+//     (multicast); its accumulator-empty barriers count both epilogues.
+//   rank 1: producer and epilogue only.
+template <int MODE> struct PairGeo {
+    static constexpr int A_BYTES = BM * BK * 2;              // 16 KB
+    static constexpr int STAGE_BYTES = A_BYTES + WROWS * BK * 2;   // + 16 KB of weights
+    static constexpr int EPI_COLS = 32;
+    static constexpr int EPI_STRIDE = EPI_COLS + 4;
+    static constexpr int EPI = MODE == GEMM_DOWN ? 4 * 32 * EPI_STRIDE * 4 : 0;
+    static constexpr int EXTRA = kSmemBase + EPI;
+    static constexpr int FIT = (kSmemLimit - EXTRA) / STAGE_BYTES;
+    static constexpr int STAGES = FIT < 8 ? FIT : 8;
+    static constexpr int OUTC = MODE == GEMM_UP_SWIGLU ? BNM / 2 : BNM;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EXTRA;
+};
+constexpr int kPairRows = 2 * BM;
+// After an abort, how long a CTA waits for its own copies in flight: they
+// land within microseconds, and rank 1 cannot observe their completion (it is
+// counted on rank 0's barrier), so it waits this long.
+constexpr uint64_t kPairDrainNs = 20000000ull;   // 20 ms
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of `addr` (a shared::cta address) in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// mbar_wait for a barrier that the other CTA of the pair arrives on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    const uint64_t limit = g_main_wait_limit_ns;
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            flag_error(kErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+// TMA load into this CTA's shared memory, completing on a barrier of either
+// CTA of the pair (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *tm, int c0,
+                                                 int c1, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+// Arrive on the barrier at offset `bar` in both CTAs of the pair once this
+// thread's MMAs have completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"((uint16_t)3) : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB0,
+                         const __grid_constant__ CUtensorMap tmB1, Args g) {
+    using P = PairGeo<MODE>;
+    constexpr int STAGES = P::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * P::STAGE_BYTES);
+    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done[1]
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *epi_stage = reinterpret_cast<float *>(smem + STAGES * P::STAGE_BYTES + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);       // rank 0's arrive.expect_tx of both CTAs' bytes
+            mbar_init(empty0 + 8 * s, 1);      // rank 0's commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);      // rank 0's commit
+            mbar_init(tempty0 + 8 * a, 8);     // 4 epilogue warps of each CTA
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 2) {
+        // one warp of each CTA allocates, collectively, the same columns in both
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();      // both CTAs' barriers are initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int tiles = (*g.n_mtiles) * g.n_ntiles;
+    const int nk = (g.K + BK - 1) / BK;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        const uint32_t full_r0 = map_to_rank(full0, 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, issued_par = 0;
+        bool ok = true;
+        for (int L = pair; L < tiles && ok; L += npairs) {
+            const TileCoord c = decode_tile<kPairRows, P::OUTC>(g, L, tiles, nk);
+            const CUtensorMap *tb = (MODE == GEMM_UP_SWIGLU && rank) ? &tmB1 : &tmB0;
+            const int brow = c.e * g.b_rows + c.n0 + (MODE == GEMM_UP_SWIGLU ? 0 : WROWS * (int)rank);
+            for (int kb = c.kb0; kb < c.kb1; ++kb) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+                if (rank == 0) mbar_expect_tx(full0 + 8 * stage, 2 * P::STAGE_BYTES);
+                const uint32_t sa = smem_u32(smem + stage * P::STAGE_BYTES);
+                const uint32_t fb = full_r0 + 8 * stage;
+                tma_load_2d_pair(sa, &tmA, (kb * BK) % g.a_k_period, c.m0 + BM * (int)rank, fb);
+                tma_load_2d_pair(sa + P::A_BYTES, tb, kb * BK, brow, fb);
+                issued |= 1u << stage;
+                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok) {
+            // Let the copies already issued land before the CTA can exit.
+            // Rank 0: the last load into stage s completes the phase of parity
+            // issued_par[s] (once rank 1's bytes for it have landed too).
+            // Rank 1 cannot see its copies complete; it waits the drain time.
+            const uint64_t t0 = globaltimer();
+            if (rank == 0) {
+                for (int s = 0; s < STAGES; ++s) {
+                    if (!(issued >> s & 1u)) continue;
+                    const uint32_t par = issued_par >> s & 1u;
+                    while (!mbar_try_wait(full0 + 8 * s, par) && globaltimer() - t0 < kPairDrainNs) {
+                    }
+                }
+            } else {
+                while (globaltimer() - t0 < kPairDrainNs) {
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        if (rank == 0) {
+            // -------------------------------------------- MMA issuer (rank 0)
+            constexpr uint32_t idesc = idesc_bf16(kPairRows, BNM);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            if (g_stall_mma && !mbar_wait(done_bar, 0, abort_flag)) ok = false;
+            for (int L = pair; L < tiles && ok; L += npairs) {
+                if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * P::STAGE_BYTES);
+                    const uint32_t sb = sa + P::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_pair(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32),
+                                    idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_pair(empty0 + 8 * stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit_pair(tfull0 + 8 * acc);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            // Every MMA of the pair completes (both CTAs' done barriers) before
+            // either CTA frees its tensor memory.
+            tc_commit_pair(done_bar);
+        }
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(done_bar, 0) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int quarter = warp - 4;
+        const uint32_t tempty_r0 = map_to_rank(tempty0, 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int L = pair; L < tiles; L += npairs) {
+            const TileCoord c = decode_tile<kPairRows, P::OUTC>(g, L, tiles, nk);
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+            const int row0 = c.m0 + BM * (int)rank + quarter * 32;
+            const int row = row0 + lane;
+            const bool vrow = row < c.mend;
+            if (MODE == GEMM_UP_SWIGLU) {
+                __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+#pragma unroll 1
+                for (int cc = 0; cc < BNM / 2; cc += 16) {
+                    float gt[16], up[16];
+                    tmem_ld16(tbase + cc, gt);
+                    tmem_ld16(tbase + BNM / 2 + cc, up);
+                    tmem_ld_wait();
+                    float h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) h[i] = silu(gt[i]) * up[i];
+                    const int col = c.n0 + cc;
+                    if (vrow) {
+                        __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                        if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(h);
+                        if (col + 8 < g.N) *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(h + 8);
+                    }
+                }
+            } else if (MODE == GEMM_UP_RELU) {
+                __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(g.C);
+#pragma unroll 1
+                for (int cc = 0; cc < BNM; cc += 16) {
+                    float v[16];
+                    tmem_ld16(tbase + cc, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], 0.f);
+                    const int col = c.n0 + cc;
+                    if (vrow) {
+                        __nv_bfloat16 *dst = H + (size_t)row * g.ldc + col;
+                        if (col < g.N) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
+                        if (col + 8 < g.N) *reinterpret_cast<uint4 *>(dst + 8) = pack_bf16x8(v + 8);
+                    }
+                }
+            } else {
+                float *O = static_cast<float *>(g.C);
+                float *stg = epi_stage + quarter * (32 * P::EPI_STRIDE);
+                store_f32_rows<P::EPI_COLS, BNM>(tbase, stg, lane, O, g.ldc, row0, c.mend, c.n0,
+                                                 g.N);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(tempty_r0 + 8 * acc);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // Neither CTA leaves while the other may still reach its shared memory
+    // (rank 0's MMAs read rank 1's, the barriers are signalled across).
+    cluster_sync_all();
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    }
+    cluster_sync_all();
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -796,11 +1109,43 @@ static cudaError_t launch_geo(const Maps &m, const Args &g, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// SM-pair geometry: as many pairs as can be resident at once (clusters of two
+// CTAs of about 200 KB of shared memory each), every pair persistent.
+template <int MODE>
+static cudaError_t launch_pair(const Maps &m, const Args &g, cudaStream_t st) {
+    using P = PairGeo<MODE>;
+    static_assert(P::SMEM <= (size_t)kSmemLimit, "shared memory");
+    auto kern = grouped_gemm_pair_kernel<MODE>;
+    static int grid = 0;
+    if (!grid) {
+        cudaError_t err =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(num_sms());
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = P::SMEM;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            clusters = num_sms() / 2;
+        }
+        grid = 2 * std::min(clusters, num_sms() / 2);
+    }
+    kern<<<grid, 256, P::SMEM, st>>>(m.a, m.b0, m.b1, g);
+    note_launch();
+    return cudaGetLastError();
+}
+
 template <int MODE>
 static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args &g,
                                cudaStream_t st) {
     switch (nt) {
         case 0:
+            if (mh == TILE_ROWS_256_PAIR) {
+                if constexpr (MODE == GEMM_LOGITS) return cudaErrorInvalidValue;
+                else return launch_pair<MODE>(m, g, st);
+            }
             if (mh == 2) return launch_geo<MODE, 0, BNM, 2>(m, g, st);
             return bn == BNM ? launch_geo<MODE, 0, BNM>(m, g, st)
                              : launch_geo<MODE, 0, BNM / 2>(m, g, st);
@@ -820,8 +1165,10 @@ static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args
 // launch_build_tiles with row tiles of 128 (nt = 0) or nt rows (nt = 16, 32,
 // 64, 256: weights on the MMA's M side; 256, down projection only, sets the
 // MMA N per tile).  bn (nt = 0 only): MMA N of 256 or 128; 128 doubles the
-// output tiles when there are too few to fill the SMs.  mh = 2 (nt = 0,
-// bn = 256 only): 256-row tiles, tile table built with 256-row tiles.  A's column for
+// output tiles when there are too few to fill the SMs.  mh (nt = 0, bn = 256
+// only; tile table built with 256-row tiles): TILE_ROWS_256, 256-row tiles on
+// one SM; TILE_ROWS_256_PAIR, 256-row tiles on an SM pair (the up and down
+// modes, k_splits = 1).  A's column for
 // reduction index k is k mod a_k_period (a_k_period = K: no wrap).  With k_splits > 1 split s of
 // every tile writes fp32 partial sums to C + s * split_stride: GEMM_DOWN
 // always (row-major [rows, ldc]); the up modes only with nt > 0, writing the
@@ -842,7 +1189,10 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
     const int nk = (K + BK - 1) / BK;
     if (nt != 0 && nt != 16 && nt != 32 && nt != 64 && nt != kVarRows) return cudaErrorInvalidValue;
     if (bn != BNM && bn != BNM / 2) return cudaErrorInvalidValue;
-    if (mh != 1 && (mh != 2 || nt != 0 || bn != BNM)) return cudaErrorInvalidValue;
+    if (mh != 1 && ((mh != 2 && mh != TILE_ROWS_256_PAIR) || nt != 0 || bn != BNM))
+        return cudaErrorInvalidValue;
+    if (mh == TILE_ROWS_256_PAIR && (k_splits != 1 || mode == GEMM_LOGITS || a_k_period != K))
+        return cudaErrorInvalidValue;
     if (mode == GEMM_LOGITS && (nt != 0 || bn != BNM || mh != 1 || chain_kb < 1))
         return cudaErrorInvalidValue;
     if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN && mode != GEMM_LOGITS && nt == 0) ||
@@ -855,7 +1205,8 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
     k_splits = (nk + kbps - 1) / kbps;          // every split gets at least one K block
     const bool var = nt == kVarRows;
     if (var && mode != GEMM_DOWN) return cudaErrorInvalidValue;
-    const int rows = var ? 128 : nt ? nt : BM * mh;
+    // rows of one A box: one CTA's share of a tile
+    const int rows = var ? 128 : nt ? nt : mh == TILE_ROWS_256_PAIR ? BM : BM * mh;
     Maps m;
     if (!make_map(&m.a, A, a_rows, a_cols, rows)) return cudaErrorInvalidValue;
     m.a64 = m.a32 = m.a16 = m.a;

@@ -165,6 +165,12 @@ cudaError_t launch_simt_gemm(const GroupedGemmArgs &g, int mode, int dtype, cuda
 
 // gemm_tcgen05.cu: tcgen05/TMEM grouped GEMM for the bf16 workloads.
 constexpr int kTcBM = 128;
+// Token-row tiling of the nt = 0 geometries (launch_tc_gemm's mh): 128-row
+// tiles; 256-row tiles on one SM (two M = 128 MMAs per weight stage, one
+// accumulator); 256-row tiles on a pair of SMs (a cluster of two CTAs,
+// tcgen05.mma.cta_group::2 with M = 256, two accumulators).
+enum { TILE_ROWS_128 = 1, TILE_ROWS_256 = 2, TILE_ROWS_256_PAIR = 3 };
+inline int tile_rows(int mh) { return mh == TILE_ROWS_128 ? kTcBM : 2 * kTcBM; }
 cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long long a_rows,
                            int a_cols,
                            const void *B0, const void *B1, int E, int b_rows, int N, int K,

@@ -118,7 +118,8 @@ struct FfnPlan {
     int nt, s_up, s_down;
     int bn_up, bn_down;     // nt = 0: MMA N (256, or 128 when tiles are few)
     int nt_down;            // geometry of the down projection
-    int mh_down;            // nt_down = 0: 128-row halves per tile (1, or 2: 256 rows)
+    int mh_down;            // nt_down = 0: token-row tiling (TILE_ROWS_*)
+    int mh_up;              // nt = 0: token-row tiling of the up projection
 };
 constexpr int kPlanSMs = 148;   // SM count the split choice assumes (B300)
 constexpr int kVarTileRows = 256;
@@ -136,6 +137,22 @@ constexpr double kVarPadGain = 1.3;
 // 6.1 ms, its unoverlapped epilogue being a fifth of a tile.
 constexpr long long kWideMinRows = 512;
 constexpr long long kWideMinK = 8192;
+// 256-row tiles on SM pairs (cta_group::2: 32 KB stages per SM, two
+// accumulators) for every nt = 0, N = 256 projection whose experts hold at
+// least kPairMinRows rows on average.  Measured on B300 against the one-SM
+// tiles: Switch T = 8192 (1024 rows per expert) 0.184 -> 0.170 ms and Mixtral
+// T = 4096 2.06 -> 2.00 ms at the same clock; Mixtral T = 16384 5 % fewer
+// cycles, about even in time under the power cap; DeepSeek T = 8192 (256
+// rows on average, most experts far fewer) slower, the padding rows of
+// 256-row tiles costing MMA work and power.
+constexpr long long kPairMinRows = 512;
+// moe_debug_set_pair_tiles: 0 the rule above, -1 never, 1 for every
+// projection with token rows on the M side (nt = 0; N set to 256).
+static int g_pair_policy = 0;
+static bool use_pair(long long per, int bn, int splits) {
+    if (g_pair_policy < 0 || bn != 256 || splits != 1) return false;
+    return g_pair_policy > 0 || per >= kPairMinRows;
+}
 
 // Split the reduction only when the tiles do not fill the SMs once, and then
 // only up to one round of work items: measured at the Mixtral shape, a split
@@ -154,7 +171,7 @@ int split_count(long long tiles, long long nk) {
 // rows: dispatched rows (T*k routed, T shared); groups: experts; K = d.
 FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long long F,
                  bool swiglu) {
-    FfnPlan p{0, 1, 1, 256, 256, 0, 1};   // nt s_up s_down bn_up bn_down nt_down mh_down
+    FfnPlan p{0, 1, 1, 256, 256, 0, TILE_ROWS_128, TILE_ROWS_128};
     if (c->dtype != MOE_DTYPE_BF16 || rows <= 0 || F <= 0) return p;
     const long long d = c->d_model;
     const long long active = std::min(groups, rows);
@@ -172,7 +189,10 @@ FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long lon
         const long long mt = (rows + 127) / 128 + active;
         if (mt * ((F + up_cols - 1) / up_cols) < 2 * kPlanSMs) p.bn_up = 128;
         if (mt * ((d + 255) / 256) < kPlanSMs) p.bn_down = 128;
-        if (per >= kWideMinRows && F >= kWideMinK && p.bn_down == 256) p.mh_down = 2;
+        if (g_pair_policy > 0) p.bn_up = p.bn_down = 256;
+        if (per >= kWideMinRows && F >= kWideMinK && p.bn_down == 256) p.mh_down = TILE_ROWS_256;
+        if (use_pair(per, p.bn_up, p.s_up)) p.mh_up = TILE_ROWS_256_PAIR;
+        if (use_pair(per, p.bn_down, p.s_down)) p.mh_down = TILE_ROWS_256_PAIR;
         const double pad128 = (double)((per + 127) / 128 * 128) / per;
         const double pad16 = (double)((per + 15) / 16 * 16) / per;
         if (pad128 > kVarPadGain * pad16) {
@@ -442,8 +462,9 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
     const int d = c->d_model;
     const int nt = plan.nt;
     cudaEvent_t ev = up_stage >= 0 ? stage_begin(st) : nullptr;
-    MOE_CUDA(launch_build_tiles(offsets, groups, nt ? nt : kTcBM, tile_e, nullptr, tile_start,
-                                ntiles, st));
+    const int up_rows = nt ? nt : tile_rows(plan.mh_up);
+    MOE_CUDA(launch_build_tiles(offsets, groups, up_rows, tile_e, nullptr, tile_start, ntiles,
+                                st));
     if (plan.s_up > 1) {
         const int upw = up_mode == GEMM_UP_SWIGLU ? 2 : 1;
         MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, 1, A, rows, d, w1, w3, groups, F, F, d,
@@ -454,17 +475,19 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
                                          up_mode == GEMM_UP_SWIGLU, offsets + groups, rows,
                                          static_cast<__nv_bfloat16 *>(h), st));
     } else {
-        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, 1, A, rows, d, w1, w3, groups, F, F, d,
-                                d, 1, 0, tile_e, tile_start, ntiles, offsets, h, F, st));
+        MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, nt ? TILE_ROWS_128 : plan.mh_up, A, rows,
+                                d, w1, w3, groups, F, F, d, d, 1, 0, tile_e, tile_start, ntiles,
+                                offsets, h, F, st));
     }
     if (up_stage >= 0) {
         stage_end(up_stage, ev, st);
         ev = stage_begin(st);
     }
-    const int mh_down = plan.nt_down ? 1 : plan.mh_down;
-    if (plan.nt_down != nt || mh_down != 1)
-        MOE_CUDA(launch_build_tiles(offsets, groups, plan.nt_down ? plan.nt_down : kTcBM * mh_down,
-                                    tile_e, nullptr, tile_start, ntiles, st));
+    const int mh_down = plan.nt_down ? TILE_ROWS_128 : plan.mh_down;
+    const int down_rows = plan.nt_down ? plan.nt_down : tile_rows(mh_down);
+    if (down_rows != up_rows)
+        MOE_CUDA(launch_build_tiles(offsets, groups, down_rows, tile_e, nullptr, tile_start,
+                                    ntiles, st));
     MOE_CUDA(launch_tc_gemm(GEMM_DOWN, plan.nt_down, plan.bn_down, mh_down, h, rows, F, w2, nullptr,
                             groups, d, d, F, F, plan.s_down, rows * d, tile_e, tile_start, ntiles,
                             offsets, out, d, st));
@@ -676,7 +699,15 @@ int moe_ffn_plan(const moe_config *cfg, int32_t shared, moe_ffn_plan_info *out) 
     out->up_n = p.bn_up;
     out->down_n = p.bn_down;
     out->down_rows_per_tile = p.nt_down;
-    out->down_halves = p.nt_down ? 1 : p.mh_down;
+    out->down_halves = p.nt_down || p.mh_down == TILE_ROWS_128 ? 1 : 2;
+    out->up_pair = !p.nt && p.s_up == 1 && p.mh_up == TILE_ROWS_256_PAIR;
+    out->down_pair = !p.nt_down && p.mh_down == TILE_ROWS_256_PAIR;
+    return MOE_OK;
+}
+
+int moe_debug_set_pair_tiles(int32_t policy) {
+    if (policy < -1 || policy > 1) return MOE_ERR_INVALID_ARG;
+    g_pair_policy = policy;
     return MOE_OK;
 }
 

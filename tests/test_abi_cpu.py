@@ -115,17 +115,21 @@ def test_ffn_plan_geometries():
     assert (big["rows_per_tile"], big["up_n"], big["down_n"]) == (0, 256, 256)
     assert (big["down_rows_per_tile"], big["down_halves"]) == (0, 2)
     assert big["up_splits"] == big["down_splits"] == 1
+    assert big["up_pair"] == big["down_pair"] == 1      # 256-row tiles on SM pairs
     one = _plan("mixtral", 1)                # 2 rows: swap-AB, split down projection
     assert one["rows_per_tile"] == 16 and one["down_rows_per_tile"] == 16
     assert one["up_splits"] == 1 and one["down_splits"] > 1
     e896 = _plan("e896", 16384)              # about 146 rows per expert
     assert (e896["rows_per_tile"], e896["down_rows_per_tile"], e896["down_halves"]) == (0, 256, 1)
+    assert e896["up_pair"] == e896["down_pair"] == 0
     ds = _plan("deepseek", 8192)             # 256 rows per expert, reduction 2048 down
     assert (ds["rows_per_tile"], ds["down_rows_per_tile"], ds["down_halves"]) == (0, 0, 1)
+    assert ds["up_pair"] == ds["down_pair"] == 0
+    assert _plan("switch", 8192)["up_pair"] == 1            # 1024 rows per expert
     sw = _plan("switch", 8192)               # 288 down tiles of N = 256: one round of SMs
     assert (sw["rows_per_tile"], sw["down_n"]) == (0, 256)
     shared = moe.ffn_plan(moe.config_for(mi.workload("deepseek"), 8192), shared=True)
-    assert shared["rows_per_tile"] == 0 and shared["down_halves"] == 1
+    assert shared["rows_per_tile"] == 0 and shared["up_pair"] == 1
 
 
 @pytest.mark.parametrize("name,T,rows,splits", [
@@ -142,7 +146,24 @@ def test_ffn_plan_swapped_tiles_for_few_rows(name, T, rows, splits):
     p = _plan(name, T)
     assert p["rows_per_tile"] == rows and p["down_rows_per_tile"] == rows
     assert (p["up_splits"], p["down_splits"]) == splits
-    assert p["down_halves"] == 1
+    assert p["down_halves"] == 1 and p["up_pair"] == p["down_pair"] == 0
+
+
+def test_pair_tiles_switch():
+    """moe_debug_set_pair_tiles: -1 keeps the one-SM tiles, 1 takes the SM
+    pairs wherever token rows are on the M side with N = 256 and no split."""
+    try:
+        moe.debug_set_pair_tiles(-1)
+        assert _plan("mixtral", 16384)["up_pair"] == 0
+        assert _plan("mixtral", 16384)["down_halves"] == 2          # one-SM 256-row tiles
+        moe.debug_set_pair_tiles(1)
+        p = _plan("mixtral", 1000, d_model=512, d_ff=2048)          # 250 rows per expert
+        assert p["up_pair"] == p["down_pair"] == 1
+        assert _plan("mixtral", 16)["up_pair"] == 0                 # swapped tiles stay
+        with pytest.raises(moe.MoEError):
+            moe.debug_set_pair_tiles(2)
+    finally:
+        moe.debug_set_pair_tiles(0)
 
 
 def test_ffn_plan_rejects_fp32_and_missing_shared_expert():

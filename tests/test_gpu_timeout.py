@@ -4,7 +4,8 @@ barrier phase that nothing completes, with the main-loop limit at 1 ms; the
 wait runs out, the kernel flags MOE_ERR_DEVICE_TIMEOUT, drains its own copies
 and MMAs, frees its tensor memory and returns.  The host reads the status,
 and the next call, with the hooks back to normal, runs on the same context and
-matches the oracle."""
+matches the oracle.  The SM-pair tiles (a cluster of two CTAs) take the same
+path in both CTAs: the CTA without the MMA issuer runs out of its own waits."""
 import pytest
 import torch
 
@@ -17,25 +18,33 @@ DEV = "cuda"
 MOE_ERR_DEVICE_TIMEOUT = -5
 
 
-@pytest.mark.parametrize("sizes,T", [({"d_model": 256, "d_ff": 512}, 300),    # 128-row tiles
-                                     ({"d_model": 1024, "d_ff": 2048}, 5)])   # swapped, split
-def test_expired_wait_is_reported_and_the_context_stays_usable(sizes, T):
+@pytest.mark.parametrize("sizes,T,pair", [
+    ({"d_model": 256, "d_ff": 512}, 300, 0),     # 128-row tiles
+    ({"d_model": 1024, "d_ff": 2048}, 5, 0),     # swapped, split
+    ({"d_model": 512, "d_ff": 2048}, 1000, 1),   # 256-row tiles on SM pairs
+], ids=["tiles128", "swapped", "pair"])
+def test_expired_wait_is_reported_and_the_context_stays_usable(sizes, T, pair):
     w = mi.workload("mixtral").with_sizes(**sizes)
     inp = mi.generate(w, T, DEV)
     cfg = moe.config_for(w, T)
-    full_check(w, T, inp)                              # a healthy call first
-    assert moe.device_status() == 0
-    moe.debug_set_wait_hooks(1_000_000, True)
+    moe.debug_set_pair_tiles(pair)
     try:
-        moe.layer_forward(cfg, inp["x"], weights_dict(inp))
-        torch.cuda.synchronize()
-        assert moe.device_status() == MOE_ERR_DEVICE_TIMEOUT
-        assert moe.device_status() == 0                # read and cleared
+        assert moe.ffn_plan(cfg)["up_pair"] == pair
+        full_check(w, T, inp)                              # a healthy call first
+        assert moe.device_status() == 0
+        moe.debug_set_wait_hooks(1_000_000, True)
+        try:
+            moe.layer_forward(cfg, inp["x"], weights_dict(inp))
+            torch.cuda.synchronize()
+            assert moe.device_status() == MOE_ERR_DEVICE_TIMEOUT
+            assert moe.device_status() == 0                # read and cleared
+        finally:
+            moe.debug_set_wait_hooks()
+        rep, _, _ = full_check(w, T, inp)
+        print(rep)
+        assert moe.device_status() == 0
     finally:
-        moe.debug_set_wait_hooks()
-    rep, _, _ = full_check(w, T, inp)
-    print(rep)
-    assert moe.device_status() == 0
+        moe.debug_set_pair_tiles(0)
 
 
 def test_hook_arguments_checked():
