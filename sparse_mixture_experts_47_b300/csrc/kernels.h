@@ -111,6 +111,9 @@ cudaError_t launch_expert_scale(const ExpertOut &o, int d, const int32_t *offset
 cudaError_t launch_gather_rows(const void *x, int elem_bytes, int d, const int32_t *perm,
                                const int32_t *offsets_end, int k, long long max_rows, void *xs,
                                cudaStream_t st);
+// The same rows, token-major: x[t] to row inv[t*k+j] of xs for every kept slot.
+cudaError_t launch_scatter_rows(const void *x, int elem_bytes, int d, const int32_t *inv, int k,
+                                long long T, void *xs, cudaStream_t st);
 // y[t] = sum_j w o[row] + s[t]; `sh` (the shared expert's output, p NULL
 // when there is none) is read like `o`.
 cudaError_t launch_combine(const ExpertOut &o, const int32_t *inv, const float *w,

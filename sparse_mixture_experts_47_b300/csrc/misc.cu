@@ -294,6 +294,53 @@ cudaError_t launch_gather_rows(const void *x, int elem_bytes, int d, const int32
     return cudaGetLastError();
 }
 
+// Token-major form of the same copy (token choice, slots known by inv): one
+// warp per token reads its row of x once and writes it to the rows of its
+// kept slots.  x is read from HBM once instead of k times through L2, which
+// misses once x outgrows L2 (the 896-expert layer: 134 MB of x, k = 8).
+__global__ void scatter_rows_kernel(const uint4 *x, int vec_per_row, const int32_t *inv, int k,
+                                    long long T, uint4 *xs) {
+    const long long t = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    // rows of the token's slots (k <= 16), spread to every lane while the
+    // whole warp is converged
+    const int my_row = lane < k ? inv[t * k + lane] : -1;
+    int rows[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) rows[j] = __shfl_sync(0xffffffffu, my_row, j);
+    const uint4 *src = x + t * vec_per_row;
+    int i = lane;
+    for (; i + 224 < vec_per_row; i += 256) {
+        uint4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = src[i + 32 * q];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= k || rows[j] < 0) continue;
+            uint4 *dst = xs + (long long)rows[j] * vec_per_row;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) __stcs(dst + i + 32 * q, v[q]);
+        }
+    }
+    for (; i < vec_per_row; i += 32) {
+        const uint4 v = src[i];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < k && rows[j] >= 0) __stcs(xs + (long long)rows[j] * vec_per_row + i, v);
+    }
+}
+
+cudaError_t launch_scatter_rows(const void *x, int elem_bytes, int d, const int32_t *inv, int k,
+                                long long T, void *xs, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int vpr = d * elem_bytes / 16;
+    scatter_rows_kernel<<<(unsigned)((T + 7) / 8), 256, 0, st>>>(
+        static_cast<const uint4 *>(x), vpr, inv, k, T, static_cast<uint4 *>(xs));
+    note_launch();
+    return cudaGetLastError();
+}
+
 // y[t] = sum_j [inv >= 0] w[t,j] o[inv[t,j]] (j in order) + s[t], where
 // o = sum of the out_sorted planes and s = sum of the shared planes, each in
 // plane order.

@@ -192,7 +192,11 @@ FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long lon
         if (g_pair_policy > 0) p.bn_up = p.bn_down = 256;
         if (per >= kWideMinRows && F >= kWideMinK && p.bn_down == 256) p.mh_down = TILE_ROWS_256;
         if (use_pair(per, p.bn_up, p.s_up)) p.mh_up = TILE_ROWS_256_PAIR;
-        if (use_pair(per, p.bn_down, p.s_down)) p.mh_down = TILE_ROWS_256_PAIR;
+        // the long-reduction down projection keeps its one-SM 256-row tiles
+        // (measured at Mixtral T = 16384: 2.48 ms against 2.54-2.58 on pairs)
+        if (use_pair(per, p.bn_down, p.s_down) &&
+            (p.mh_down != TILE_ROWS_256 || g_pair_policy > 0))
+            p.mh_down = TILE_ROWS_256_PAIR;
         const double pad128 = (double)((per + 127) / 128 * 128) / per;
         const double pad16 = (double)((per + 15) / 16 * 16) / per;
         if (pad128 > kVarPadGain * pad16) {
@@ -499,9 +503,10 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
 // planes of R*d elements).  bf16: gather the rows into x_sorted, tcgen05 up
 // (+activation, h in bf16) into h, tcgen05 down into out_sorted.  fp32: SIMT
 // GEMMs reading x through perm directly.
+// inv (token choice, may be NULL): the slots' rows, for the token-major copy.
 int run_experts(const moe_config *c, const void *x, const int32_t *perm, const int32_t *offsets,
                 const void *w1, const void *w3, const void *w2, float *out_sorted, void *ws,
-                const Layout &L, cudaStream_t st) {
+                const Layout &L, cudaStream_t st, const int32_t *inv = nullptr) {
     const Sizes s = sizes(c);
     if (s.R == 0) return MOE_OK;
     const int gk = expert_choice(c) ? 1 : (int)s.k;   // perm holds t*k+j, or t itself
@@ -511,7 +516,10 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
     if (c->dtype == MOE_DTYPE_BF16) {
         void *xs = at<void>(ws, L.xs), *h = at<void>(ws, L.h);
         cudaEvent_t ev = stage_begin(st);
-        MOE_CUDA(launch_gather_rows(x, 2, (int)s.d, perm, offsets + s.E, gk, s.R, xs, st));
+        if (inv && !expert_choice(c))
+            MOE_CUDA(launch_scatter_rows(x, 2, (int)s.d, inv, (int)s.k, s.T, xs, st));
+        else
+            MOE_CUDA(launch_gather_rows(x, 2, (int)s.d, perm, offsets + s.E, gk, s.R, xs, st));
         stage_end(MOE_STAGE_GATHER, ev, st);
         return run_tc_ffn(c, routed_plan(c), up_mode, xs, s.R, (int)s.E, (int)s.F, offsets, w1,
                           w3, w2, h, at<float>(ws, L.up_part), out_sorted, tile_e,
@@ -1004,7 +1012,8 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
                                          obs->expert_out_std, obs->expert_out_max_abs, st));
         return MOE_OK;
     }
-    rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted, ws, L, st);
+    rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted, ws, L, st,
+                     expert_choice(cfg) ? nullptr : inv);
     if (rc != MOE_OK) return rc;
     if (want_scale)
         MOE_CUDA(launch_expert_scale(eo, (int)s.d, offsets, (int)s.E, s.R,

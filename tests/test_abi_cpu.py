@@ -115,7 +115,7 @@ def test_ffn_plan_geometries():
     assert (big["rows_per_tile"], big["up_n"], big["down_n"]) == (0, 256, 256)
     assert (big["down_rows_per_tile"], big["down_halves"]) == (0, 2)
     assert big["up_splits"] == big["down_splits"] == 1
-    assert big["up_pair"] == big["down_pair"] == 1      # 256-row tiles on SM pairs
+    assert big["up_pair"] == 1 and big["down_pair"] == 0  # up on SM pairs, down one-SM 256 rows
     one = _plan("mixtral", 1)                # 2 rows: swap-AB, split down projection
     assert one["rows_per_tile"] == 16 and one["down_rows_per_tile"] == 16
     assert one["up_splits"] == 1 and one["down_splits"] > 1
