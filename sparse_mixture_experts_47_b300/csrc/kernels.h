@@ -39,8 +39,12 @@ inline int router_slices(int d, int E, int dtype) {
 int router_blocks(int T, int E, int dtype);
 size_t router_smem_bytes(int E, int dtype);
 cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStream_t st);
+// W_r split into bf16 parts, and the tile table of the logit GEMM's single
+// group of T rows (128-row tiles).
 cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp, int parts,
-                                       __nv_bfloat16 *out, cudaStream_t st);
+                                       __nv_bfloat16 *out, int T, int32_t *offsets,
+                                       int32_t *tile_e, int32_t *tile_start, int32_t *n_tiles,
+                                       cudaStream_t st);
 cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, int S,
                                       cudaStream_t st);
 cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int E, int k,

@@ -157,9 +157,10 @@ static bool use_pair(long long per, int bn, int splits) {
 // Split the reduction only when the tiles do not fill the SMs once, and then
 // only up to one round of work items: measured at the Mixtral shape, a split
 // that spreads the items over more rounds, or any split of the up projection
-// at T = 1 and 16, costs more in partial sums than it gains in balance, while
-// splitting the down projection at T = 1 (64 tiles) in two cuts it from 68
-// to 45 us.
+// at T = 1 and 16, costs more in partial sums than it gains in balance (a
+// split chosen to fill the rounds to 95 %, 7-way for the up projection at
+// T = 1: 0.152 -> 0.163 ms per layer), while splitting the down projection at
+// T = 1 (64 tiles) in two cuts it from 68 to 45 us.
 int split_count(long long tiles, long long nk) {
     if (tiles <= 0 || nk <= 0 || tiles >= kPlanSMs) return 1;
     long long S = kPlanSMs / tiles;
@@ -419,11 +420,8 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         int32_t *off = at<int32_t>(ws, L.rt_offsets);
         int32_t *te = at<int32_t>(ws, L.rt_tile_e), *ts = at<int32_t>(ws, L.rt_tile_start);
         int32_t *nt = at<int32_t>(ws, L.rt_ntiles);
-        MOE_CUDA(launch_split_router_weight(w_r, a.E, a.d, dp, kRouterParts, wsplit, st));
-        set_pair_kernel<<<1, 1, 0, st>>>(off, 0, a.T);
-        note_launch();
-        MOE_CUDA(cudaGetLastError());
-        MOE_CUDA(launch_build_tiles(off, 1, kTcBM, te, nullptr, ts, nt, st));
+        MOE_CUDA(launch_split_router_weight(w_r, a.E, a.d, dp, kRouterParts, wsplit, a.T, off,
+                                            te, ts, nt, st));
         // chains of router_chain_kb K blocks summed on chip in chain order,
         // one plane per group of chains; the softmax adds the G planes in order
         MOE_CUDA(launch_tc_gemm(GEMM_LOGITS, 0, 256, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E,

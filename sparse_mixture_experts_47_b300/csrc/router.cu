@@ -568,19 +568,57 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(RouterArgs a) {
 // x W_r^T = x [hi|lo|..]^T over a parts*dp reduction with x's column taken
 // mod dp.  bf16 x bf16 products are exact in fp32.
 // --------------------------------------------------------------------------
+// A thread takes 8 consecutive columns (dp is a multiple of 64) and stores
+// each part as one 16-byte vector.  Block 0 also writes the logit GEMM's tile
+// table for its single group of T rows in 128-row tiles (offsets {0, T},
+// tile_e = 0, tile_start {0, tiles}, n_tiles), the table the grouped GEMM
+// reads.
+constexpr int kRouterMaxParts = 3;
 __global__ void split_router_weight_kernel(const float *w_r, int E, int d, int dp, int parts,
-                                           __nv_bfloat16 *out) {
-    const long long n = (long long)E * dp;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+                                           __nv_bfloat16 *out, int T, int32_t *offsets,
+                                           int32_t *tile_e, int32_t *tile_start,
+                                           int32_t *n_tiles) {
+    const long long n8 = (long long)E * (dp / 8);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
          i += (long long)gridDim.x * blockDim.x) {
-        const int e = (int)(i / dp), c = (int)(i % dp);
-        float r = c < d ? w_r[(size_t)e * d + c] : 0.f;
-        __nv_bfloat16 *row = out + (size_t)e * parts * dp;
+        const int e = (int)(i / (dp / 8)), c0 = 8 * (int)(i % (dp / 8));
+        const float *src = w_r + (size_t)e * d;
+        float r[8];
+        if (c0 + 8 <= d && (d & 3) == 0) {
+            const float4 a = *reinterpret_cast<const float4 *>(src + c0);
+            const float4 b = *reinterpret_cast<const float4 *>(src + c0 + 4);
+            r[0] = a.x; r[1] = a.y; r[2] = a.z; r[3] = a.w;
+            r[4] = b.x; r[5] = b.y; r[6] = b.z; r[7] = b.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r[j] = c0 + j < d ? src[c0 + j] : 0.f;
+        }
+        __nv_bfloat16 *row = out + (size_t)e * parts * dp + c0;
         // each part is the round-to-nearest bf16 of what the earlier parts left
-        for (int q = 0; q < parts; ++q) {
-            const __nv_bfloat16 b = __float2bfloat16_rn(r);
-            row[q * dp + c] = b;
-            r -= __bfloat162float(b);
+#pragma unroll
+        for (int q = 0; q < kRouterMaxParts; ++q) {
+            if (q >= parts) break;
+            uint32_t packed[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(r[j], r[j + 1]);
+                r[j] -= __low2float(b);
+                r[j + 1] -= __high2float(b);
+                packed[j / 2] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            *reinterpret_cast<uint4 *>(row + (size_t)q * dp) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+    if (blockIdx.x == 0) {
+        const int tiles = (T + 127) / 128;
+        for (int i = threadIdx.x; i < tiles; i += blockDim.x) tile_e[i] = 0;
+        if (threadIdx.x == 0) {
+            offsets[0] = 0;
+            offsets[1] = T;
+            tile_start[0] = 0;
+            tile_start[1] = tiles;
+            *n_tiles = tiles;
         }
     }
 }
@@ -959,10 +997,14 @@ cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStrea
 }
 
 cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp, int parts,
-                                       __nv_bfloat16 *out, cudaStream_t st) {
-    const long long n = (long long)E * dp;
-    const int grid = (int)std::min<long long>((n + 255) / 256, 148 * 8);
-    split_router_weight_kernel<<<grid, 256, 0, st>>>(w_r, E, d, dp, parts, out);
+                                       __nv_bfloat16 *out, int T, int32_t *offsets,
+                                       int32_t *tile_e, int32_t *tile_start, int32_t *n_tiles,
+                                       cudaStream_t st) {
+    if (parts < 1 || parts > kRouterMaxParts || dp % 64 != 0) return cudaErrorInvalidValue;
+    const long long n8 = (long long)E * (dp / 8);
+    const int grid = (int)std::max<long long>(1, std::min<long long>((n8 + 255) / 256, 148 * 4));
+    split_router_weight_kernel<<<grid, 256, 0, st>>>(w_r, E, d, dp, parts, out, T, offsets,
+                                                     tile_e, tile_start, n_tiles);
     note_launch();
     return cudaGetLastError();
 }
