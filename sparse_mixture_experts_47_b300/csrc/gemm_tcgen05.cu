@@ -33,7 +33,8 @@
 // MMA's N chosen per tile: a tile holds up to 256 of one expert's rows and
 // its MMA N is that count rounded up to 16, so an expert with 146 rows costs
 // a 160-wide tile instead of two 128-row tiles.
-// GEMM_LOGITS (NT = 0, N = 256): the router's logits x W_r^T over a long
+// GEMM_LOGITS (NT = 0, N = 256, or 224 where that pads the experts less):
+// the router's logits x W_r^T over a long
 // reduction cut into chains of equal K ranges (the tensor core's fp32
 // accumulation loses precision along one long chain).  Chain 0 of a tile
 // accumulates into TMEM columns 0-255 (S), every later chain into columns
@@ -69,6 +70,7 @@ constexpr int kSmemBase = 1024 /* alignment slack */ + 256 /* barriers */;
 // [32 rows][32 or 16 columns] fp32 block per warp (Geo::EPI_COLS).
 constexpr int kEpiSwapBytes = 4 * 16 * 32 * 2;
 constexpr int kVarRows = 256;        // NT of the per-tile-width geometry
+constexpr int kLogitsN224 = 224;     // GEMM_LOGITS column tile that divides 896 experts
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress
 
 // Failure-detection test hooks (moe_debug_set_wait_hooks).  The limit of the
@@ -107,7 +109,10 @@ template <int MODE, int NT, int BN, int MH> struct Geo {
     static constexpr int EXTRA = kSmemBase + EPI;
     static constexpr int FIT = (kSmemLimit - EXTRA) / STAGE_BYTES;
     static constexpr int STAGES =
-        SWAP ? (FIT < 8 ? FIT : 8) : MH == 2 ? 3 : (BN == BNM ? 4 : 6);
+        SWAP ? (FIT < 8 ? FIT : 8)
+             : MH == 2 ? 3
+                       : (MODE == GEMM_LOGITS && BN != BNM) ? (FIT < 8 ? FIT : 8)
+                                                            : (BN == BNM ? 4 : 6);
     static constexpr int NACC = MH == 2 ? 1 : 2;                 // accumulator buffers
     // output columns (features) of one tile
     static constexpr int OUTC = SWAP ? WROWS : (MODE == GEMM_UP_SWIGLU ? BN / 2 : BN);
@@ -1174,7 +1179,7 @@ static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args
 // always (row-major [rows, ldc]); the up modes only with nt > 0, writing the
 // pre-activation sums (SwiGLU: W1 part at column f, W3 part at N + f).
 // k_splits = 1 up modes write the activation in bf16; GEMM_DOWN writes fp32.
-// GEMM_LOGITS (nt = 0, bn = 256, mh = 1): the reduction is cut into chains of
+// GEMM_LOGITS (nt = 0, bn = 256 or 224, mh = 1): the reduction is cut into chains of
 // chain_kb K blocks, and k_splits splits of whole chains; each split sums its
 // chains on chip in chain order and writes one fp32 plane.
 cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long long a_rows,
@@ -1188,12 +1193,14 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
     if (a_rows == 0) return cudaSuccess;
     const int nk = (K + BK - 1) / BK;
     if (nt != 0 && nt != 16 && nt != 32 && nt != 64 && nt != kVarRows) return cudaErrorInvalidValue;
-    if (bn != BNM && bn != BNM / 2) return cudaErrorInvalidValue;
+    if (bn != BNM && bn != BNM / 2 && !(mode == GEMM_LOGITS && bn == kLogitsN224))
+        return cudaErrorInvalidValue;
     if (mh != 1 && ((mh != 2 && mh != TILE_ROWS_256_PAIR) || nt != 0 || bn != BNM))
         return cudaErrorInvalidValue;
     if (mh == TILE_ROWS_256_PAIR && (k_splits != 1 || mode == GEMM_LOGITS || a_k_period != K))
         return cudaErrorInvalidValue;
-    if (mode == GEMM_LOGITS && (nt != 0 || bn != BNM || mh != 1 || chain_kb < 1))
+    if (mode == GEMM_LOGITS &&
+        (nt != 0 || (bn != BNM && bn != kLogitsN224) || mh != 1 || chain_kb < 1))
         return cudaErrorInvalidValue;
     if (k_splits < 1 || (k_splits > 1 && mode != GEMM_DOWN && mode != GEMM_LOGITS && nt == 0) ||
         (a_k_period % BK != 0 && a_k_period != K))
@@ -1238,7 +1245,9 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
     g.chain_kb = chain_kb;
     if (mode == GEMM_UP_SWIGLU) return launch_mode<GEMM_UP_SWIGLU>(nt, bn, mh, m, g, st);
     if (mode == GEMM_UP_RELU) return launch_mode<GEMM_UP_RELU>(nt, bn, mh, m, g, st);
-    if (mode == GEMM_LOGITS) return launch_geo<GEMM_LOGITS, 0, BNM>(m, g, st);
+    if (mode == GEMM_LOGITS)
+        return bn == kLogitsN224 ? launch_geo<GEMM_LOGITS, 0, kLogitsN224>(m, g, st)
+                                 : launch_geo<GEMM_LOGITS, 0, BNM>(m, g, st);
     return launch_mode<GEMM_DOWN>(nt, bn, mh, m, g, st);
 }
 

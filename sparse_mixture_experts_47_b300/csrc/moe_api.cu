@@ -424,7 +424,10 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
                                             te, ts, nt, st));
         // chains of router_chain_kb K blocks summed on chip in chain order,
         // one plane per group of chains; the softmax adds the G planes in order
-        MOE_CUDA(launch_tc_gemm(GEMM_LOGITS, 0, 256, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E,
+        // column tiles of 224 where they pad the experts less than 256 (896:
+        // four tiles of 224 instead of 1024 columns)
+        const int rbn = (a.E + 223) / 224 * 224 < (a.E + 255) / 256 * 256 ? 224 : 256;
+        MOE_CUDA(launch_tc_gemm(GEMM_LOGITS, 0, rbn, 1, x, s.T, a.d, wsplit, nullptr, 1, a.E,
                                 a.E, kRouterParts * dp, dp, G, s.T * s.E, te, ts, nt, off, part,
                                 a.E, st, router_chain_kb(c)));
         MOE_CUDA(launch_router_from_logits(a, part, G, st));

@@ -353,28 +353,72 @@ __device__ __forceinline__ void load4_f32(const __nv_bfloat16 *p, float *v) {
     v[2] = __uint_as_float(a.y << 16); v[3] = __uint_as_float(a.y & 0xffff0000u);
 }
 
-// One round of top-k selection over a warp: lane L holds the scores of
-// experts L + 32 i in sc[i] (-inf where absent or already taken).  Returns
-// the expert with the largest score, exactly equal scores going to the lower
-// expert index, and marks it taken.
+// Top-k selection over a warp: lane L holds the scores of experts L + 32 i in
+// sc[i] (-inf where absent).  next() returns the experts in order of score,
+// exactly equal scores going to the lower expert index.  Each lane keeps its
+// best two (score, expert) keys, found by one scan in expert order with
+// strict comparisons (a later expert displaces an earlier one only with a
+// larger score, which is the order's tie rule); a pick is the argmax of the
+// lanes' first keys over the warp (5 shuffle steps), and the lane whose key
+// was taken moves its second key up.  A lane that has given up both rescans
+// its scores for the best two keys after the last one taken (one lane
+// providing three or more of a token's picks: a few per cent of tokens).
+// Rescanning all scores for each of the 8 picks of the 896-expert layer kept
+// the ALU pipe 88 % busy.
 constexpr int kTopkPerLane = 32;   // E <= 1024
-__device__ __forceinline__ int warp_take_max(float (&sc)[kTopkPerLane], int lane) {
-    float bv = -CUDART_INF_F;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kTopkPerLane; ++i)
-        if (sc[i] > bv) { bv = sc[i]; bi = lane + 32 * i; }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-#pragma unroll
-    for (int i = 0; i < kTopkPerLane; ++i)
-        if (lane + 32 * i == bi) sc[i] = -CUDART_INF_F;
-    return bi;
+__device__ __forceinline__ bool key_before(float va, int ea, float vb, int eb) {
+    return va > vb || (va == vb && ea < eb);
 }
+struct WarpTopK {
+    float v0, v1;
+    int e0, e1;
+    int left;   // keys of the pair not taken yet
+    // the lane's best two keys (after (lv, le) unless FIRST)
+    template <bool FIRST>
+    __device__ __forceinline__ void scan(const float (&sc)[kTopkPerLane], int lane, float lv,
+                                         int le) {
+        v0 = v1 = -CUDART_INF_F;
+        e0 = e1 = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kTopkPerLane; ++i) {
+            const float x = sc[i];
+            const int ex = lane + 32 * i;
+            if (!FIRST && !key_before(lv, le, x, ex)) continue;
+            if (x > v0) {
+                v1 = v0; e1 = e0;
+                v0 = x; e0 = ex;
+            } else if (x > v1) {
+                v1 = x; e1 = ex;
+            }
+        }
+        left = 2;
+    }
+    __device__ __forceinline__ void init(const float (&sc)[kTopkPerLane], int lane) {
+        scan<true>(sc, lane, 0.f, 0);
+    }
+    __device__ __forceinline__ int next(const float (&sc)[kTopkPerLane], int lane) {
+        float bv = v0;
+        int be = e0;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (key_before(ov, oe, bv, be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (be == e0) {   // this lane's first key was taken
+            if (--left == 0) {
+                scan<false>(sc, lane, bv, be);
+            } else {
+                v0 = v1; e0 = e1;
+                v1 = -CUDART_INF_F; e1 = 0x7fffffff;
+            }
+        }
+        return be;
+    }
+};
 
 // Softmax, load-statistics partial sums, optional probs/probsT, optional
 // gate-entropy partial sum and top-k with renormalisation for a tile of TB
@@ -478,8 +522,10 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
         }
         float psum = 0.f, my_p = 0.f;
         int my_e = 0;
+        WarpTopK topk;
+        topk.init(sc, lane);
         for (int j = 0; j < a.k + a.n_cand; ++j) {
-            const int bi = warp_take_max(sc, lane);
+            const int bi = topk.next(sc, lane);
             const float pw = expf(row[bi] - m) / s;
             if (j < a.k) psum += pw;
             if (lane == j) { my_e = bi; my_p = pw; }
@@ -811,6 +857,43 @@ __device__ float radix_select_col(const float *col, int T, long long r, RadixScr
     return __uint_as_float(prefix);
 }
 
+// (v_lo, v_hi): the values of rank lo and lo + 1 (v_lo when lo + 1 == n) of
+// col[0..n); 512 threads, all of which must call it.
+__device__ float2 rank_pair(const float *col, int n, long long lo, RadixScratch &sc,
+                            unsigned *min_gt) {
+    const float v_lo = radix_select_col(col, n, lo, sc);
+    float v_hi = v_lo;
+    if (lo + 1 < n) {
+        if (threadIdx.x == 0) *min_gt = 0xffffffffu;
+        __syncthreads();
+        const unsigned vb = __float_as_uint(v_lo);
+        int le = 0;
+        unsigned mn = 0xffffffffu;
+        for (int i0 = threadIdx.x; i0 < n; i0 += kRadixBatch * blockDim.x) {
+            unsigned v[kRadixBatch];
+#pragma unroll
+            for (int q = 0; q < kRadixBatch; ++q) {
+                const int i = i0 + q * blockDim.x;
+                v[q] = i < n ? __float_as_uint(col[i]) : 0xffffffffu;
+            }
+#pragma unroll
+            for (int q = 0; q < kRadixBatch; ++q) {
+                if (i0 + q * (int)blockDim.x >= n) break;
+                if (v[q] <= vb) ++le;
+                else mn = min(mn, v[q]);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        if ((threadIdx.x & 31) == 0) atomicMin(min_gt, mn);
+        block_exclusive_scan_512(le, sc.warp_tot, &sc.total);
+        const long long n_le = sc.total;
+        v_hi = n_le >= lo + 2 ? v_lo : __uint_as_float(*min_gt);
+    }
+    __syncthreads();
+    return make_float2(v_lo, v_hi);
+}
+
 __global__ void __launch_bounds__(512) quantile_bias_kernel(const float *probsT, int T,
                                                             long long lo, float frac,
                                                             float *bias_out) {
@@ -818,36 +901,160 @@ __global__ void __launch_bounds__(512) quantile_bias_kernel(const float *probsT,
     __shared__ unsigned min_gt;
     extern __shared__ float colbuf[];
     const float *col = stage_col(probsT + (size_t)blockIdx.x * T, T, colbuf);
-    const float v_lo = radix_select_col(col, T, lo, sc);
-    float v_hi = v_lo;
-    if (lo + 1 < T) {
-        if (threadIdx.x == 0) min_gt = 0xffffffffu;
-        __syncthreads();
-        const unsigned vb = __float_as_uint(v_lo);
-        int le = 0;
-        unsigned mn = 0xffffffffu;
-        for (int i0 = threadIdx.x; i0 < T; i0 += kRadixBatch * blockDim.x) {
-            unsigned v[kRadixBatch];
-#pragma unroll
-            for (int q = 0; q < kRadixBatch; ++q) {
-                const int i = i0 + q * blockDim.x;
-                v[q] = i < T ? __float_as_uint(col[i]) : 0xffffffffu;
-            }
-#pragma unroll
-            for (int q = 0; q < kRadixBatch; ++q) {
-                if (i0 + q * (int)blockDim.x >= T) break;
-                if (v[q] <= vb) ++le;
-                else mn = min(mn, v[q]);
-            }
+    const float2 r = rank_pair(col, T, lo, sc, &min_gt);
+    if (threadIdx.x == 0) bias_out[blockIdx.x] = -(r.x + frac * (r.y - r.x));
+}
+
+// The same order statistics when they lie in the column's top tail (n_top =
+// T - lo values at ranks >= lo, a few hundred of T, as with many experts and
+// q = 1 - k/E).  The ranks are found by narrowing the column with thresholds
+// and counting, with few block barriers (a radix pass over a small array
+// costs about five):
+//  1. a threshold L from a fixed sample of kQSample values (every
+//     (T / kQSample)-th): kQPivots of the sample values are pivots, each
+//     counted against the whole sample; L is the largest pivot with at least
+//     m sample values >= it, m chosen so that about 3 n_top column values
+//     are >= L;
+//  2. one pass copies the column's values >= L (its c largest) to shared
+//     memory; ranks lo and lo + 1 of the column are then descending ranks
+//     n_top and n_top - 1 of the copies, provided c >= n_top;
+//  3. pivots taken from the copies, counted against them, give the largest
+//     threshold A with at least n_top copies >= A, and the copies >= A (c2 of
+//     them, a few more than n_top) are copied once more;
+//  4. each thread takes one of those and counts the ones above it and not
+//     below it: the value whose descending rank range holds n_top is v_lo,
+//     the one holding n_top - 1 is v_hi.
+// Whenever a count falls outside what the buffers hold (c outside [n_top,
+// kQCand], c2 > blockDim.x, no pivot qualifies) the kernel runs the radix
+// select of quantile_bias_kernel on the copies or on the whole column, so the
+// result is exact either way.
+constexpr int kQSample = 512, kQCand = 2048, kQPivots = 64;
+__device__ __forceinline__ void count_pivots(const float *vals, int n, const float *piv,
+                                             int *cnt) {
+    // kQPivots pivots x (blockDim.x / kQPivots) threads, each counting a
+    // slice of vals against its pivot; blockDim.x = 512
+    const int p = threadIdx.x >> 3, q = threadIdx.x & 7;
+    const float x = piv[p];
+    int c = 0;
+#pragma unroll 8
+    for (int i = q; i < n; i += 8) c += vals[i] >= x;
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    if (q == 0) cnt[p] = c;
+}
+// The largest pivot with at least `need` values >= it (warp 0 of the block
+// writes it to *out, or -1 as a bit pattern when no pivot qualifies).
+__device__ __forceinline__ void pick_pivot(const float *piv, const int *cnt, long long need,
+                                           unsigned *out) {
+    if (threadIdx.x >= 32) return;
+    unsigned best = 0u;
+    bool any = false;
+    for (int p = threadIdx.x; p < kQPivots; p += 32)
+        if (cnt[p] >= need) {
+            best = max(best, __float_as_uint(piv[p]));
+            any = true;
         }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-        if ((threadIdx.x & 31) == 0) atomicMin(&min_gt, mn);
-        block_exclusive_scan_512(le, sc.warp_tot, &sc.total);
-        const long long n_le = sc.total;
-        v_hi = n_le >= lo + 2 ? v_lo : __uint_as_float(min_gt);
+    for (int off = 16; off >= 1; off >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, off));
+    any = __any_sync(0xffffffffu, any);
+    if (threadIdx.x == 0) *out = any ? best : 0xffffffffu;
+}
+// Copies the values of src[0..n) >= thr (a bit pattern; values >= 0) to
+// dst[0..cap) in any order; returns their count (all threads).
+__device__ __forceinline__ int compact_ge(const float *src, int n, unsigned thr, float *dst,
+                                          int cap, int *counter) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid == 0) *counter = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += kRadixBatch * blockDim.x) {
+        unsigned xs[kRadixBatch];
+#pragma unroll
+        for (int q = 0; q < kRadixBatch; ++q) {
+            const int i = i0 + q * blockDim.x + tid;
+            xs[q] = i < n ? __float_as_uint(src[i]) : 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < kRadixBatch; ++q) {
+            const int i = i0 + q * blockDim.x + tid;
+            const bool take = i < n && xs[q] >= thr;
+            const unsigned bal = __ballot_sync(0xffffffffu, take);
+            if (!bal) continue;                          // uniform over the warp
+            int base = 0;
+            if (lane == 0) base = atomicAdd(counter, __popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const int pos = base + __popc(bal & ((1u << lane) - 1u));
+            if (take && pos < cap) dst[pos] = __uint_as_float(xs[q]);
+        }
     }
-    if (threadIdx.x == 0) bias_out[blockIdx.x] = -(v_lo + frac * (v_hi - v_lo));
+    __syncthreads();
+    return *counter;
+}
+__global__ void __launch_bounds__(512) quantile_tail_kernel(const float *probsT, int T,
+                                                            long long lo, float frac,
+                                                            float *bias_out) {
+    __shared__ RadixScratch sc;
+    __shared__ unsigned min_gt, thr;
+    __shared__ int counter, cnt[kQPivots];
+    __shared__ float samp[kQSample], piv[kQPivots];
+    __shared__ __align__(16) float cand[kQCand];
+    __shared__ __align__(16) float cand2[512];
+    __shared__ float res[2];
+    const int tid = threadIdx.x;
+    const float *col = probsT + (size_t)blockIdx.x * T;
+    const long long n_top = (long long)T - lo;
+    float2 r = make_float2(0.f, 0.f);
+    int path = 0;                    // 0: whole column, 1: the copies, 2: counted
+    int c = -1;                      // column values >= L
+    const long long m = (3 * n_top * kQSample + T - 1) / T + 2;   // sample count wanted
+    if (m <= kQSample) {
+        for (int j = tid; j < kQSample; j += blockDim.x) samp[j] = col[(long long)j * T / kQSample];
+        __syncthreads();
+        if (tid < kQPivots) piv[tid] = samp[tid * (kQSample / kQPivots) + kQSample / kQPivots / 2];
+        __syncthreads();
+        count_pivots(samp, kQSample, piv, cnt);
+        __syncthreads();
+        pick_pivot(piv, cnt, m, &thr);
+        __syncthreads();
+        const unsigned L = thr;
+        c = L == 0xffffffffu ? -1 : compact_ge(col, T, L, cand, kQCand, &counter);
+        if (c >= n_top && c <= kQCand) {
+            path = 1;
+            if (tid < kQPivots) piv[tid] = cand[(long long)tid * c / kQPivots];
+            __syncthreads();
+            count_pivots(cand, c, piv, cnt);
+            __syncthreads();
+            pick_pivot(piv, cnt, n_top, &thr);
+            __syncthreads();
+            const unsigned A = thr;
+            const int c2 = A == 0xffffffffu ? -1 : compact_ge(cand, c, A, cand2, 512, &counter);
+            if (c2 >= n_top && c2 <= (int)blockDim.x) {
+                path = 2;
+                // descending ranks (gt, ge]: v_lo holds n_top, v_hi holds n_top - 1
+                if (tid < c2) {
+                    const float v = cand2[tid];
+                    int gt = 0, ge = 0;
+                    const int c4 = c2 & ~3;
+                    for (int i = 0; i < c4; i += 4) {   // 16-byte reads (cand2 is 16-byte aligned)
+                        const float4 u = *reinterpret_cast<const float4 *>(cand2 + i);
+                        gt += (u.x > v) + (u.y > v) + (u.z > v) + (u.w > v);
+                        ge += (u.x >= v) + (u.y >= v) + (u.z >= v) + (u.w >= v);
+                    }
+                    for (int i = c4; i < c2; ++i) {
+                        gt += cand2[i] > v;
+                        ge += cand2[i] >= v;
+                    }
+                    if (gt < n_top && n_top <= ge) res[0] = v;
+                    if (n_top >= 2 && gt < n_top - 1 && n_top - 1 <= ge) res[1] = v;
+                }
+                __syncthreads();
+                r = make_float2(res[0], n_top >= 2 ? res[1] : res[0]);
+            }
+        }
+    }
+    if (path == 1) r = rank_pair(cand, c, c - n_top, sc, &min_gt);
+    if (path == 0) r = rank_pair(col, T, lo, sc, &min_gt);
+    if (tid == 0) bias_out[blockIdx.x] = -(r.x + frac * (r.y - r.x));
 }
 
 // --------------------------------------------------------------------------
@@ -855,7 +1062,7 @@ __global__ void __launch_bounds__(512) quantile_bias_kernel(const float *probsT,
 // quantile balancing, and the plain top-k of the unbiased counts): one warp
 // per token, the row read coalesced, top-k from registers.
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) select_rows_kernel(const float *probs, const float *bias,
+__global__ void __launch_bounds__(256, 3) select_rows_kernel(const float *probs, const float *bias,
                                                           int T, int E, int k, int32_t *idx,
                                                           float *w, int n_cand,
                                                           int32_t *cand_idx, float *cand_w) {
@@ -879,8 +1086,10 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const float *probs, co
     __syncwarp();
     float psum = 0.f, my_p = 0.f;
     int my_e = 0;
+    WarpTopK topk;
+    topk.init(sc, lane);
     for (int j = 0; j < k + n_cand; ++j) {
-        const int bi = warp_take_max(sc, lane);
+        const int bi = topk.next(sc, lane);
         const float pw = srow[bi];
         if (j < k) psum += pw;
         if (lane == j) { my_e = bi; my_p = pw; }
@@ -1035,6 +1244,13 @@ cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int
 cudaError_t launch_quantile_bias(const float *probsT, int T, int E, long long lo, float frac,
                                  float *bias_out, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
+    // a top tail of at most a sixth of the candidate buffer: the sampled kernel
+    const long long n_top = (long long)T - lo;
+    if (T >= 4 * kQSample && n_top * 6 <= kQCand) {
+        quantile_tail_kernel<<<E, 512, 0, st>>>(probsT, T, lo, frac, bias_out);
+        note_launch();
+        return cudaGetLastError();
+    }
     const size_t smem = stage_col_bytes(T);
     cudaError_t err = cudaFuncSetAttribute(quantile_bias_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
