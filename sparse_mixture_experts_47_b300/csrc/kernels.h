@@ -36,7 +36,9 @@ inline int router_slices(int d, int E, int dtype) {
     const int c = router_slice_cols(E, dtype);
     return (d + c - 1) / c;
 }
-int router_blocks(int T, int E, int dtype);
+// select: the softmax kernel also takes the top-k (false: quantile balance
+// and expert choice, which select later)
+int router_blocks(int T, int E, int dtype, bool select);
 size_t router_smem_bytes(int E, int dtype);
 cudaError_t launch_router(const RouterArgs &a, int dtype, float *part, cudaStream_t st);
 // W_r split into bf16 parts, and the tile table of the logit GEMM's single

@@ -84,6 +84,11 @@ Sizes sizes(const moe_config *c) {
 // group into its own fp32 plane, and the softmax adds the planes in group
 // order.  Chains and groups depend on d only, so a token's logits do not
 // depend on the batch it comes in (batch invariance).
+// The router's softmax kernel also takes the top-k, unless the selection
+// comes later (quantile balance, expert choice).
+bool router_selects(const moe_config *c) {
+    return !(c->quantile_balance || c->routing == MOE_ROUTING_EXPERT_CHOICE);
+}
 bool tc_router(const moe_config *c) {
     return c->dtype == MOE_DTYPE_BF16 && c->n_experts > 32 && c->n_experts % 4 == 0;
 }
@@ -232,7 +237,7 @@ long long n_candidates(const moe_config *c) {
 Layout layout(const moe_config *c) {
     const Sizes s = sizes(c);
     const size_t eb = elem_bytes(c->dtype);
-    const long long rb = router_blocks((int)s.T, (int)s.E, c->dtype);
+    const long long rb = router_blocks((int)s.T, (int)s.E, c->dtype, router_selects(c));
     const long long nb = dispatch_blocks(s.Tk);
     const FfnPlan rp = routed_plan(c), sp = shared_plan(c);
     const long long mt = max_tiles(s.R, (int)s.E, std::min(kSimtBM, rp.nt ? rp.nt : kSimtBM));
@@ -435,10 +440,12 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
         MOE_CUDA(launch_router(a, c->dtype, at<float>(ws, L.rt_logits), st));
     }
     if (p_out && s.T > 0)
-        MOE_CUDA(launch_p_finalize(a.p_partial, router_blocks(a.T, a.E, c->dtype), a.E, a.T,
+        MOE_CUDA(launch_p_finalize(a.p_partial,
+                                   router_blocks(a.T, a.E, c->dtype, a.do_select != 0), a.E, a.T,
                                    p_out, st));
     if (entropy_out && s.T > 0)
-        MOE_CUDA(launch_p_finalize(a.ent_partial, router_blocks(a.T, a.E, c->dtype), 1, a.T,
+        MOE_CUDA(launch_p_finalize(a.ent_partial,
+                                   router_blocks(a.T, a.E, c->dtype, a.do_select != 0), 1, a.T,
                                    entropy_out,
                                    st));
     if (c->quantile_balance && s.T > 0) {

@@ -366,21 +366,24 @@ __device__ __forceinline__ void load4_f32(const __nv_bfloat16 *p, float *v) {
 // Rescanning all scores for each of the 8 picks of the 896-expert layer kept
 // the ALU pipe 88 % busy.
 constexpr int kTopkPerLane = 32;   // E <= 1024
+// Score slots per lane for E experts: 8, 16 or 32.
+inline int topk_per_lane(int E) { return E <= 256 ? 8 : E <= 512 ? 16 : 32; }
 __device__ __forceinline__ bool key_before(float va, int ea, float vb, int eb) {
     return va > vb || (va == vb && ea < eb);
 }
+template <int PER>
 struct WarpTopK {
     float v0, v1;
     int e0, e1;
     int left;   // keys of the pair not taken yet
     // the lane's best two keys (after (lv, le) unless FIRST)
     template <bool FIRST>
-    __device__ __forceinline__ void scan(const float (&sc)[kTopkPerLane], int lane, float lv,
+    __device__ __forceinline__ void scan(const float (&sc)[PER], int lane, float lv,
                                          int le) {
         v0 = v1 = -CUDART_INF_F;
         e0 = e1 = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kTopkPerLane; ++i) {
+        for (int i = 0; i < PER; ++i) {
             const float x = sc[i];
             const int ex = lane + 32 * i;
             if (!FIRST && !key_before(lv, le, x, ex)) continue;
@@ -393,10 +396,10 @@ struct WarpTopK {
         }
         left = 2;
     }
-    __device__ __forceinline__ void init(const float (&sc)[kTopkPerLane], int lane) {
+    __device__ __forceinline__ void init(const float (&sc)[PER], int lane) {
         scan<true>(sc, lane, 0.f, 0);
     }
-    __device__ __forceinline__ int next(const float (&sc)[kTopkPerLane], int lane) {
+    __device__ __forceinline__ int next(const float (&sc)[PER], int lane) {
         float bv = v0;
         int be = e0;
 #pragma unroll
@@ -427,9 +430,11 @@ struct WarpTopK {
 // (TB/8)(w+1) - 1.  st_m, st_s, st_h hold TB floats each.  Without top-k
 // (do_select = 0) the tile is turned into probabilities in place and the
 // expert-major copy probsT is written from it in segments of TB tokens.
-template <int TB>
+template <int TB, int SEL = 2, int PER = kTopkPerLane>
 __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m, float *st_s,
                                      float *st_h, int t0) {
+    // SEL: 0 no top-k (probabilities only), 1 top-k, 2 as a.do_select says
+    const bool do_select = SEL == 2 ? (a.do_select != 0) : SEL == 1;
     constexpr int TPWR = TB / 8;
     const int E = a.E, lde = router_lde(E);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -460,7 +465,7 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
             st_s[tt] = s;
             st_h[tt] = t < a.T ? logf(s) - hz / s : 0.f;
         }
-        if (!a.do_select) {
+        if (!do_select) {
             for (int e = lane; e < E; e += 32) {
                 const float p = expf(row[e] - m) / s;
                 row[e] = p;
@@ -475,7 +480,7 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
     // Column pass: per-block partial sums of probs (fixed token order) and
     // the expert-major copy used by quantile balancing and expert choice.
     const int nt = min(TB, a.T - t0);
-    if (!a.do_select) {
+    if (!do_select) {
         for (int e = tid; e < E; e += 256) {
             float sum = 0.f;
             for (int tt = 0; tt < nt; ++tt) sum += lg[tt * lde + e];
@@ -502,7 +507,7 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
         for (int tt = 0; tt < TB; ++tt) tot += st_h[tt];
         a.ent_partial[blockIdx.x] = tot;
     }
-    if (!a.do_select) return;
+    if (!do_select) return;
     __syncthreads();
 
     // Top-k per token from the selection scores held in registers.
@@ -511,9 +516,9 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
         if (t >= a.T) break;
         const float *row = lg + tt * lde;
         const float m = st_m[tt], s = st_s[tt];
-        float sc[kTopkPerLane];
+        float sc[PER];
 #pragma unroll
-        for (int i = 0; i < kTopkPerLane; ++i) {
+        for (int i = 0; i < PER; ++i) {
             const int e = lane + 32 * i;
             sc[i] = -CUDART_INF_F;
             if (e < E)
@@ -522,7 +527,7 @@ __device__ void router_rows_epilogue(const RouterArgs &a, float *lg, float *st_m
         }
         float psum = 0.f, my_p = 0.f;
         int my_e = 0;
-        WarpTopK topk;
+        WarpTopK<PER> topk;
         topk.init(sc, lane);
         for (int j = 0; j < a.k + a.n_cand; ++j) {
             const int bi = topk.next(sc, lane);
@@ -671,7 +676,7 @@ __global__ void split_router_weight_kernel(const float *w_r, int E, int d, int d
 
 // Logits = sum of S partial products (fixed order) + logit offset, then the
 // same per-token epilogue as the SIMT router.
-template <int TB>
+template <int TB, int SEL, int PER>
 __global__ void __launch_bounds__(256) router_from_logits_kernel(RouterArgs a,
                                                                  const float *part, int S) {
     extern __shared__ __align__(16) float smem[];
@@ -725,7 +730,7 @@ __global__ void __launch_bounds__(256) router_from_logits_kernel(RouterArgs a,
         }
     }
     __syncthreads();
-    router_rows_epilogue<TB>(a, lg, st_m, st_s, st_h, t0);
+    router_rows_epilogue<TB, SEL, PER>(a, lg, st_m, st_s, st_h, t0);
 }
 
 // --------------------------------------------------------------------------
@@ -1062,6 +1067,7 @@ __global__ void __launch_bounds__(512) quantile_tail_kernel(const float *probsT,
 // quantile balancing, and the plain top-k of the unbiased counts): one warp
 // per token, the row read coalesced, top-k from registers.
 // --------------------------------------------------------------------------
+template <int PER>
 __global__ void __launch_bounds__(256, 3) select_rows_kernel(const float *probs, const float *bias,
                                                           int T, int E, int k, int32_t *idx,
                                                           float *w, int n_cand,
@@ -1072,9 +1078,9 @@ __global__ void __launch_bounds__(256, 3) select_rows_kernel(const float *probs,
     if (t >= T) return;
     const float *row = probs + (size_t)t * E;
     float *srow = srows + wib * E;
-    float sc[kTopkPerLane];
+    float sc[PER];
 #pragma unroll
-    for (int i = 0; i < kTopkPerLane; ++i) {
+    for (int i = 0; i < PER; ++i) {
         const int e = lane + 32 * i;
         sc[i] = -CUDART_INF_F;
         if (e < E) {
@@ -1086,7 +1092,7 @@ __global__ void __launch_bounds__(256, 3) select_rows_kernel(const float *probs,
     __syncwarp();
     float psum = 0.f, my_p = 0.f;
     int my_e = 0;
-    WarpTopK topk;
+    WarpTopK<PER> topk;
     topk.init(sc, lane);
     for (int j = 0; j < k + n_cand; ++j) {
         const int bi = topk.next(sc, lane);
@@ -1146,27 +1152,31 @@ static cudaError_t launch_partial(const RouterArgs &a, float *part, cudaStream_t
 }
 
 // Tokens per CTA of the router's softmax kernels: 8 warps x 32/EP tokens for
-// E <= 32; for E > 32, kTB (fp32 SIMT router) or kTBLogits (bf16, softmax
-// over the tensor-core logits: 16 tokens so that several CTAs fit an SM).
-constexpr int kTBLogits = 16;
-static int router_tokens_per_block(int E, int dtype) {
+// E <= 32; for E > 32, kTB (fp32 SIMT router) or, for the softmax over the
+// tensor-core logits (bf16), kTBLogits with top-k selection and
+// kTBLogitsProbs without it (quantile balance, expert choice): a tile of 8
+// tokens (29 KB of shared memory at E = 896) and no top-k state in registers
+// let more CTAs share an SM, which the latency-bound kernel needs.
+constexpr int kTBLogits = 16, kTBLogitsProbs = 8;
+static int router_tokens_per_block(int E, int dtype, bool select) {
     if (E <= 8) return 32;
     if (E <= 16) return 16;
     if (E <= 32) return 8;
-    return dtype == MOE_DTYPE_BF16 ? kTBLogits : kTB;
+    if (dtype != MOE_DTYPE_BF16) return kTB;
+    return select ? kTBLogits : kTBLogitsProbs;
 }
 
 // Blocks of the router's softmax kernels: the row count of the per-block
 // partial sums (p_partial, ent_partial).
-int router_blocks(int T, int E, int dtype) {
-    const int tb = router_tokens_per_block(E, dtype);
+int router_blocks(int T, int E, int dtype, bool select) {
+    const int tb = router_tokens_per_block(E, dtype, select);
     return (T + tb - 1) / tb;
 }
 
 template <int EP>
 static cudaError_t launch_small_epilogue(const RouterArgs &a, const float *part, int S,
                                          cudaStream_t st) {
-    router_small_epilogue_kernel<EP><<<router_blocks(a.T, a.E, MOE_DTYPE_FP32), 256, 0, st>>>(
+    router_small_epilogue_kernel<EP><<<router_blocks(a.T, a.E, MOE_DTYPE_FP32, true), 256, 0, st>>>(
         a, part, S);
     note_launch();
     return cudaGetLastError();
@@ -1218,25 +1228,46 @@ cudaError_t launch_split_router_weight(const float *w_r, int E, int d, int dp, i
     return cudaGetLastError();
 }
 
+template <int TB, int SEL, int PER>
+static cudaError_t launch_from_logits_tb(const RouterArgs &a, const float *part, int S,
+                                         cudaStream_t st) {
+    const size_t smem = sizeof(float) * ((size_t)TB * router_lde(a.E) + 3 * TB);
+    auto kern = router_from_logits_kernel<TB, SEL, PER>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    kern<<<(a.T + TB - 1) / TB, 256, smem, st>>>(a, part, S);
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_router_from_logits(const RouterArgs &a, const float *part, int S,
                                       cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
-    constexpr int TB = kTBLogits;
-    const size_t smem = sizeof(float) * ((size_t)TB * router_lde(a.E) + 3 * TB);
-    cudaError_t err = cudaFuncSetAttribute(router_from_logits_kernel<TB>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    router_from_logits_kernel<TB><<<(a.T + TB - 1) / TB, 256, smem, st>>>(a, part, S);
-    note_launch();
-    return cudaGetLastError();
+    if (!a.do_select) return launch_from_logits_tb<kTBLogitsProbs, 0, 8>(a, part, S, st);
+    switch (topk_per_lane(a.E)) {
+        case 8: return launch_from_logits_tb<kTBLogits, 1, 8>(a, part, S, st);
+        case 16: return launch_from_logits_tb<kTBLogits, 1, 16>(a, part, S, st);
+        default: return launch_from_logits_tb<kTBLogits, 1, 32>(a, part, S, st);
+    }
 }
 
 cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int E, int k,
                                int32_t *idx, float *w, cudaStream_t st, int n_cand,
                                int32_t *cand_idx, float *cand_w) {
     if (T == 0) return cudaSuccess;
-    select_rows_kernel<<<(T + 7) / 8, 256, sizeof(float) * 8 * E, st>>>(
-        probs, bias, T, E, k, idx, w, n_cand, cand_idx, cand_w);
+    const dim3 grid((T + 7) / 8);
+    const size_t smem = sizeof(float) * 8 * E;
+    const int per = topk_per_lane(E);
+    if (per == 8)
+        select_rows_kernel<8><<<grid, 256, smem, st>>>(probs, bias, T, E, k, idx, w, n_cand,
+                                                       cand_idx, cand_w);
+    else if (per == 16)
+        select_rows_kernel<16><<<grid, 256, smem, st>>>(probs, bias, T, E, k, idx, w, n_cand,
+                                                        cand_idx, cand_w);
+    else
+        select_rows_kernel<32><<<grid, 256, smem, st>>>(probs, bias, T, E, k, idx, w, n_cand,
+                                                        cand_idx, cand_w);
     note_launch();
     return cudaGetLastError();
 }
