@@ -409,7 +409,8 @@ int moe_debug_set_wait_hooks(uint64_t main_loop_limit_ns, int32_t stall_mma);
 
 /* Tuning and test switch of the 256-row SM-pair tiles (see
  * moe_ffn_plan_info.up_pair): 0 (default) the library's rule (experts
- * averaging at least 512 rows), -1 never (128-row or one-SM 256-row tiles
+ * averaging at least 512 rows, or loads balanced by quantile balancing or expert
+ * choice), -1 never (128-row or one-SM 256-row tiles
  * instead), 1 for every projection that runs token rows on the MMA's M side
  * (rows_per_tile = 0; its N is then 256).  Host-only; it applies to the calls
  * planned after it, on every device.  MOE_ERR_INVALID_ARG outside {-1, 0, 1}. */

@@ -143,20 +143,23 @@ constexpr double kVarPadGain = 1.3;
 constexpr long long kWideMinRows = 512;
 constexpr long long kWideMinK = 8192;
 // 256-row tiles on SM pairs (cta_group::2: 32 KB stages per SM, two
-// accumulators) for every nt = 0, N = 256 projection whose experts hold at
-// least kPairMinRows rows on average.  Measured on B300 against the one-SM
+// accumulators) for an nt = 0, N = 256 projection whose experts hold at least
+// kPairMinRows rows on average, or whose loads are balanced by construction
+// (quantile balancing, expert choice).  Measured on B300 against the one-SM
 // tiles: Switch T = 8192 (1024 rows per expert) 0.184 -> 0.170 ms and Mixtral
 // T = 4096 2.06 -> 2.00 ms at the same clock; Mixtral T = 16384 5 % fewer
-// cycles, about even in time under the power cap; DeepSeek T = 8192 (256
-// rows on average, most experts far fewer) slower, the padding rows of
-// 256-row tiles costing MMA work and power.
+// cycles, about even in time under the power cap; the 896-expert layer
+// (quantile-balanced, about 146 rows per expert, bound by HBM) 3.57 -> 3.49 ms,
+// one 256-row tile per expert reading each weight tile once instead of two
+// 128-row tiles reading it twice.  DeepSeek T = 8192 (256 rows on average,
+// most experts far fewer under its selection bias) and its capacity-limited
+// variant ran 10-15 % slower on pairs, at lower clocks: the padding rows of
+// light experts' 256-row tiles cost MMA work and power.
 constexpr long long kPairMinRows = 512;
-// moe_debug_set_pair_tiles: 0 the rule above, -1 never, 1 for every
-// projection with token rows on the M side (nt = 0; N set to 256).
 static int g_pair_policy = 0;
-static bool use_pair(long long per, int bn, int splits) {
+static bool use_pair(long long per, int bn, int splits, bool balanced) {
     if (g_pair_policy < 0 || bn != 256 || splits != 1) return false;
-    return g_pair_policy > 0 || per >= kPairMinRows;
+    return g_pair_policy > 0 || per >= kPairMinRows || balanced;
 }
 
 // Split the reduction only when the tiles do not fill the SMs once, and then
@@ -197,10 +200,13 @@ FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long lon
         if (mt * ((d + 255) / 256) < kPlanSMs) p.bn_down = 128;
         if (g_pair_policy > 0) p.bn_up = p.bn_down = 256;
         if (per >= kWideMinRows && F >= kWideMinK && p.bn_down == 256) p.mh_down = TILE_ROWS_256;
-        if (use_pair(per, p.bn_up, p.s_up)) p.mh_up = TILE_ROWS_256_PAIR;
+        // expert loads equal by construction: quantile balancing, expert choice
+        const bool balanced = groups > 1 && (c->quantile_balance ||
+                                             c->routing == MOE_ROUTING_EXPERT_CHOICE);
+        if (use_pair(per, p.bn_up, p.s_up, balanced)) p.mh_up = TILE_ROWS_256_PAIR;
         // the long-reduction down projection keeps its one-SM 256-row tiles
         // (measured at Mixtral T = 16384: 2.48 ms against 2.54-2.58 on pairs)
-        if (use_pair(per, p.bn_down, p.s_down) &&
+        if (use_pair(per, p.bn_down, p.s_down, balanced) &&
             (p.mh_down != TILE_ROWS_256 || g_pair_policy > 0))
             p.mh_down = TILE_ROWS_256_PAIR;
         const double pad128 = (double)((per + 127) / 128 * 128) / per;

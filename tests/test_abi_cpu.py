@@ -121,10 +121,12 @@ def test_ffn_plan_geometries():
     assert one["up_splits"] == 1 and one["down_splits"] > 1
     e896 = _plan("e896", 16384)              # about 146 rows per expert
     assert (e896["rows_per_tile"], e896["down_rows_per_tile"], e896["down_halves"]) == (0, 256, 1)
-    assert e896["up_pair"] == e896["down_pair"] == 0
+    assert e896["up_pair"] == 1 and e896["down_pair"] == 0   # balanced loads: SM pairs
     ds = _plan("deepseek", 8192)             # 256 rows per expert, reduction 2048 down
     assert (ds["rows_per_tile"], ds["down_rows_per_tile"], ds["down_halves"]) == (0, 0, 1)
-    assert ds["up_pair"] == ds["down_pair"] == 0
+    assert ds["up_pair"] == ds["down_pair"] == 0            # uneven experts: one-SM tiles
+    dsc = _plan("deepseek_cap", 8192)
+    assert dsc["up_pair"] == dsc["down_pair"] == 0
     assert _plan("switch", 8192)["up_pair"] == 1            # 1024 rows per expert
     sw = _plan("switch", 8192)               # 288 down tiles of N = 256: one round of SMs
     assert (sw["rows_per_tile"], sw["down_n"]) == (0, 256)
