@@ -390,13 +390,65 @@ __device__ __forceinline__ void store_y4(TO *y, long long i, float4 acc) {
     }
 }
 
-// One CTA per token: its slots' rows and weights are read once into shared
-// memory; each thread then holds U column vectors, with the U loads of a
-// slot in flight together, and adds the slots in j order.  U = 4 for k <= 2
-// (Mixtral's combine 0.139 -> 0.129 ms); with k = 8 the k loads of one
-// vector are already in flight, and U = 4 made it slower (0.36 -> 0.41 ms).
+// One warp per (token, chunk of U * 32 float4 columns): lane l holds columns
+// c0 + l + 32 u (u < U) of the token's output, loads the U vectors of a slot
+// together and adds the slots in j order (then the shared expert): the same
+// arithmetic per element for every chunk width.  U follows the grid: 8
+// vectors per lane when the batch fills the GPU, fewer when few tokens must
+// spread their columns over more warps (DeepSeek T = 128: 14 chunks of 128
+// columns per token instead of one CTA per token on 128 of 148 SMs).  One
+// CTA per token took 28 us for Switch's 8192 tokens of 4 KB of output each.
+template <typename TO, int U>
+__global__ void __launch_bounds__(256) combine_kernel(ExpertOut out_sorted, const int32_t *inv,
+                                                      const float *w, ExpertOut sh, int T, int k,
+                                                      int d4, int chunks, TO *y) {
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= (long long)T * chunks) return;
+    const long long t = gw / chunks;
+    const int c0 = (int)(gw - t * chunks) * (U * 32) + lane;
+    // slot rows and weights (k <= 16), spread to every lane
+    const int my_row = lane < k ? inv[t * k + lane] : -1;
+    const float my_w = lane < k ? w[t * k + lane] : 0.f;
+    float4 acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+        const int s = __shfl_sync(0xffffffffu, my_row, j);
+        const float wj = __shfl_sync(0xffffffffu, my_w, j);
+        if (s < 0) continue;
+        float4 o[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + 32 * u;
+            o[u] = c < d4 ? expert_out4(out_sorted, (long long)s * d4 + c)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            acc[u].x = fmaf(wj, o[u].x, acc[u].x); acc[u].y = fmaf(wj, o[u].y, acc[u].y);
+            acc[u].z = fmaf(wj, o[u].z, acc[u].z); acc[u].w = fmaf(wj, o[u].w, acc[u].w);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= d4) break;
+        if (sh.p) {
+            const float4 sv = expert_out4(sh, t * d4 + c);
+            acc[u].x += sv.x; acc[u].y += sv.y; acc[u].z += sv.z; acc[u].w += sv.w;
+        }
+        store_y4(y, t * d4 + c, acc[u]);
+    }
+}
+
+// One CTA per token (with more than 2 slots and enough tokens to fill the GPU):
+// its slots' rows and weights are read once into shared memory, each thread
+// takes one column vector at a time and adds the slots in j order.  At k = 8
+// this kept more loads in flight than a warp per column chunk (DeepSeek
+// T = 8192 0.345 against 0.40 ms, the 896-expert layer 0.343 against 0.38).
 template <typename TO, int kCombineU>
-__global__ void combine_kernel(ExpertOut out_sorted, const int32_t *inv, const float *w,
+__global__ void combine_token_kernel(ExpertOut out_sorted, const int32_t *inv, const float *w,
                                ExpertOut sh, int k, int d4, TO *y) {
     __shared__ int srow[16];
     __shared__ float sw[16];
@@ -440,22 +492,47 @@ __global__ void combine_kernel(ExpertOut out_sorted, const int32_t *inv, const f
     }
 }
 
+template <typename TO, int U>
+static void launch_combine_u(const ExpertOut &o, const int32_t *inv, const float *w,
+                             const ExpertOut &sh, int T, int k, int d4, TO *y, cudaStream_t st) {
+    const int chunks = (d4 + U * 32 - 1) / (U * 32);
+    const long long warps = (long long)T * chunks;
+    combine_kernel<TO, U><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(o, inv, w, sh, T, k, d4,
+                                                                        chunks, y);
+}
+
+template <typename TO>
+static void launch_combine_t(const ExpertOut &o, const int32_t *inv, const float *w,
+                             const ExpertOut &sh, int T, int k, int d4, TO *y, cudaStream_t st) {
+    // the widest chunk that still gives every SM about 32 warps; with more
+    // than 2 slots at most 2 vectors per lane
+    constexpr long long kWantWarps = 148 * 32;
+    auto warps = [&](int u) { return (long long)T * ((d4 + u * 32 - 1) / (u * 32)); };
+    if (k <= 2 && warps(8) >= kWantWarps) launch_combine_u<TO, 8>(o, inv, w, sh, T, k, d4, y, st);
+    else if (k <= 2 && warps(4) >= kWantWarps)
+        launch_combine_u<TO, 4>(o, inv, w, sh, T, k, d4, y, st);
+    else if (warps(2) >= kWantWarps) launch_combine_u<TO, 2>(o, inv, w, sh, T, k, d4, y, st);
+    else launch_combine_u<TO, 1>(o, inv, w, sh, T, k, d4, y, st);
+}
+
 cudaError_t launch_combine(const ExpertOut &o, const int32_t *inv, const float *w,
                            const ExpertOut &sh, int T, int k, int d, int out_dtype, void *y,
                            cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int d4 = d / 4;
-    const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
-    float *yf = static_cast<float *>(y);
-    __nv_bfloat16 *yb = static_cast<__nv_bfloat16 *>(y);
-    if (out_dtype == MOE_DTYPE_FP32 && k <= 2)
-        combine_kernel<float, 4><<<T, threads, 0, st>>>(o, inv, w, sh, k, d4, yf);
-    else if (out_dtype == MOE_DTYPE_FP32)
-        combine_kernel<float, 1><<<T, threads, 0, st>>>(o, inv, w, sh, k, d4, yf);
-    else if (k <= 2)
-        combine_kernel<__nv_bfloat16, 4><<<T, threads, 0, st>>>(o, inv, w, sh, k, d4, yb);
-    else
-        combine_kernel<__nv_bfloat16, 1><<<T, threads, 0, st>>>(o, inv, w, sh, k, d4, yb);
+    if (k > 2 && T >= 148 * 8) {
+        const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
+        if (out_dtype == MOE_DTYPE_FP32)
+            combine_token_kernel<float, 1><<<T, threads, 0, st>>>(o, inv, w, sh, k, d4,
+                                                                   static_cast<float *>(y));
+        else
+            combine_token_kernel<__nv_bfloat16, 1><<<T, threads, 0, st>>>(
+                o, inv, w, sh, k, d4, static_cast<__nv_bfloat16 *>(y));
+    } else if (out_dtype == MOE_DTYPE_FP32) {
+        launch_combine_t(o, inv, w, sh, T, k, d4, static_cast<float *>(y), st);
+    } else {
+        launch_combine_t(o, inv, w, sh, T, k, d4, static_cast<__nv_bfloat16 *>(y), st);
+    }
     note_launch();
     return cudaGetLastError();
 }
