@@ -30,6 +30,12 @@ CASES = {
     # 700 tokens
     "deepseek_T700": (mi.workload("deepseek").with_sizes(d_model=512, n_experts=16, d_ff=512,
                                                          d_ff_shared=512), 700),
+    # widths that fill no tile: the last K block (520 = 8 x 64 + 8), the last
+    # SwiGLU column tile (1000 = 7 x 128 + 104) and the last down tile
+    # (520 = 2 x 256 + 8) are partial
+    "mixtral_ragged_T1100": (mi.workload("mixtral").with_sizes(d_model=520, d_ff=1000), 1100),
+    # the same widths with the down projection on pairs too (375 rows per expert)
+    "mixtral_ragged_T1500": (mi.workload("mixtral").with_sizes(d_model=520, d_ff=1000), 1500),
 }
 
 
@@ -47,7 +53,9 @@ def test_pair_tiles_vs_oracle(name, pair_tiles):
     w, T = CASES[name]
     cfg = moe.config_for(w, T)
     plan = moe.ffn_plan(cfg)
-    assert plan["rows_per_tile"] == 0 and plan["up_pair"] == 1 and plan["down_pair"] == 1
+    assert plan["rows_per_tile"] == 0 and plan["up_pair"] == 1
+    # the down projection takes pairs unless its per-tile-width geometry applies
+    assert plan["down_pair"] == 1 or plan["down_rows_per_tile"] == 256
     if w.d_ff_shared:
         sh = moe.ffn_plan(cfg, shared=True)
         assert sh["up_pair"] == 1 and sh["down_pair"] == 1
@@ -57,6 +65,21 @@ def test_pair_tiles_vs_oracle(name, pair_tiles):
     print(name, rep)
     if w.capacity_factor > 0:
         assert int(gpu["n_dropped"][0]) > 0
+
+
+@pytest.mark.parametrize("name", ["mixtral_ragged_T1100", "mixtral_ragged_T1500"])
+def test_ragged_widths_one_sm_tiles(name):
+    """The same ragged layer on the one-SM tiles, against the oracle."""
+    w, T = CASES[name]
+    moe.debug_set_pair_tiles(-1)
+    try:
+        assert moe.ffn_plan(moe.config_for(w, T))["up_pair"] == 0
+        inp = mi.generate(w, T, DEV)
+        rep, _, _ = full_check(w, T, inp)
+        assert moe.device_status() == 0
+        print(name, rep)
+    finally:
+        moe.debug_set_pair_tiles(0)
 
 
 def test_pair_tiles_match_one_sm_tiles(pair_tiles):
