@@ -20,6 +20,7 @@ struct RouterArgs {
     int n_cand;           // experts ranked after the top k to report (0: none)
     int32_t *cand_idx;    // [T, n_cand] next-best experts, descending score
     float *cand_w;        // [T, n_cand] their probability over the top-k sum
+    float *p_direct;      // E <= 32 with one softmax block: p [E] written by that block
 };
 
 // router.cu

@@ -89,7 +89,9 @@ cudaError_t launch_prob_partials(const float *probs, int T, int E, float *p_part
 }
 
 // f_e = count_e / (T k); aux = E * sum_e f_e p_e (fp64, fixed tree order);
-// load = max_e count_e / (T k / E).  One CTA of 1024 threads, E <= 1024.
+// load = max_e count_e / (T k / E).  One CTA of n threads, n the power of two
+// >= E (32 to 1024): the tree over n leaves adds the same nonzero terms in the
+// same order as over 1024 (the other leaves are exact zeros).
 // Optional observability outputs (ObsArgs): drop_ratio = n_dropped / (T k);
 // bias_mean_abs, bias_max_abs = mean and max |b_e| of the selection bias in
 // effect (0 without one).
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(1024) stats_finalize_kernel(const int32_t *cou
     __shared__ double redb[1024];
     __shared__ float redbm[1024];
     __shared__ int redmax[1024];
-    const int e = threadIdx.x;
+    const int e = threadIdx.x, n = blockDim.x;
     const double tk = (double)T * (double)k;
     double fp = 0.0;
     int c = 0;
@@ -120,8 +122,7 @@ __global__ void __launch_bounds__(1024) stats_finalize_kernel(const int32_t *cou
     redb[e] = b;
     redbm[e] = b;
     __syncthreads();
-#pragma unroll
-    for (int off = 512; off >= 1; off >>= 1) {
+    for (int off = n / 2; off >= 1; off >>= 1) {
         if (e < off) {
             red[e] += red[e + off];
             redmax[e] = max(redmax[e], redmax[e + off]);
@@ -143,7 +144,9 @@ __global__ void __launch_bounds__(1024) stats_finalize_kernel(const int32_t *cou
 cudaError_t launch_stats_finalize(const int32_t *counts, const float *p, int T, int E, int k,
                                   float *f, float *p_out, float *aux, float *load,
                                   cudaStream_t st, const ObsArgs &o) {
-    stats_finalize_kernel<<<1, 1024, 0, st>>>(counts, p, T, E, k, f, p_out, aux, load, o);
+    int n = 32;
+    while (n < E && n < 1024) n *= 2;
+    stats_finalize_kernel<<<1, n, 0, st>>>(counts, p, T, E, k, f, p_out, aux, load, o);
     note_launch();
     return cudaGetLastError();
 }

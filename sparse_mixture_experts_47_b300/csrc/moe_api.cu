@@ -423,6 +423,10 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
     a.n_cand = (int)n_candidates(c);
     a.cand_idx = cand_out ? cand_out : at<int32_t>(ws, L.cand_idx);
     a.cand_w = at<float>(ws, L.cand_w);
+    // E <= 32 with a single softmax block (at most 32, 16 or 8 tokens for
+    // E <= 8, 16, 32): that block writes p itself, one launch fewer
+    a.p_direct = (!tc_router(c) && s.E <= 32 && p_out &&
+                  router_blocks(a.T, a.E, c->dtype, a.do_select != 0) == 1) ? p_out : nullptr;
     if (tc_router(c)) {
         const int dp = (int)router_dp(c);
         const int G = router_groups(c);
@@ -445,7 +449,7 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
     } else {
         MOE_CUDA(launch_router(a, c->dtype, at<float>(ws, L.rt_logits), st));
     }
-    if (p_out && s.T > 0)
+    if (p_out && s.T > 0 && !a.p_direct)
         MOE_CUDA(launch_p_finalize(a.p_partial,
                                    router_blocks(a.T, a.E, c->dtype, a.do_select != 0), a.E, a.T,
                                    p_out, st));

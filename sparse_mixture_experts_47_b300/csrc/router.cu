@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(256) router_small_epilogue_kernel(RouterArgs a
         for (int w = 0; w < 8; ++w)
             for (int g = 0; g < TPW; ++g) sum += red[w * 32 + g * EP + e];
         a.p_partial[(size_t)blockIdx.x * a.E + e] = sum;
+        // a batch of one block: the mean probability directly, as
+        // p_finalize_kernel computes it from one partial row
+        if (a.p_direct) a.p_direct[e] = (float)((double)sum / (double)a.T);
     }
     // Per-block sum of the tokens' gate entropies -sum_e p ln p, with
     // ln p = (logit - max) - ln(sum): fixed butterfly, then warps in order.
