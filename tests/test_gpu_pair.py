@@ -99,3 +99,32 @@ def test_pair_tiles_match_one_sm_tiles(pair_tiles):
     rms = float(np.sqrt(np.mean(b["y"].astype(np.float64) ** 2)))
     print(f"pair vs one-SM tiles: max |dy| = {diff:.3e} (RMS {rms:.3e})")
     assert diff <= 1e-2 * rms
+
+
+def test_pair_tiles_in_a_captured_graph(pair_tiles):
+    """The layer captured in a CUDA graph (LayerGraph) with the SM-pair
+    kernels (clusters of two CTAs) gives exactly the eager call's outputs,
+    batch by batch; so does the copy-overlapped pipeline."""
+    w, T = CASES["mixtral_T1000"]
+    inp = mi.generate(w, T, DEV)
+    cfg = moe.config_for(w, T, moe.DTYPE_BF16)
+    assert moe.ffn_plan(cfg)["up_pair"] == 1
+    wts = {k: inp.get(k) for k in moe._WEIGHT_KEYS}
+    g = torch.Generator(device=DEV)
+    g.manual_seed(5)
+    batches = [torch.randn(inp["x"].shape, generator=g, device=DEV).to(inp["x"].dtype)
+               for _ in range(3)]
+    eager = [moe.layer_forward(cfg, b, wts)["y"].float().cpu() for b in batches]
+    graph = moe.LayerGraph(cfg, batches[0].clone(), wts)
+    for b, ref in zip(batches, eager):
+        graph.x.copy_(b)
+        assert torch.equal(graph.replay()["y"].float().cpu(), ref)
+    xs = [b.cpu().pin_memory() for b in batches]
+    pipe = moe.LayerPipeline(cfg, wts, DEV)
+    pipe.OVERLAP_MIN_BYTES = 0
+    ys = [torch.empty((T, w.d_model), dtype=torch.bfloat16).pin_memory() for _ in batches]
+    pipe.run(xs, ys)
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    for y, ref in zip(ys, eager):
+        assert torch.equal(y.float(), ref)
