@@ -262,6 +262,17 @@ struct TileCoord {
     int e, m0, mend, n0, split, kb0, kb1;
 };
 
+// Serpentine reduction order: a CTA walks the K blocks of every second work
+// item backwards, so that each wave of tiles starts on the K blocks the
+// previous wave loaded last, which are still in L2 (token-row tiles only: the
+// router's chains keep their order, and swapped tiles stream weights that no
+// other item reads).  Only the fp32 order of the K blocks within a tile
+// changes, fixed by the item's position.
+template <int MODE, int NT>
+__device__ __forceinline__ bool serpentine(int it) {
+    return MODE != GEMM_LOGITS && NT == 0 && (it & 1);
+}
+
 // Work item L -> (split, expert, row tile, output-column tile, K-block
 // range).  Splits are outermost so that the CTAs in flight work on the same K
 // slice.  Inside an expert, output-column tiles are outer and row tiles inner
@@ -402,15 +413,17 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t issued = 0;       // stages that received a load
         uint32_t issued_par = 0;   // bit s: phase parity of stage s's last load
         bool ok = true;
-        for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+        for (int L = blockIdx.x, it = 0; L < total && ok; L += gridDim.x, ++it) {
             const TileCoord c = decode_tile<G::ROWS, G::OUTC, MODE == GEMM_LOGITS>(g, L, tiles, nk);
+            const bool rev = serpentine<MODE, NT>(it);
             int b0, b1;
             if (G::SWAP) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
             else if (MODE == GEMM_UP_SWIGLU) { b0 = c.e * g.b_rows + c.n0; b1 = b0; }
             else { b0 = c.e * g.b_rows + c.n0; b1 = b0 + BN / 2; }
             const int n16 = G::VARN ? tile_n16<G::ROWS>(c) : G::ROWS;
             const uint32_t stage_tx = G::W_BYTES + n16 * BK * 2;
-            for (int kb = c.kb0; kb < c.kb1; ++kb) {
+            for (int i = 0; i < c.kb1 - c.kb0; ++i) {
+                const int kb = rev ? c.kb1 - 1 - i : c.kb0 + i;
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
                 mbar_expect_tx(fb, stage_tx);
@@ -503,7 +516,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
             }
         } else {
-            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+            for (int L = blockIdx.x, it = 0; L < total && ok; L += gridDim.x, ++it) {
                 // The K range depends on the split alone; only the per-tile
                 // width (NT = 256) needs the tile table here.
                 const int kb0 = (L / tiles) * g.kb_per_split;
@@ -515,14 +528,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                // (the K blocks arrive in the producer's order; the first of
+                // them starts the accumulator)
+                for (int i = 0; i < kb1 - kb0; ++i) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * G::STAGE_BYTES);
                     const uint32_t sb = sa + G::ACT_BYTES;
     #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
                         if (G::SWAP) {
                             // weights (M side) x tokens (N side)
                             tc_mma(d_tmem, desc_sw128(sb + kk * 32), desc_sw128(sa + kk * 32), idesc,
@@ -897,11 +912,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t phase = 0;
         uint32_t issued = 0, issued_par = 0;
         bool ok = true;
-        for (int L = pair; L < tiles && ok; L += npairs) {
+        for (int L = pair, it = 0; L < tiles && ok; L += npairs, ++it) {
             const TileCoord c = decode_tile<kPairRows, P::OUTC>(g, L, tiles, nk);
             const CUtensorMap *tb = (MODE == GEMM_UP_SWIGLU && rank) ? &tmB1 : &tmB0;
             const int brow = c.e * g.b_rows + c.n0 + (MODE == GEMM_UP_SWIGLU ? 0 : WROWS * (int)rank);
-            for (int kb = c.kb0; kb < c.kb1; ++kb) {
+            const bool rev = serpentine<MODE, 0>(it);
+            for (int i = 0; i < c.kb1 - c.kb0; ++i) {
+                const int kb = rev ? c.kb1 - 1 - i : c.kb0 + i;
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
                 if (rank == 0) mbar_expect_tx(full0 + 8 * stage, 2 * P::STAGE_BYTES);
                 const uint32_t sa = smem_u32(smem + stage * P::STAGE_BYTES);
@@ -948,7 +965,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int i = 0; i < nk; ++i) {   // in the producers' order (serpentine)
                     if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * P::STAGE_BYTES);
@@ -956,7 +973,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         tc_mma_pair(d_tmem, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32),
-                                    idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                                    idesc, (i > 0 || kk > 0) ? 1u : 0u);
                     tc_commit_pair(empty0 + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
