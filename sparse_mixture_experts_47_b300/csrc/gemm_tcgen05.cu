@@ -34,8 +34,8 @@
 // its MMA N is that count rounded up to 16, so an expert with 146 rows costs
 // a 160-wide tile instead of two 128-row tiles.
 // GEMM_LOGITS (NT = 0, N = 256, or 224 where that pads the experts less):
-// the router's logits x W_r^T over a long
-// reduction cut into chains of equal K ranges (the tensor core's fp32
+// the router's logits x W_r^T over a long reduction cut into chains of equal
+// K ranges (the tensor core's fp32
 // accumulation loses precision along one long chain).  Chain 0 of a tile
 // accumulates into TMEM columns 0-255 (S), every later chain into columns
 // 256-511 (A); after each later chain the epilogue adds A into S in TMEM
@@ -44,6 +44,10 @@
 // K step sharing the weight tile, so a 64 KB stage feeds twice the MMA work
 // of a 48 KB one; the 256 x 256 fp32 accumulator fills TMEM, so there is one
 // accumulator and the epilogue does not overlap the next tile's MMAs.
+// SM pairs (grouped_gemm_pair_kernel, below): tiles of 256 token rows on a
+// cluster of two CTAs running one tcgen05.mma.cta_group::2 of M = 256, each
+// CTA staging half of the rows and half of the weight tile (32 KB stages,
+// two accumulators).
 // Every mbarrier wait is bounded (about 2 s of no progress); on expiry the
 // kernel sets the device error word, stops issuing, lets its own copies and
 // MMAs land, frees TMEM and returns.

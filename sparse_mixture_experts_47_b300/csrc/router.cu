@@ -9,10 +9,16 @@
 // "Kimi K3 → Quantile Balancing" (bias read off each expert's score
 // distribution so that the target share of tokens lands in the top-k).
 //
-// The logits are fp32 FFMA on CUDA cores (x widened from bf16/fp32, W_r fp32);
-// softmax with max subtraction and expf; exactly equal selection scores go to
-// the lower expert index.  Every reduction has a fixed order, so results are
-// bitwise reproducible.
+// Up to 32 experts (and for fp32 layers) the logits are fp32 FFMA on CUDA
+// cores (x widened from bf16/fp32, W_r fp32); above that a bf16 layer takes
+// them from the grouped tensor-core GEMM over a two-part bf16 split of W_r
+// (split_router_weight_kernel here, the GEMM in gemm_tcgen05.cu), and the
+// softmax kernel adds its planes.  Softmax with max subtraction and expf;
+// exactly equal selection scores go to the lower expert index.  Every
+// reduction has a fixed order, so results are bitwise reproducible.  With
+// quantile balancing the bias comes from order statistics of each expert's
+// column (quantile_tail_kernel / quantile_bias_kernel) and a second pass
+// selects (select_rows_kernel).
 #include "common.cuh"
 #include "kernels.h"
 
