@@ -37,6 +37,12 @@ inline int router_slices(int d, int E, int dtype) {
     const int c = router_slice_cols(E, dtype);
     return (d + c - 1) / c;
 }
+// The router's logits come from the tensor-core GEMM (bf16 x, E > 32,
+// E % 4 == 0: its fp32 planes are stored as float4 rows); otherwise from the
+// CUDA-core kernels of router.cu.
+inline bool router_on_tensor_cores(int E, int dtype) {
+    return dtype == MOE_DTYPE_BF16 && E > 32 && E % 4 == 0;
+}
 // select: the softmax kernel also takes the top-k (false: quantile balance
 // and expert choice, which select later)
 int router_blocks(int T, int E, int dtype, bool select);

@@ -89,9 +89,7 @@ Sizes sizes(const moe_config *c) {
 bool router_selects(const moe_config *c) {
     return !(c->quantile_balance || c->routing == MOE_ROUTING_EXPERT_CHOICE);
 }
-bool tc_router(const moe_config *c) {
-    return c->dtype == MOE_DTYPE_BF16 && c->n_experts > 32 && c->n_experts % 4 == 0;
-}
+bool tc_router(const moe_config *c) { return router_on_tensor_cores(c->n_experts, c->dtype); }
 long long router_dp(const moe_config *c) { return (c->d_model + 63) / 64 * 64; }
 constexpr int kRouterChainBlocks = 16;
 constexpr int kRouterParts = 2;

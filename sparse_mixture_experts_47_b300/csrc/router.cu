@@ -1161,8 +1161,9 @@ static cudaError_t launch_partial(const RouterArgs &a, float *part, cudaStream_t
 }
 
 // Tokens per CTA of the router's softmax kernels: 8 warps x 32/EP tokens for
-// E <= 32; for E > 32, kTB (fp32 SIMT router) or, for the softmax over the
-// tensor-core logits (bf16), kTBLogits with top-k selection and
+// E <= 32; for E > 32, kTB (the CUDA-core tiled router: fp32 layers, and bf16
+// ones whose E is not a multiple of 4) or, for the softmax over the
+// tensor-core logits, kTBLogits with top-k selection and
 // kTBLogitsProbs without it (quantile balance, expert choice): a tile of 8
 // tokens (29 KB of shared memory at E = 896) and no top-k state in registers
 // let more CTAs share an SM, which the latency-bound kernel needs.
@@ -1171,7 +1172,7 @@ static int router_tokens_per_block(int E, int dtype, bool select) {
     if (E <= 8) return 32;
     if (E <= 16) return 16;
     if (E <= 32) return 8;
-    if (dtype != MOE_DTYPE_BF16) return kTB;
+    if (!router_on_tensor_cores(E, dtype)) return kTB;   // router_tiled_kernel
     return select ? kTBLogits : kTBLogitsProbs;
 }
 

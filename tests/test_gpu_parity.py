@@ -50,6 +50,16 @@ SMALL = {
     "mixtral_cap_small": (mi.workload("mixtral_cap").with_sizes(d_model=512, d_ff=1024), 300),
     "deepseek_cap_small": (mi.workload("deepseek_cap").with_sizes(
         d_model=256, n_experts=64, d_ff=128, d_ff_shared=192), 400),
+    # router paths by expert count: 8 < E <= 32 (W_r slices in shared memory,
+    # 16 and 32 lanes per token), E > 32 not a multiple of 4 in a bf16 layer
+    # (the CUDA-core tiled router), and an fp32 layer with E > 32
+    "mixtral_E12": (mi.workload("mixtral").with_sizes(d_model=256, n_experts=12, d_ff=512), 300),
+    "mixtral_E24_k3": (mi.workload("mixtral").with_sizes(d_model=512, n_experts=24, top_k=3,
+                                                         d_ff=256), 400),
+    "deepseek_E50": (mi.workload("deepseek").with_sizes(d_model=256, n_experts=50, d_ff=128,
+                                                        d_ff_shared=192), 300),
+    "tiny_E40": (mi.workload("tiny").with_sizes(n_experts=40, top_k=3), 200),
+    "e896_E50": (mi.workload("e896").with_sizes(d_model=128, n_experts=50, d_ff=64), 600),
 }
 
 
