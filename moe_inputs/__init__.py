@@ -72,6 +72,7 @@ class MoEWorkload:
     quantile_balance: bool = False
     reroute_rounds: int = 0       # capacity overflow: 0 dropped, R > 0 redirected
     routing: str = "token"        # "token" (token choice) | "expert" (expert choice)
+    select_space: str = "probs"   # "probs" | "logits": what the selection bias is added to
 
     def with_sizes(self, **kw) -> "MoEWorkload":
         """A reduced copy (same recipe, smaller shapes) for small test cases."""

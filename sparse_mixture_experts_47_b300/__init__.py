@@ -598,7 +598,8 @@ def config_for(workload, T: int, out_dtype: int = DTYPE_FP32) -> MoEConfig:
         d_ff=workload.d_ff, act=ACT_SWIGLU if workload.act == "swiglu" else ACT_RELU,
         dtype=DTYPE_FP32 if workload.dtype == "fp32" else DTYPE_BF16,
         capacity_factor=float(workload.capacity_factor), d_ff_shared=workload.d_ff_shared,
-        select_space=SELECT_PROBS, quantile_balance=int(bool(workload.quantile_balance)),
+        select_space=SELECT_LOGITS if getattr(workload, "select_space", "probs") == "logits"
+        else SELECT_PROBS, quantile_balance=int(bool(workload.quantile_balance)),
         out_dtype=out_dtype, reroute_rounds=int(getattr(workload, "reroute_rounds", 0)),
         routing=ROUTING_EXPERT_CHOICE if getattr(workload, "routing", "token") == "expert"
         else ROUTING_TOKEN_CHOICE)

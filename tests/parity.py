@@ -68,12 +68,12 @@ def act_dtype(workload) -> str:
 
 def oracle_route(workload, inp) -> "om.RouterOut":
     return om.route(inp["x"], inp["w_r"], workload.top_k, inp.get("logit_bias"),
-                    inp.get("select_bias"), "probs", workload.quantile_balance)
+                    inp.get("select_bias"), workload.select_space, workload.quantile_balance)
 
 
 def oracle_layer(workload, inp, tokens=None, ranking=None, router=None):
     return om.moe_forward(inp, workload.top_k, workload.act, workload.capacity_factor,
-                          "probs", workload.quantile_balance, tokens, act_dtype(workload),
+                          workload.select_space, workload.quantile_balance, tokens, act_dtype(workload),
                           reroute_rounds=workload.reroute_rounds, ranking=ranking,
                           router=router)
 

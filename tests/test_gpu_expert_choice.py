@@ -162,6 +162,11 @@ SMALL = {
     "e896_ec_small": (mi.workload("e896").with_sizes(d_model=128, d_ff=64, capacity_factor=1.0,
                                                      routing="expert", quantile_balance=False),
                       2000),
+    # 50 experts in a bf16 layer: the CUDA-core tiled router writes the
+    # expert-major probabilities
+    "deepseek_ec_E50": (mi.workload("deepseek").with_sizes(
+        d_model=256, n_experts=50, d_ff=128, d_ff_shared=192, capacity_factor=1.0,
+        routing="expert", select_bias="none"), 400),
 }
 
 

@@ -60,6 +60,26 @@ SMALL = {
                                                         d_ff_shared=192), 300),
     "tiny_E40": (mi.workload("tiny").with_sizes(n_experts=40, top_k=3), 200),
     "e896_E50": (mi.workload("e896").with_sizes(d_model=128, n_experts=50, d_ff=64), 600),
+    # top-k at its largest (16): 32 experts on one warp per token, and 64
+    # experts on the tensor-core router with the selection bias
+    "mixtral_E32_k16": (mi.workload("mixtral").with_sizes(d_model=256, n_experts=32, top_k=16,
+                                                          d_ff=256), 200),
+    "deepseek_E64_k16": (mi.workload("deepseek").with_sizes(d_model=256, n_experts=64, top_k=16,
+                                                            d_ff=128, d_ff_shared=192), 300),
+    # the selection bias added to the logits instead of the probabilities, on
+    # each router path: 8 experts, 24 (W_r slices in shared memory), 50 (the
+    # CUDA-core tiled router), 64 (tensor cores), and an fp32 layer
+    "mixtral_logits": (mi.workload("mixtral").with_sizes(
+        d_model=256, d_ff=512, select_bias="uniform", select_space="logits"), 300),
+    "mixtral_E24_logits": (mi.workload("mixtral").with_sizes(
+        d_model=256, n_experts=24, top_k=3, d_ff=256, select_bias="uniform",
+        select_space="logits"), 300),
+    "deepseek_E50_logits": (mi.workload("deepseek").with_sizes(
+        d_model=256, n_experts=50, d_ff=128, d_ff_shared=192, select_space="logits"), 300),
+    "deepseek_logits": (mi.workload("deepseek").with_sizes(
+        d_model=256, n_experts=64, d_ff=128, d_ff_shared=192, select_space="logits"), 300),
+    "tiny_E40_logits": (mi.workload("tiny").with_sizes(n_experts=40, top_k=3, select_bias="uniform",
+                                                       select_space="logits"), 200),
 }
 
 

@@ -88,6 +88,14 @@ SMALL = {
         d_model=512, d_ff=1024, reroute_rounds=2), 300),
     "deepseek_cap_reroute_small": (mi.workload("deepseek_cap").with_sizes(
         d_model=256, n_experts=64, d_ff=128, d_ff_shared=192, reroute_rounds=2), 400),
+    # 16 slots and 16 candidates per token (the 32 the router can rank):
+    # every expert of 32 ranked, and 32 of 64 on the tensor-core router with
+    # the selection bias on the logits
+    "mixtral_cap_reroute_k16": (mi.workload("mixtral_cap").with_sizes(
+        d_model=256, n_experts=32, top_k=16, d_ff=256, reroute_rounds=1), 300),
+    "deepseek_cap_reroute_k16_logits": (mi.workload("deepseek_cap").with_sizes(
+        d_model=256, n_experts=64, top_k=16, d_ff=128, d_ff_shared=192, reroute_rounds=1,
+        select_space="logits"), 300),
 }
 
 
@@ -97,7 +105,7 @@ def test_layer_reroute_small_full_oracle(name):
     inp = mi.generate(w, T, DEV)
     rep, gpu, orc = full_check(w, T, inp, want_slots=True)
     print(name, rep)
-    plain = om.moe_forward(inp, w.top_k, w.act, w.capacity_factor, "probs", False, [0],
+    plain = om.moe_forward(inp, w.top_k, w.act, w.capacity_factor, w.select_space, False, [0],
                            "bf16")
     assert orc["dispatch"].n_dropped < plain["dispatch"].n_dropped   # redirection helps
     assert (orc["dispatch"].slot_round > 0).any()
