@@ -310,6 +310,8 @@ def run_ours(args, w, T):
     import sparse_mixture_experts_47_b300 as moe
     if args.pair_tiles:
         moe.debug_set_pair_tiles(args.pair_tiles)
+    if args.var_up:
+        moe.debug_set_var_up_tiles(args.var_up)
 
     world, rank, local = dist_setup(args)
     dev = torch.device("cuda", local if world > 1 else 0)
@@ -445,7 +447,10 @@ def run_ours(args, w, T):
                 "frac": up_gbs / peaks["hbm_gbs"], "peak_source": f"{src} hbm_gbs"}
     plan = moe.ffn_plan(cfg) if w.dtype == "bf16" else {}
     roof["kernel"] = ("grouped_gemm_pair_kernel (up projection, 256-row tiles on SM pairs)"
-                      if plan.get("up_pair") else "grouped_gemm_tc_kernel (up projection)")
+                      if plan.get("up_pair") else
+                      "grouped_gemm_tc_kernel (up projection, weights on the M side, the MMA N "
+                      "set per tile)" if plan.get("rows_per_tile") == 256 else
+                      "grouped_gemm_tc_kernel (up projection)")
     roof["algorithmic_per_launch"] = {"flops": up_flops, "bytes": up_bytes}
     roof["ms_per_launch"] = up_ms
     roof["traffic"] = None
@@ -533,6 +538,10 @@ def main():
     ap.add_argument("--pair-tiles", type=int, default=0, choices=[-1, 0, 1],
                     help="the library's switch of the 256-row SM-pair GEMM tiles: 0 its own "
                          "rule (default), -1 never, 1 wherever the geometry allows")
+    ap.add_argument("--var-up", type=int, default=0, choices=[-1, 0, 1],
+                    help="the library's switch of the up projection's per-tile-width "
+                         "geometry: 1 wherever the experts average more than 64 rows, "
+                         "0 (default) and -1 never")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     w = mi.workload(args.workload)

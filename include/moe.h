@@ -179,7 +179,8 @@ int64_t moe_reroute_candidates(const moe_config *cfg);
  * alone.  shared = 0: the routed experts; 1: the shared expert.
  *   rows_per_tile  up projection: 0 = 128 token rows on the MMA's M side;
  *                  16/32/64 = weights on the M side and that many token rows
- *                  on the N side (swap-AB, a few rows per expert)
+ *                  on the N side (swap-AB, a few rows per expert); 256 = up
+ *                  to 256 rows per tile with the MMA N set per tile
  *   up_splits, down_splits  reduction split over CTAs (partial sums added in
  *                  split order)
  *   up_n, down_n   MMA N of 128-row tiles (256, or 128 with few tiles)
@@ -415,6 +416,16 @@ int moe_debug_set_wait_hooks(uint64_t main_loop_limit_ns, int32_t stall_mma);
  * (rows_per_tile = 0; its N is then 256).  Host-only; it applies to the calls
  * planned after it, on every device.  MOE_ERR_INVALID_ARG outside {-1, 0, 1}. */
 int moe_debug_set_pair_tiles(int32_t policy);
+
+/* Tuning and test switch of the up projection's per-tile-width geometry
+ * (moe_ffn_plan_info.rows_per_tile = 256: weights on the MMA's M side, up to
+ * 256 of one expert's rows on its N side, the N rounded up to 16 per tile):
+ * 1 wherever the experts average more than 64 rows; 0 (default) and -1
+ * never (the library does not choose it by itself: on the workloads
+ * measured, token-row tiles ran the up projection faster).  The down
+ * projection keeps its own rule.  Host-only; it applies to the calls planned
+ * after it, on every device.  MOE_ERR_INVALID_ARG outside {-1, 0, 1}. */
+int moe_debug_set_var_up_tiles(int32_t policy);
 
 /* The architecture the library's kernels were compiled for, as the CUDA
  * runtime reports it for one of them on the current device (binaryVersion:

@@ -115,6 +115,8 @@ def _load():
     L.moe_debug_set_wait_hooks.restype = I
     L.moe_debug_set_pair_tiles.argtypes = [ctypes.c_int32]
     L.moe_debug_set_pair_tiles.restype = I
+    L.moe_debug_set_var_up_tiles.argtypes = [ctypes.c_int32]
+    L.moe_debug_set_var_up_tiles.restype = I
     L.moe_stage_timing_enable.argtypes = [I]; L.moe_stage_timing_enable.restype = I
     L.moe_stage_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int64)]
@@ -572,6 +574,13 @@ def debug_set_pair_tiles(policy: int = 0) -> None:
     0 the library's rule, -1 never, 1 for every projection with token rows on
     the MMA's M side."""
     _check("moe_debug_set_pair_tiles", lib.moe_debug_set_pair_tiles(int(policy)))
+
+
+def debug_set_var_up_tiles(policy: int = 0) -> None:
+    """Switch of the up projection's per-tile-width geometry (see
+    moe_debug_set_var_up_tiles): 1 wherever the experts average more than 64
+    rows, 0 (the default) and -1 never."""
+    _check("moe_debug_set_var_up_tiles", lib.moe_debug_set_var_up_tiles(int(policy)))
 
 
 def stage_timing(on: bool) -> None:

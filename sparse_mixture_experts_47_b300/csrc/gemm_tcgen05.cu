@@ -29,10 +29,11 @@
 // against a narrow token tile instead of padding 128 token rows.  The
 // reduction can then be split over CTAs (k_splits): each split writes fp32
 // partial sums that a later kernel adds in split order.
-// NT = 256 (down projection only) is the same swapped pipeline with the
-// MMA's N chosen per tile: a tile holds up to 256 of one expert's rows and
-// its MMA N is that count rounded up to 16, so an expert with 146 rows costs
-// a 160-wide tile instead of two 128-row tiles.
+// NT = 256 is the same swapped pipeline with the MMA's N chosen per tile: a
+// tile holds up to 256 of one expert's rows and its MMA N is that count
+// rounded up to 16, so an expert with 146 rows costs a 160-wide tile instead
+// of two 128-row tiles.  For SwiGLU the W1 and W3 parts of a tile fill the 512
+// TMEM columns, so there is one accumulator.
 // GEMM_LOGITS (NT = 0, N = 256, or 224 where that pads the experts less):
 // the router's logits x W_r^T over a long reduction cut into chains of equal
 // K ranges (the tensor core's fp32
@@ -94,7 +95,7 @@ template <int MODE, int NT, int BN, int MH> struct Geo {
     static_assert(MH == 1 || (MH == 2 && NT == 0 && BN == BNM), "256-row tiles: NT 0, N 256");
     static constexpr bool SWAP = NT > 0;
     static constexpr bool VARN = NT == kVarRows;                 // MMA N chosen per tile
-    static_assert(!VARN || MODE == GEMM_DOWN, "per-tile width: down projection only");
+    static_assert(!VARN || MODE != GEMM_LOGITS, "per-tile width: expert projections only");
     static constexpr int ROWS = SWAP ? NT : BM * MH;             // activation rows per tile
     static constexpr int WT = (SWAP && MODE == GEMM_UP_SWIGLU) ? 2 : 1;
     // rows of one weight TMA box: 128 (NT > 0), BN / 2 (NT = 0: two boxes)
@@ -117,7 +118,9 @@ template <int MODE, int NT, int BN, int MH> struct Geo {
              : MH == 2 ? 3
                        : (MODE == GEMM_LOGITS && BN != BNM) ? (FIT < 8 ? FIT : 8)
                                                             : (BN == BNM ? 4 : 6);
-    static constexpr int NACC = MH == 2 ? 1 : 2;                 // accumulator buffers
+    // accumulator buffers: one where a tile fills all 512 TMEM columns (two
+    // 256-column MMA halves, or SwiGLU's W1 and W3 parts of up to 256 tokens)
+    static constexpr int NACC = (MH == 2 || (VARN && MODE == GEMM_UP_SWIGLU)) ? 1 : 2;
     // output columns (features) of one tile
     static constexpr int OUTC = SWAP ? WROWS : (MODE == GEMM_UP_SWIGLU ? BN / 2 : BN);
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EXTRA;
@@ -1179,7 +1182,7 @@ static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args
         case 32: return launch_geo<MODE, 32, BNM>(m, g, st);
         case 64: return launch_geo<MODE, 64, BNM>(m, g, st);
         case kVarRows:
-            if constexpr (MODE == GEMM_DOWN) return launch_geo<MODE, kVarRows, BNM>(m, g, st);
+            if constexpr (MODE != GEMM_LOGITS) return launch_geo<MODE, kVarRows, BNM>(m, g, st);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
@@ -1189,8 +1192,7 @@ static cudaError_t launch_mode(int nt, int bn, int mh, const Maps &m, const Args
 
 // A [a_rows, a_cols], weights B0/B1 [E*b_rows, K]; tile table from
 // launch_build_tiles with row tiles of 128 (nt = 0) or nt rows (nt = 16, 32,
-// 64, 256: weights on the MMA's M side; 256, down projection only, sets the
-// MMA N per tile).  bn (nt = 0 only): MMA N of 256 or 128; 128 doubles the
+// 64, 256: weights on the MMA's M side; 256 sets the MMA N per tile).  bn (nt = 0 only): MMA N of 256 or 128; 128 doubles the
 // output tiles when there are too few to fill the SMs.  mh (nt = 0, bn = 256
 // only; tile table built with 256-row tiles): TILE_ROWS_256, 256-row tiles on
 // one SM; TILE_ROWS_256_PAIR, 256-row tiles on an SM pair (the up and down
@@ -1232,7 +1234,7 @@ cudaError_t launch_tc_gemm(int mode, int nt, int bn, int mh, const void *A, long
     const int kbps = (chains + k_splits - 1) / k_splits * unit;
     k_splits = (nk + kbps - 1) / kbps;          // every split gets at least one K block
     const bool var = nt == kVarRows;
-    if (var && mode != GEMM_DOWN) return cudaErrorInvalidValue;
+    if (var && mode == GEMM_LOGITS) return cudaErrorInvalidValue;
     // rows of one A box: one CTA's share of a tile
     const int rows = var ? 128 : nt ? nt : mh == TILE_ROWS_256_PAIR ? BM : BM * mh;
     Maps m;

@@ -159,6 +159,15 @@ static bool use_pair(long long per, int bn, int splits, bool balanced) {
     if (g_pair_policy < 0 || bn != 256 || splits != 1) return false;
     return g_pair_policy > 0 || per >= kPairMinRows || balanced;
 }
+// The up projection on the per-tile-width geometry (weights on the MMA's M
+// side, up to 256 of one expert's rows on its N side, rounded up to 16) only
+// on request (g_var_up_policy 1: wherever the experts average more than 64
+// rows; 0 and -1: never).  Measured on the 896-expert layer (about 146 rows
+// per expert), whose SwiGLU up projection streams 7.5 GB of W1 and W3 and is
+// bound by HBM: 1.56 ms against 1.46 ms on 256-row SM-pair tiles.  One
+// SwiGLU tile fills the 512 TMEM columns (no second accumulator), and its
+// 64 KB stages leave room for 3 (the pairs keep 7 of 32 KB in flight).
+static int g_var_up_policy = 0;
 
 // Split the reduction only when the tiles do not fill the SMs once, and then
 // only up to one round of work items: measured at the Mixtral shape, a split
@@ -209,11 +218,15 @@ FfnPlan ffn_plan(const moe_config *c, long long rows, long long groups, long lon
             p.mh_down = TILE_ROWS_256_PAIR;
         const double pad128 = (double)((per + 127) / 128 * 128) / per;
         const double pad16 = (double)((per + 15) / 16 * 16) / per;
+        const long long var_tiles = active * ((per + kVarTileRows - 1) / kVarTileRows);
         if (pad128 > kVarPadGain * pad16) {
             p.nt_down = kVarTileRows;
-            p.s_down = split_count(active * ((per + kVarTileRows - 1) / kVarTileRows) *
-                                       ((d + 127) / 128),
-                                   (F + 63) / 64);
+            p.s_down = split_count(var_tiles * ((d + 127) / 128), (F + 63) / 64);
+        }
+        if (g_var_up_policy > 0) {
+            p.nt = kVarTileRows;
+            p.mh_up = TILE_ROWS_128;
+            p.s_up = split_count(var_tiles * ((F + 127) / 128), (d + 63) / 64);
         }
         return p;
     }
@@ -732,6 +745,12 @@ int moe_ffn_plan(const moe_config *cfg, int32_t shared, moe_ffn_plan_info *out) 
 int moe_debug_set_pair_tiles(int32_t policy) {
     if (policy < -1 || policy > 1) return MOE_ERR_INVALID_ARG;
     g_pair_policy = policy;
+    return MOE_OK;
+}
+
+int moe_debug_set_var_up_tiles(int32_t policy) {
+    if (policy < -1 || policy > 1) return MOE_ERR_INVALID_ARG;
+    g_var_up_policy = policy;
     return MOE_OK;
 }
 

@@ -168,6 +168,28 @@ def test_pair_tiles_switch():
         moe.debug_set_pair_tiles(0)
 
 
+def test_var_up_tiles_switch():
+    """moe_debug_set_var_up_tiles: 1 takes the per-tile-width geometry for the
+    up projection wherever the experts average more than 64 rows; the down
+    projection keeps its own rule; 0 and -1 keep token-row tiles."""
+    try:
+        moe.debug_set_var_up_tiles(1)
+        p = _plan("e896", 16384)
+        assert (p["rows_per_tile"], p["up_pair"], p["down_rows_per_tile"]) == (256, 0, 256)
+        assert p["up_splits"] == 1
+        p = _plan("mixtral", 4096)                                   # 1024 rows per expert
+        assert (p["rows_per_tile"], p["up_pair"], p["down_rows_per_tile"]) == (256, 0, 0)
+        assert _plan("mixtral", 16)["rows_per_tile"] == 16           # swapped tiles stay
+        with pytest.raises(moe.MoEError):
+            moe.debug_set_var_up_tiles(2)
+        moe.debug_set_var_up_tiles(-1)
+        assert _plan("e896", 16384)["rows_per_tile"] == 0
+    finally:
+        moe.debug_set_var_up_tiles(0)
+    assert _plan("mixtral", 4096)["rows_per_tile"] == 0
+    assert _plan("e896", 16384)["rows_per_tile"] == 0
+
+
 def test_ffn_plan_rejects_fp32_and_missing_shared_expert():
     with pytest.raises(moe.MoEError):
         moe.ffn_plan(moe.config_for(mi.workload("tiny"), 64))             # fp32 layer

@@ -42,10 +42,12 @@ CASES = {
 @pytest.fixture
 def pair_tiles():
     moe.debug_set_pair_tiles(1)
+    moe.debug_set_var_up_tiles(-1)      # token rows on the M side for the up projection too
     try:
         yield
     finally:
         moe.debug_set_pair_tiles(0)
+        moe.debug_set_var_up_tiles(0)
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -72,14 +74,17 @@ def test_ragged_widths_one_sm_tiles(name):
     """The same ragged layer on the one-SM tiles, against the oracle."""
     w, T = CASES[name]
     moe.debug_set_pair_tiles(-1)
+    moe.debug_set_var_up_tiles(-1)
     try:
-        assert moe.ffn_plan(moe.config_for(w, T))["up_pair"] == 0
+        plan = moe.ffn_plan(moe.config_for(w, T))
+        assert plan["up_pair"] == 0 and plan["rows_per_tile"] == 0
         inp = mi.generate(w, T, DEV)
         rep, _, _ = full_check(w, T, inp)
         assert moe.device_status() == 0
         print(name, rep)
     finally:
         moe.debug_set_pair_tiles(0)
+        moe.debug_set_var_up_tiles(0)
 
 
 def test_pair_tiles_match_one_sm_tiles(pair_tiles):

@@ -18,18 +18,21 @@ DEV = "cuda"
 MOE_ERR_DEVICE_TIMEOUT = -5
 
 
-@pytest.mark.parametrize("sizes,T,pair", [
-    ({"d_model": 256, "d_ff": 512}, 300, 0),     # 128-row tiles
-    ({"d_model": 1024, "d_ff": 2048}, 5, 0),     # swapped, split
-    ({"d_model": 512, "d_ff": 2048}, 1000, 1),   # 256-row tiles on SM pairs
-], ids=["tiles128", "swapped", "pair"])
-def test_expired_wait_is_reported_and_the_context_stays_usable(sizes, T, pair):
+@pytest.mark.parametrize("sizes,T,pair,rows", [
+    ({"d_model": 256, "d_ff": 512}, 300, 0, 64),      # swapped, 64 token rows
+    ({"d_model": 1024, "d_ff": 2048}, 5, 0, 16),      # swapped, split
+    ({"d_model": 512, "d_ff": 2048}, 1000, 1, 0),     # 256-row tiles on SM pairs
+    ({"d_model": 512, "d_ff": 1024}, 1100, 0, 256),   # the MMA N set per tile (forced)
+], ids=["swapped64", "swapped", "pair", "var_width"])
+def test_expired_wait_is_reported_and_the_context_stays_usable(sizes, T, pair, rows):
     w = mi.workload("mixtral").with_sizes(**sizes)
     inp = mi.generate(w, T, DEV)
     cfg = moe.config_for(w, T)
     moe.debug_set_pair_tiles(pair)
+    moe.debug_set_var_up_tiles(1 if rows == 256 else 0)
     try:
-        assert moe.ffn_plan(cfg)["up_pair"] == pair
+        plan = moe.ffn_plan(cfg)
+        assert plan["up_pair"] == pair and plan["rows_per_tile"] == rows
         full_check(w, T, inp)                              # a healthy call first
         assert moe.device_status() == 0
         moe.debug_set_wait_hooks(1_000_000, True)
@@ -45,6 +48,7 @@ def test_expired_wait_is_reported_and_the_context_stays_usable(sizes, T, pair):
         assert moe.device_status() == 0
     finally:
         moe.debug_set_pair_tiles(0)
+        moe.debug_set_var_up_tiles(0)
 
 
 def test_hook_arguments_checked():
