@@ -11,10 +11,11 @@
 //   2. one CTA: counts[e] = sum_b hist[b][e], per-chunk bases
 //      base[b][e] = sum_{b'<b} hist[b'][e], offsets = exclusive scan of
 //      min(counts, C), n_dropped,
-//   3. per chunk, one warp walks its slots in order; the rank of a slot in
-//      its expert is base[b][e] + (earlier slots of e in the chunk), found
-//      with __match_any_sync; rank < C keeps the slot at row offsets[e] +
-//      rank.
+//   3. per chunk, 8 warps each walk 128 of its slots in order; the rank of
+//      a slot in its expert is base[b][e] + (earlier slots of e in the
+//      chunk: in earlier warps' ranges, counted first, then in its own warp,
+//      found with __match_any_sync); rank < C keeps the slot at row
+//      offsets[e] + rank.
 // A batch of at most one chunk (T*k <= 1024) runs the three steps in one
 // CTA instead, with the same results.
 #include "common.cuh"
@@ -95,21 +96,26 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
     }
 }
 
-// One warp per chunk.  The chunk's expert indices are loaded up front (32
-// per lane, coalesced) and the expert offsets staged in shared memory, so
-// the in-order walk below touches only registers and shared memory.
-__global__ void dispatch_scatter_kernel(const int32_t *idx, long long n, int E, long long C,
-                                        const int32_t *block_base, const int32_t *offsets,
-                                        int32_t *perm, int32_t *inv) {
-    extern __shared__ int run[];          // [E] running rank, then [E] offsets
-    int *off = run + E;
-    const int lane = threadIdx.x;
-    for (int i = lane; i < E; i += 32) {
-        run[i] = block_base[(size_t)blockIdx.x * E + i];
-        off[i] = offsets[i];
-    }
-    const long long base = (long long)blockIdx.x * kDispatchChunk;
-    constexpr int kIter = kDispatchChunk / 32;
+// One CTA of kScatterWarps warps per chunk; warp w walks its kScatterSlots
+// consecutive slots of the chunk in order.  Its starting rank in expert e is
+// the chunk's base[b][e] plus the slots of e in the chunk's earlier warps,
+// so the ranks are those of one in-order walk over the chunk.  The expert
+// indices are loaded up front and the ranks and offsets kept in shared
+// memory, so each walk touches only registers and shared memory.
+constexpr int kScatterWarps = 8;
+constexpr int kScatterSlots = kDispatchChunk / kScatterWarps;
+__global__ void __launch_bounds__(32 * kScatterWarps) dispatch_scatter_kernel(
+        const int32_t *idx, long long n, int E, long long C, const int32_t *block_base,
+        const int32_t *offsets, int32_t *perm, int32_t *inv) {
+    extern __shared__ int sh[];          // [kScatterWarps][E] counts, then ranks; [E] offsets
+    int *off = sh + kScatterWarps * E;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) sh[i] = 0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) off[i] = offsets[i];
+    __syncthreads();
+    const long long base = (long long)blockIdx.x * kDispatchChunk + warp * kScatterSlots;
+    constexpr int kIter = kScatterSlots / 32;
+    int *run = sh + warp * E;
     int ev[kIter];
 #pragma unroll
     for (int it = 0; it < kIter; ++it) {
@@ -120,8 +126,18 @@ __global__ void dispatch_scatter_kernel(const int32_t *idx, long long n, int E, 
             if (e < 0 || e >= E) e = -1;
         }
         ev[it] = e;
+        if (e >= 0) atomicAdd(&run[e], 1);
     }
-    __syncwarp();
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int r = block_base[(size_t)blockIdx.x * E + e];
+        for (int w = 0; w < kScatterWarps; ++w) {
+            const int c = sh[w * E + e];
+            sh[w * E + e] = r;
+            r += c;
+        }
+    }
+    __syncthreads();
 #pragma unroll
     for (int it = 0; it < kIter; ++it) {
         const long long f = base + it * 32 + lane;
@@ -231,8 +247,9 @@ cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long 
                                              n_dropped);
     note_launch();
     if (nblk > 0) {
-        dispatch_scatter_kernel<<<nblk, 32, 2 * sizeof(int) * E, st>>>(idx, n, E, C, block_base,
-                                                                       offsets, perm, inv);
+        dispatch_scatter_kernel<<<nblk, 32 * kScatterWarps,
+                                  (kScatterWarps + 1) * sizeof(int) * E, st>>>(
+            idx, n, E, C, block_base, offsets, perm, inv);
         note_launch();
     }
     return cudaGetLastError();

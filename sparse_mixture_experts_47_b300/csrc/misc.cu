@@ -293,18 +293,23 @@ __global__ void gather_rows_kernel(const uint4 *x, int vec_per_row, const int32_
     const long long t = perm[s] / k;
     const uint4 *src = x + t * vec_per_row;
     uint4 *dst = xs + s * vec_per_row;
-    // eight 16-byte loads in flight per lane before the stores; the grouped
-    // rows are written once and read by the up projection, so they are
-    // stored evict-first and leave L2 to x, which each token's k rows re-read
-    int i = lane;
-    for (; i + 224 < vec_per_row; i += 256) {
+    // up to eight 16-byte loads in flight per lane before the stores; the
+    // grouped rows are written once and read by the up projection, so they
+    // are stored evict-first and leave L2 to x, which each token's k rows
+    // re-read
+    for (int i0 = 0; i0 < vec_per_row; i0 += 256) {
         uint4 v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = src[i + 32 * q];
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + lane + 32 * q;
+            if (i < vec_per_row) v[q] = src[i];
+        }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) __stcs(dst + i + 32 * q, v[q]);
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + lane + 32 * q;
+            if (i < vec_per_row) __stcs(dst + i, v[q]);
+        }
     }
-    for (; i < vec_per_row; i += 32) __stcs(dst + i, src[i]);
 }
 
 cudaError_t launch_gather_rows(const void *x, int elem_bytes, int d, const int32_t *perm,
@@ -335,24 +340,25 @@ __global__ void scatter_rows_kernel(const uint4 *x, int vec_per_row, const int32
 #pragma unroll
     for (int j = 0; j < 16; ++j) rows[j] = __shfl_sync(0xffffffffu, my_row, j);
     const uint4 *src = x + t * vec_per_row;
-    int i = lane;
-    for (; i + 224 < vec_per_row; i += 256) {
+    // up to 8 16-byte loads per lane in flight before the stores (a row of
+    // 1024 bf16 is 4 per lane)
+    for (int i0 = 0; i0 < vec_per_row; i0 += 256) {
         uint4 v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = src[i + 32 * q];
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + lane + 32 * q;
+            if (i < vec_per_row) v[q] = src[i];
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             if (j >= k || rows[j] < 0) continue;
             uint4 *dst = xs + (long long)rows[j] * vec_per_row;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) __stcs(dst + i + 32 * q, v[q]);
+            for (int q = 0; q < 8; ++q) {
+                const int i = i0 + lane + 32 * q;
+                if (i < vec_per_row) __stcs(dst + i, v[q]);
+            }
         }
-    }
-    for (; i < vec_per_row; i += 32) {
-        const uint4 v = src[i];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (j < k && rows[j] >= 0) __stcs(xs + (long long)rows[j] * vec_per_row + i, v);
     }
 }
 

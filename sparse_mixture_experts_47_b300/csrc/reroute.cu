@@ -106,28 +106,42 @@ __global__ void __launch_bounds__(1024) rr_scan_kernel(const int32_t *hist, int 
     if (counts) counts[e] = run;
 }
 
-// Per chunk, one warp walks its slots in order: the rank of a live slot among
-// this round's slots of its expert is block_base + earlier slots of the same
-// expert in the chunk; it is served when the rank fits in the room left.
-__global__ void rr_scatter_kernel(const int32_t *slot_e, int32_t *served, long long n, int E,
-                                  long long C, const int32_t *block_base,
-                                  const int32_t *filled_before) {
-    extern __shared__ int run[];          // [E] running rank, then [E] rows before the round
-    int *fb = run + E;
-    const int lane = threadIdx.x;
-    for (int i = lane; i < E; i += 32) {
-        run[i] = block_base[(size_t)blockIdx.x * E + i];
-        fb[i] = filled_before[i];
-    }
-    const long long base = (long long)blockIdx.x * kDispatchChunk;
-    constexpr int kIter = kDispatchChunk / 32;
+// Per chunk, 8 warps each walk 128 of its slots in order: the rank of a live
+// slot among this round's slots of its expert is block_base + earlier slots
+// of the same expert in the chunk (in earlier warps' ranges, counted first,
+// then in its own warp); it is served when the rank fits in the room left.
+constexpr int kRrWarps = 8;
+constexpr int kRrSlots = kDispatchChunk / kRrWarps;
+__global__ void __launch_bounds__(32 * kRrWarps) rr_scatter_kernel(
+        const int32_t *slot_e, int32_t *served, long long n, int E, long long C,
+        const int32_t *block_base, const int32_t *filled_before) {
+    extern __shared__ int sh[];    // [kRrWarps][E] counts, then ranks; [E] rows before the round
+    int *fb = sh + kRrWarps * E;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kRrWarps * E; i += blockDim.x) sh[i] = 0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) fb[i] = filled_before[i];
+    __syncthreads();
+    const long long base = (long long)blockIdx.x * kDispatchChunk + warp * kRrSlots;
+    constexpr int kIter = kRrSlots / 32;
+    int *run = sh + warp * E;
     int ev[kIter];
 #pragma unroll
     for (int it = 0; it < kIter; ++it) {
         const long long f = base + it * 32 + lane;
-        ev[it] = (f < n && served[f] < 0) ? slot_e[f] : -1;
+        const int e = (f < n && served[f] < 0) ? slot_e[f] : -1;
+        ev[it] = e;
+        if (e >= 0) atomicAdd(&run[e], 1);
     }
-    __syncwarp();
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int r = block_base[(size_t)blockIdx.x * E + e];
+        for (int w = 0; w < kRrWarps; ++w) {
+            const int c = sh[w * E + e];
+            sh[w * E + e] = r;
+            r += c;
+        }
+    }
+    __syncthreads();
 #pragma unroll
     for (int it = 0; it < kIter; ++it) {
         if (base + it * 32 >= n) break;
@@ -212,9 +226,8 @@ cudaError_t launch_dispatch_reroute(const int32_t *topk_idx, const float *topk_w
                                            w.filled_before, r == 0 ? counts : nullptr);
         note_launch();
         if (nblk > 0) {
-            rr_scatter_kernel<<<nblk, 32, 2 * sizeof(int) * E, st>>>(w.slot_e, w.served, n, E, C,
-                                                                     w.block_base,
-                                                                     w.filled_before);
+            rr_scatter_kernel<<<nblk, 32 * kRrWarps, (kRrWarps + 1) * sizeof(int) * E, st>>>(
+                w.slot_e, w.served, n, E, C, w.block_base, w.filled_before);
             note_launch();
         }
     }
