@@ -17,7 +17,10 @@
 //      found with __match_any_sync); rank < C keeps the slot at row
 //      offsets[e] + rank.
 // A batch of at most one chunk (T*k <= 1024) runs the three steps in one
-// CTA instead, with the same results.
+// CTA instead, with the same results.  In the layer, the CTA that computes
+// the offsets (step 2, or the one-CTA form) also computes the load
+// statistics and the up projection's tile table from them (DispatchTail).
+#include "block_ops.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -64,7 +67,7 @@ __device__ int block_exclusive_scan_1024(int v, int *warp_tot, int *total) {
 
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
         const int32_t *hist, int nblk, int E, long long C, int32_t *block_base,
-        int32_t *counts, int32_t *offsets, int32_t *n_dropped) {
+        int32_t *counts, int32_t *offsets, int32_t *n_dropped, DispatchTail tail) {
     __shared__ int warp_tot[32];
     __shared__ int total;
     const int e = threadIdx.x;
@@ -93,6 +96,10 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
     if (e == 0) {
         if (offsets) offsets[E] = total;
         if (n_dropped) *n_dropped = all_total - total;
+    }
+    if (tail.stats || tail.tile_rows > 0) {
+        __syncthreads();
+        dispatch_tail(tail, run, E, offsets);
     }
 }
 
@@ -166,7 +173,8 @@ __global__ void __launch_bounds__(32 * kScatterWarps) dispatch_scatter_kernel(
 __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t *idx, int n, int E,
                                                               long long C, int32_t *counts,
                                                               int32_t *offsets, int32_t *perm,
-                                                              int32_t *inv, int32_t *n_dropped) {
+                                                              int32_t *inv, int32_t *n_dropped,
+                                                              DispatchTail tail) {
     extern __shared__ int sh[];          // [E] counts, then running ranks; [E] offsets
     int *h = sh, *off = sh + E;
     __shared__ int warp_tot[32];
@@ -200,6 +208,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t *idx
         if (n_dropped) *n_dropped = all_total - total;
     }
     __syncthreads();
+    if (tail.stats || tail.tile_rows > 0) dispatch_tail(tail, run, E, offsets);
     if (tid >= 32) return;
     const int lane = tid;
     for (int b = 0; b < n; b += 32) {
@@ -230,12 +239,19 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t *idx
 cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long long C,
                             int32_t *hist, int32_t *block_base, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *n_dropped,
-                            cudaStream_t st) {
+                            cudaStream_t st, const DispatchTail *tail) {
     (void)k;
+    DispatchTail t{};
+    if (tail) {
+        t = *tail;
+        // the tail reads offsets and n_dropped as this launch writes them
+        if ((t.tile_rows > 0 && !offsets) || (t.o.drop_ratio && t.o.n_dropped != n_dropped))
+            return cudaErrorInvalidValue;
+    }
     const int nblk = dispatch_blocks(n);
     if (nblk == 1) {
         dispatch_small_kernel<<<1, 1024, 2 * sizeof(int) * E, st>>>(
-            idx, (int)n, E, C, counts, offsets, perm, inv, n_dropped);
+            idx, (int)n, E, C, counts, offsets, perm, inv, n_dropped, t);
         note_launch();
         return cudaGetLastError();
     }
@@ -244,7 +260,7 @@ cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long 
         note_launch();
     }
     dispatch_scan_kernel<<<1, 1024, 0, st>>>(hist, nblk, E, C, block_base, counts, offsets,
-                                             n_dropped);
+                                             n_dropped, t);
     note_launch();
     if (nblk > 0) {
         dispatch_scatter_kernel<<<nblk, 32 * kScatterWarps,
@@ -263,7 +279,7 @@ cudaError_t launch_histogram(const int32_t *idx, long long n, int E, int32_t *hi
         note_launch();
     }
     dispatch_scan_kernel<<<1, 1024, 0, st>>>(hist, nblk, E, (long long)1 << 40, nullptr, counts,
-                                             nullptr, nullptr);
+                                             nullptr, nullptr, DispatchTail{});
     note_launch();
     return cudaGetLastError();
 }

@@ -62,13 +62,34 @@ cudaError_t launch_select_rows(const float *probs, const float *bias, int T, int
 cudaError_t launch_quantile_bias(const float *probsT, int T, int E, long long lo, float frac,
                                  float *bias_out, cudaStream_t st);
 
+// Optional observability outputs of the load statistics (any pointer may be
+// NULL).
+struct ObsArgs {
+    const int32_t *n_dropped;   // in: dropped assignments
+    const float *bias;          // in: selection bias in effect [E]
+    float *drop_ratio, *bias_mean_abs, *bias_max_abs;
+};
+
 // dispatch.cu
 constexpr int kDispatchChunk = 1024;
 inline int dispatch_blocks(long long n) { return (int)((n + kDispatchChunk - 1) / kDispatchChunk); }
+// Work that the dispatch kernel computing the counts and offsets does after
+// them, in place of separate launches: the load statistics (stats_finalize's
+// outputs, from counts, n_dropped and the router's mean probabilities p) and
+// the tile table of the up projection (build_tiles with tile_rows-row tiles).
+struct DispatchTail {
+    bool stats;
+    const float *p;
+    int T, k;
+    float *f, *aux, *load;
+    ObsArgs o;                   // o.n_dropped: the dispatch's own n_dropped
+    int tile_rows;               // 0: no tile table
+    int32_t *tile_e, *tile_start, *n_tiles;
+};
 cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long long C,
                             int32_t *hist, int32_t *block_base, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *n_dropped,
-                            cudaStream_t st);
+                            cudaStream_t st, const DispatchTail *tail = nullptr);
 cudaError_t launch_histogram(const int32_t *idx, long long n, int E, int32_t *hist,
                              int32_t *counts, cudaStream_t st);
 
@@ -93,12 +114,6 @@ cudaError_t launch_p_finalize(const float *p_partial, int nblk, int E, int T, fl
                               cudaStream_t st);
 cudaError_t launch_prob_partials(const float *probs, int T, int E, float *p_partial,
                                  cudaStream_t st);
-// Optional observability outputs of stats_finalize (any pointer may be NULL).
-struct ObsArgs {
-    const int32_t *n_dropped;   // in: dropped assignments
-    const float *bias;          // in: selection bias in effect [E]
-    float *drop_ratio, *bias_mean_abs, *bias_max_abs;
-};
 cudaError_t launch_stats_finalize(const int32_t *counts, const float *p, int T, int E, int k,
                                   float *f, float *p_out, float *aux, float *load,
                                   cudaStream_t st, const ObsArgs &o = ObsArgs{});

@@ -8,6 +8,7 @@
 // probability, aux = E sum f p); "混合エキスパートモデル（MoE）実践"
 // (deepseekmodel.com), expert-parallel dispatch/combine (x[order // k],
 // index_add_ back to token order).
+#include "block_ops.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -88,57 +89,17 @@ cudaError_t launch_prob_partials(const float *probs, int T, int E, float *p_part
     return cudaGetLastError();
 }
 
-// f_e = count_e / (T k); aux = E * sum_e f_e p_e (fp64, fixed tree order);
-// load = max_e count_e / (T k / E).  One CTA of n threads, n the power of two
-// >= E (32 to 1024): the tree over n leaves adds the same nonzero terms in the
-// same order as over 1024 (the other leaves are exact zeros).
-// Optional observability outputs (ObsArgs): drop_ratio = n_dropped / (T k);
-// bias_mean_abs, bias_max_abs = mean and max |b_e| of the selection bias in
-// effect (0 without one).
+// Load statistics and observability outputs (block_load_stats) in one CTA of
+// n threads, n the power of two >= E (32 to 1024).
 __global__ void __launch_bounds__(1024) stats_finalize_kernel(const int32_t *counts,
                                                               const float *p, int T, int E,
                                                               int k, float *f, float *p_out,
                                                               float *aux, float *load,
                                                               ObsArgs o) {
-    __shared__ double red[1024];
-    __shared__ double redb[1024];
-    __shared__ float redbm[1024];
-    __shared__ int redmax[1024];
-    const int e = threadIdx.x, n = blockDim.x;
-    const double tk = (double)T * (double)k;
-    double fp = 0.0;
-    int c = 0;
-    float b = 0.f;
-    if (e < E) {
-        c = counts ? counts[e] : 0;
-        const double fe = tk > 0 ? (double)c / tk : 0.0;
-        if (f) f[e] = (float)fe;
-        if (p && p_out && p_out != p) p_out[e] = p[e];
-        fp = p ? fe * (double)p[e] : 0.0;
-        if (o.bias) b = fabsf(o.bias[e]);
-    }
-    red[e] = fp;
-    redmax[e] = c;
-    redb[e] = b;
-    redbm[e] = b;
-    __syncthreads();
-    for (int off = n / 2; off >= 1; off >>= 1) {
-        if (e < off) {
-            red[e] += red[e + off];
-            redmax[e] = max(redmax[e], redmax[e + off]);
-            redb[e] += redb[e + off];
-            redbm[e] = fmaxf(redbm[e], redbm[e + off]);
-        }
-        __syncthreads();
-    }
-    if (e == 0) {
-        if (aux) *aux = (float)((double)E * red[0]);
-        if (load) *load = tk > 0 ? (float)((double)redmax[0] / (tk / (double)E)) : 0.f;
-        if (o.drop_ratio)
-            *o.drop_ratio = (o.n_dropped && tk > 0) ? (float)((double)*o.n_dropped / tk) : 0.f;
-        if (o.bias_mean_abs) *o.bias_mean_abs = (float)(redb[0] / (double)E);
-        if (o.bias_max_abs) *o.bias_max_abs = redbm[0];
-    }
+    __shared__ StatsSmem sm;
+    const int e = threadIdx.x;
+    const int c = (e < E && counts) ? counts[e] : 0;
+    block_load_stats(sm, blockDim.x, c, p, T, E, k, f, p_out, aux, load, o);
 }
 
 cudaError_t launch_stats_finalize(const int32_t *counts, const float *p, int T, int E, int k,
@@ -696,55 +657,12 @@ cudaError_t launch_sum_planes(const float *P, int splits, long long plane, int d
     return cudaGetLastError();
 }
 
-// Tile table of a grouped GEMM with BM-row tiles: expert e owns
-// ceil((offsets[e+1]-offsets[e]) / BM) tiles starting at row offsets[e];
-// tile_start[e] is the index of its first tile (tile_start[E] = total).
+// Tile table of a grouped GEMM with BM-row tiles (block_build_tiles).
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *offsets, int E,
                                                            int BM, int32_t *tile_e,
                                                            int32_t *tile_m0, int32_t *tile_start,
                                                            int32_t *n_tiles) {
-    __shared__ int warp_tot[32];
-    __shared__ int carry;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
-    for (int e0 = 0; e0 < E; e0 += 1024) {
-        const int e = e0 + threadIdx.x;
-        int mt = 0;
-        if (e < E) mt = (offsets[e + 1] - offsets[e] + BM - 1) / BM;
-        int incl = mt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const int wt = warp_tot[lane];
-            int wi = wt;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, wi, off);
-                if (lane >= off) wi += o;
-            }
-            warp_tot[lane] = wi - wt;
-        }
-        __syncthreads();
-        const int start = carry + warp_tot[warp] + incl - mt;
-        if (e < E && tile_start) tile_start[e] = start;
-        for (int i = 0; i < mt; ++i) {
-            tile_e[start + i] = e;
-            if (tile_m0) tile_m0[start + i] = offsets[e] + i * BM;
-        }
-        __syncthreads();
-        if (threadIdx.x == 1023) carry = start + mt;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        *n_tiles = carry;
-        if (tile_start) tile_start[E] = carry;
-    }
+    block_build_tiles(offsets, E, BM, tile_e, tile_m0, tile_start, n_tiles);
 }
 
 cudaError_t launch_build_tiles(const int32_t *offsets, int E, int BM, int32_t *tile_e,

@@ -487,17 +487,21 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
 // (x_sorted, or x itself for the shared expert) grouped by `offsets` into
 // `groups` experts; h gets the activation in bf16; the down projection's
 // output goes to `out`: plan.s_down fp32 planes of rows*d elements.
+// Rows per tile of the up projection's tile table.
+int up_tile_rows(const FfnPlan &plan) { return plan.nt ? plan.nt : tile_rows(plan.mh_up); }
+
 int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void *A,
                long long rows, int groups, int F, const int32_t *offsets, const void *w1,
                const void *w3, const void *w2, void *h, float *up_part, float *out,
                int32_t *tile_e, int32_t *tile_start, int32_t *ntiles, int up_stage,
-               int down_stage, cudaStream_t st) {
+               int down_stage, cudaStream_t st, bool tiles_built = false) {
     const int d = c->d_model;
     const int nt = plan.nt;
     cudaEvent_t ev = up_stage >= 0 ? stage_begin(st) : nullptr;
-    const int up_rows = nt ? nt : tile_rows(plan.mh_up);
-    MOE_CUDA(launch_build_tiles(offsets, groups, up_rows, tile_e, nullptr, tile_start, ntiles,
-                                st));
+    const int up_rows = up_tile_rows(plan);
+    if (!tiles_built)
+        MOE_CUDA(launch_build_tiles(offsets, groups, up_rows, tile_e, nullptr, tile_start, ntiles,
+                                    st));
     if (plan.s_up > 1) {
         const int upw = up_mode == GEMM_UP_SWIGLU ? 2 : 1;
         MOE_CUDA(launch_tc_gemm(up_mode, nt, plan.bn_up, 1, A, rows, d, w1, w3, groups, F, F, d,
@@ -533,9 +537,12 @@ int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void
 // (+activation, h in bf16) into h, tcgen05 down into out_sorted.  fp32: SIMT
 // GEMMs reading x through perm directly.
 // inv (token choice, may be NULL): the slots' rows, for the token-major copy.
+// tiles_built: the dispatch already wrote the up projection's tile table
+// (bf16 layers; DispatchTail).
 int run_experts(const moe_config *c, const void *x, const int32_t *perm, const int32_t *offsets,
                 const void *w1, const void *w3, const void *w2, float *out_sorted, void *ws,
-                const Layout &L, cudaStream_t st, const int32_t *inv = nullptr) {
+                const Layout &L, cudaStream_t st, const int32_t *inv = nullptr,
+                bool tiles_built = false) {
     const Sizes s = sizes(c);
     if (s.R == 0) return MOE_OK;
     const int gk = expert_choice(c) ? 1 : (int)s.k;   // perm holds t*k+j, or t itself
@@ -552,7 +559,7 @@ int run_experts(const moe_config *c, const void *x, const int32_t *perm, const i
         stage_end(MOE_STAGE_GATHER, ev, st);
         return run_tc_ffn(c, routed_plan(c), up_mode, xs, s.R, (int)s.E, (int)s.F, offsets, w1,
                           w3, w2, h, at<float>(ws, L.up_part), out_sorted, tile_e,
-                          tile_start, ntiles, MOE_STAGE_UP, MOE_STAGE_DOWN, st);
+                          tile_start, ntiles, MOE_STAGE_UP, MOE_STAGE_DOWN, st, tiles_built);
     }
     cudaEvent_t ev = stage_begin(st);
     MOE_CUDA(launch_build_tiles(offsets, (int)s.E, kSimtBM, tile_e, tile_m0, nullptr, ntiles, st));
@@ -988,6 +995,15 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     ev = stage_begin(st);
     const float *comb_w = w;           // gate weight of each slot in the combine
     const bool ec = expert_choice(cfg);
+    ObsArgs oa{};
+    if (obs) {
+        oa.n_dropped = ndrop;
+        oa.bias = cfg->quantile_balance ? sbias : wts->select_bias;
+        oa.drop_ratio = obs->drop_ratio;
+        oa.bias_mean_abs = obs->bias_mean_abs;
+        oa.bias_max_abs = obs->bias_max_abs;
+    }
+    DispatchTail tail{};
     if (ec) {
         MOE_CUDA(launch_expert_choice(at<float>(ws, L.probsT), (int)s.T, (int)s.E,
                                       (int)ec_rows_per_expert(cfg), perm,
@@ -1004,9 +1020,25 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
                                          offsets, perm, inv, out->slot_expert, sw, ndrop, st));
         comb_w = sw;
     } else {
+        // the dispatch's offsets CTA also computes the load statistics and,
+        // for the tensor-core FFN, the up projection's tile table
+        tail.stats = s.T > 0;
+        tail.p = p;
+        tail.T = (int)s.T;
+        tail.k = (int)s.k;
+        tail.f = out->f;
+        tail.aux = out->aux;
+        tail.load = out->load_max_over_mean;
+        tail.o = oa;
+        if (cfg->dtype == MOE_DTYPE_BF16 && s.T > 0) {
+            tail.tile_rows = up_tile_rows(rplan);
+            tail.tile_e = at<int32_t>(ws, L.tile_e);
+            tail.tile_start = at<int32_t>(ws, L.tile_start);
+            tail.n_tiles = at<int32_t>(ws, L.ntiles);
+        }
         MOE_CUDA(launch_dispatch(idx, s.Tk, (int)s.E, (int)s.k, capacity_of(cfg),
                                  at<int32_t>(ws, L.hist), at<int32_t>(ws, L.block_base), counts,
-                                 offsets, perm, inv, ndrop, st));
+                                 offsets, perm, inv, ndrop, st, &tail));
         if (out->slot_expert || out->slot_w)
             MOE_CUDA(launch_slot_outputs(idx, w, inv, s.Tk, out->slot_expert, out->slot_w, st));
     }
@@ -1027,16 +1059,9 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     if (s.T == 0) {
         MOE_CUDA(cudaMemsetAsync(p, 0, sizeof(float) * s.E, st));
     }
-    ObsArgs oa{};
-    if (obs) {
-        oa.n_dropped = ndrop;
-        oa.bias = cfg->quantile_balance ? sbias : wts->select_bias;
-        oa.drop_ratio = obs->drop_ratio;
-        oa.bias_mean_abs = obs->bias_mean_abs;
-        oa.bias_max_abs = obs->bias_max_abs;
-    }
-    MOE_CUDA(launch_stats_finalize(counts, p, (int)s.T, (int)s.E, (int)s.k, out->f, nullptr,
-                                   out->aux, out->load_max_over_mean, st, oa));
+    if (!tail.stats)
+        MOE_CUDA(launch_stats_finalize(counts, p, (int)s.T, (int)s.E, (int)s.k, out->f, nullptr,
+                                       out->aux, out->load_max_over_mean, st, oa));
     stage_end(MOE_STAGE_STATS, ev, st);
     const bool want_scale =
         obs && (obs->expert_out_mean || obs->expert_out_std || obs->expert_out_max_abs);
@@ -1048,7 +1073,7 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
         return MOE_OK;
     }
     rc = run_experts(cfg, x, perm, offsets, wts->w1, wts->w3, wts->w2, out_sorted, ws, L, st,
-                     expert_choice(cfg) ? nullptr : inv);
+                     expert_choice(cfg) ? nullptr : inv, tail.tile_rows > 0);
     if (rc != MOE_OK) return rc;
     if (want_scale)
         MOE_CUDA(launch_expert_scale(eo, (int)s.d, offsets, (int)s.E, s.R,
