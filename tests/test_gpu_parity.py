@@ -80,6 +80,18 @@ SMALL = {
         d_model=256, n_experts=64, d_ff=128, d_ff_shared=192, select_space="logits"), 300),
     "tiny_E40_logits": (mi.workload("tiny").with_sizes(n_experts=40, top_k=3, select_bias="uniform",
                                                        select_space="logits"), 200),
+    # degenerate expert counts: one expert (a dense FFN: every probability 1,
+    # every gate weight 1), and k = E (every token to every expert)
+    "mixtral_E1": (mi.workload("mixtral").with_sizes(d_model=256, n_experts=1, top_k=1, d_ff=512),
+                   300),
+    "tiny_E1": (mi.workload("tiny").with_sizes(n_experts=1, top_k=1), 64),
+    "mixtral_kE": (mi.workload("mixtral").with_sizes(d_model=256, n_experts=4, top_k=4, d_ff=256),
+                   200),
+    # the largest expert count (1024) with the largest k (16), with the
+    # selection bias; and quantile balancing over 1024 experts
+    "deepseek_E1024_k16": (mi.workload("deepseek").with_sizes(
+        d_model=256, n_experts=1024, top_k=16, d_ff=64, d_ff_shared=128), 2048),
+    "e896_E1024": (mi.workload("e896").with_sizes(d_model=128, n_experts=1024, d_ff=64), 4096),
 }
 
 
