@@ -80,6 +80,10 @@ SMALL = {
         d_model=256, n_experts=64, d_ff=128, d_ff_shared=192, select_space="logits"), 300),
     "tiny_E40_logits": (mi.workload("tiny").with_sizes(n_experts=40, top_k=3, select_bias="uniform",
                                                        select_space="logits"), 200),
+    # a capacity of 4 rows per expert (capacity factor 0.05): almost every
+    # slot dropped, four rows per expert kept
+    "mixtral_cap_tiny": (mi.workload("mixtral_cap").with_sizes(d_model=256, d_ff=512,
+                                                               capacity_factor=0.05), 300),
     # degenerate expert counts: one expert (a dense FFN: every probability 1,
     # every gate weight 1), and k = E (every token to every expert)
     "mixtral_E1": (mi.workload("mixtral").with_sizes(d_model=256, n_experts=1, top_k=1, d_ff=512),
@@ -103,6 +107,27 @@ def test_layer_small_full_oracle(name):
     print(name, rep)
     if w.capacity_factor > 0 and T >= 16:
         assert orc["dispatch"].n_dropped > 0          # the skewed expert overflows
+
+
+@pytest.mark.parametrize("name,T", [("mixtral_small", 3000), ("switch_small", 2000)])
+def test_every_token_to_one_expert(name, T):
+    """Router collapse: a logit offset of +10 on expert 0 sends every token
+    there first (k = 2: one 3000-row group on SM-pair tiles and the second
+    choices spread over the rest; k = 1 with capacity 1.25: one expert full,
+    the rest of the batch dropped and seven experts empty)."""
+    w, _ = SMALL[name]
+    inp = mi.generate(w, T, DEV)
+    lb = torch.zeros(w.n_experts, dtype=torch.float32, device=DEV)
+    lb[0] = 10.0
+    inp["logit_bias"] = lb
+    rep, gpu, orc = full_check(w, T, inp)
+    print(name, rep)
+    assert np.all(gpu["idx"][:, 0] == 0)
+    counts = orc["stats"]["counts"]
+    assert counts[0] == T
+    if w.capacity_factor > 0:
+        assert int(gpu["n_dropped"][0]) == T - om.capacity(T, w.top_k, w.n_experts,
+                                                            w.capacity_factor)
 
 
 def test_layer_deterministic():
