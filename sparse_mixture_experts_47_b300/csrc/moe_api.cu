@@ -483,13 +483,15 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
     return MOE_OK;
 }
 
+// Rows per tile of the up projection's tile table.
+int up_tile_rows(const FfnPlan &plan) { return plan.nt ? plan.nt : tile_rows(plan.mh_up); }
+
 // Up and down projections of one grouped FFN on the tensor cores: rows of A
 // (x_sorted, or x itself for the shared expert) grouped by `offsets` into
 // `groups` experts; h gets the activation in bf16; the down projection's
 // output goes to `out`: plan.s_down fp32 planes of rows*d elements.
-// Rows per tile of the up projection's tile table.
-int up_tile_rows(const FfnPlan &plan) { return plan.nt ? plan.nt : tile_rows(plan.mh_up); }
-
+// tiles_built: the up projection's tile table is already in tile_e /
+// tile_start / ntiles (up_tile_rows rows per tile).
 int run_tc_ffn(const moe_config *c, const FfnPlan &plan, int up_mode, const void *A,
                long long rows, int groups, int F, const int32_t *offsets, const void *w1,
                const void *w3, const void *w2, void *h, float *up_part, float *out,
