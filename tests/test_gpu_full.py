@@ -15,7 +15,7 @@ DEV = "cuda"
 FULL = [("switch", 8192, None), ("mixtral", 1, None), ("mixtral", 16, None),
         ("mixtral", 4096, 192), ("mixtral", 16384, 192), ("deepseek", 128, None),
         ("deepseek", 8192, 96), ("e896", 16384, 96), ("mixtral_cap", 4096, 192),
-        ("deepseek_cap", 8192, 96)]
+        ("mixtral_cap", 16384, 192), ("deepseek_cap", 8192, 96)]
 
 
 @pytest.mark.parametrize("name,T,n_sample", FULL, ids=[f"{n}-T{T}" for n, T, _ in FULL])
