@@ -64,6 +64,39 @@ __device__ inline void block_load_stats(StatsSmem &sm, int n, int c, const float
     }
 }
 
+// p_e = (sum over blocks b of p_partial[b][e]) / T for the 32 experts e0 ..
+// e0 + 31, over a CTA of 1024 threads: lane = expert (128-byte rows of the
+// partials), warp w of 32 sums blocks w, w + 32, ... in order in fp32 with 8
+// loads in flight, and the 32 warp sums are added in warp order in fp64
+// (fixed order, no atomics).  fp64 arithmetic runs at a few operations per
+// clock per SM on this part, so it is kept to the final 32 terms: an fp64
+// sum of every partial on 28 SMs took 25 us for the 896-expert layer.
+__device__ inline void block_p_finalize(const float *p_partial, int nblk, int E, int T,
+                                        float *p, int e0) {
+    __shared__ double red[32][33];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = e0 + lane;
+    float s = 0.f;
+    if (e < E) {
+        int b = warp;
+        for (; b + 7 * 32 < nblk; b += 8 * 32) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = p_partial[(size_t)(b + 32 * q) * E + e];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) s += v[q];
+        }
+        for (; b < nblk; b += 32) s += p_partial[(size_t)b * E + e];
+    }
+    red[warp][lane] = (double)s;
+    __syncthreads();
+    if (warp == 0 && e < E) {
+        double t = 0.0;
+        for (int w = 0; w < 32; ++w) t += red[w][lane];
+        p[e] = T > 0 ? (float)(t / (double)T) : 0.f;
+    }
+}
+
 // Tile table of a grouped GEMM with BM-row tiles, over a CTA of 1024
 // threads: expert e owns ceil((offsets[e+1]-offsets[e]) / BM) tiles starting
 // at row offsets[e]; tile_start[e] is the index of its first tile
@@ -120,6 +153,10 @@ __device__ inline void block_build_tiles(const int32_t *offsets, int E, int BM, 
 // after the CTA wrote offsets and n_dropped and passed a __syncthreads().
 __device__ inline void dispatch_tail(const DispatchTail &t, int c, int E, const int32_t *offsets) {
     __shared__ StatsSmem sm;
+    if (t.p_nblk > 0) {                      // p of up to 32 experts from the router's partials
+        block_p_finalize(t.p_partial, t.p_nblk, E, t.T, t.p_out, 0);
+        __syncthreads();
+    }
     int n = 32;                              // the statistics' tree: the power of two >= E
     while (n < E) n *= 2;
     if (t.stats) block_load_stats(sm, n, c, t.p, t.T, E, t.k, t.f, nullptr, t.aux, t.load, t.o);

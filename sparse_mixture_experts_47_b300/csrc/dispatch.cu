@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
         if (offsets) offsets[E] = total;
         if (n_dropped) *n_dropped = all_total - total;
     }
-    if (tail.stats || tail.tile_rows > 0) {
+    if (tail.stats || tail.tile_rows > 0 || tail.p_nblk > 0) {
         __syncthreads();
         dispatch_tail(tail, run, E, offsets);
     }
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t *idx
         if (n_dropped) *n_dropped = all_total - total;
     }
     __syncthreads();
-    if (tail.stats || tail.tile_rows > 0) dispatch_tail(tail, run, E, offsets);
+    if (tail.stats || tail.tile_rows > 0 || tail.p_nblk > 0) dispatch_tail(tail, run, E, offsets);
     if (tid >= 32) return;
     const int lane = tid;
     for (int b = 0; b < n; b += 32) {
@@ -245,7 +245,8 @@ cudaError_t launch_dispatch(const int32_t *idx, long long n, int E, int k, long 
     if (tail) {
         t = *tail;
         // the tail reads offsets and n_dropped as this launch writes them
-        if ((t.tile_rows > 0 && !offsets) || (t.o.drop_ratio && t.o.n_dropped != n_dropped))
+        if ((t.tile_rows > 0 && !offsets) || (t.o.drop_ratio && t.o.n_dropped != n_dropped) ||
+            (t.p_nblk > 0 && (E > 32 || !t.p_partial || !t.p_out)))
             return cudaErrorInvalidValue;
     }
     const int nblk = dispatch_blocks(n);

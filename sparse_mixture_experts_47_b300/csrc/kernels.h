@@ -74,10 +74,14 @@ struct ObsArgs {
 constexpr int kDispatchChunk = 1024;
 inline int dispatch_blocks(long long n) { return (int)((n + kDispatchChunk - 1) / kDispatchChunk); }
 // Work that the dispatch kernel computing the counts and offsets does after
-// them, in place of separate launches: the load statistics (stats_finalize's
-// outputs, from counts, n_dropped and the router's mean probabilities p) and
-// the tile table of the up projection (build_tiles with tile_rows-row tiles).
+// them, in place of separate launches: the router's mean probabilities p_out
+// from its per-block partials (p_finalize, up to 32 experts), the load
+// statistics (stats_finalize's outputs, from counts, n_dropped and p) and the
+// tile table of the up projection (build_tiles with tile_rows-row tiles).
 struct DispatchTail {
+    const float *p_partial;      // p_nblk > 0: p_out = block sums of p_partial / T
+    int p_nblk;
+    float *p_out;
     bool stats;
     const float *p;
     int T, k;

@@ -29,38 +29,11 @@ __device__ double block_sum_256(double v, double *red) {
     return red[0];
 }
 
-// p_e = (sum over blocks b of p_partial[b][e]) / T in fp64: one CTA per expert,
-// thread i sums blocks i, i+256, ... in order, then a fixed tree.
-// One CTA per 32 consecutive experts: lane = expert (128-byte rows of the
-// partials), warp w of 32 sums blocks w, w + 32, ... in order in fp32 with 8
-// loads in flight, and the 32 warp sums are added in warp order in fp64
-// (fixed order, no atomics).  fp64 arithmetic runs at a few operations per
-// clock per SM on this part, so it is kept to the final 32 terms: an fp64
-// sum of every partial on 28 SMs took 25 us for the 896-expert layer.
+// p_e = (sum over blocks b of p_partial[b][e]) / T (block_p_finalize): one
+// CTA of 1024 threads per 32 consecutive experts.
 __global__ void __launch_bounds__(1024) p_finalize_kernel(const float *p_partial, int nblk, int E,
                                                           int T, float *p) {
-    __shared__ double red[32][33];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int e = blockIdx.x * 32 + lane;
-    float s = 0.f;
-    if (e < E) {
-        int b = warp;
-        for (; b + 7 * 32 < nblk; b += 8 * 32) {
-            float v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = p_partial[(size_t)(b + 32 * q) * E + e];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) s += v[q];
-        }
-        for (; b < nblk; b += 32) s += p_partial[(size_t)b * E + e];
-    }
-    red[warp][lane] = (double)s;
-    __syncthreads();
-    if (warp == 0 && e < E) {
-        double t = 0.0;
-        for (int w = 0; w < 32; ++w) t += red[w][lane];
-        p[e] = T > 0 ? (float)(t / (double)T) : 0.f;
-    }
+    block_p_finalize(p_partial, nblk, E, T, p, blockIdx.x * 32);
 }
 
 cudaError_t launch_p_finalize(const float *p_partial, int nblk, int E, int T, float *p,

@@ -411,10 +411,21 @@ void stage_end(int stage, cudaEvent_t a, cudaStream_t st) {
 }
 
 // Router incl. quantile balancing; p (mean probs) when p_out != NULL.
+// The layer's dispatch computes p from the router's per-block partials
+// (DispatchTail) instead of a p_finalize launch: token choice without
+// redirection, up to 32 experts on the CUDA-core router, more than one
+// softmax block (one block writes p itself).
+bool p_from_dispatch(const moe_config *c) {
+    const Sizes s = sizes(c);
+    return s.T > 0 && !expert_choice(c) && c->reroute_rounds == 0 && !tc_router(c) &&
+           s.E <= 32 && router_blocks((int)s.T, (int)s.E, c->dtype, router_selects(c)) > 1;
+}
+
+// defer_p: leave p to the dispatch (p_from_dispatch(c) must hold).
 int run_router(const moe_config *c, const void *x, const float *w_r, const float *logit_bias,
                const float *select_bias, int32_t *idx, float *w, float *probs, float *p_out,
                float *sbias_out, bool want_probsT, void *ws, const Layout &L, cudaStream_t st,
-               float *entropy_out = nullptr, int32_t *cand_out = nullptr) {
+               float *entropy_out = nullptr, int32_t *cand_out = nullptr, bool defer_p = false) {
     const Sizes s = sizes(c);
     RouterArgs a{};
     a.x = x; a.w_r = w_r; a.logit_bias = logit_bias;
@@ -460,7 +471,7 @@ int run_router(const moe_config *c, const void *x, const float *w_r, const float
     } else {
         MOE_CUDA(launch_router(a, c->dtype, at<float>(ws, L.rt_logits), st));
     }
-    if (p_out && s.T > 0 && !a.p_direct)
+    if (p_out && s.T > 0 && !a.p_direct && !defer_p)
         MOE_CUDA(launch_p_finalize(a.p_partial,
                                    router_blocks(a.T, a.E, c->dtype, a.do_select != 0), a.E, a.T,
                                    p_out, st));
@@ -988,7 +999,7 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
     if (s.T > 0) {
         rc = run_router(cfg, x, wts->w_r, wts->logit_bias, wts->select_bias, idx, w, nullptr, p,
                         sbias, want_unb && biased, ws, L, st, obs ? obs->gate_entropy : nullptr,
-                        cand);
+                        cand, p_from_dispatch(cfg));
         if (rc != MOE_OK) return rc;
     } else if (obs && obs->gate_entropy) {
         MOE_CUDA(cudaMemsetAsync(obs->gate_entropy, 0, sizeof(float), st));
@@ -1022,8 +1033,14 @@ int moe_layer_forward_observed(const moe_config *cfg, const void *x,
                                          offsets, perm, inv, out->slot_expert, sw, ndrop, st));
         comb_w = sw;
     } else {
-        // the dispatch's offsets CTA also computes the load statistics and,
-        // for the tensor-core FFN, the up projection's tile table
+        // the dispatch's offsets CTA also computes p (when the router left
+        // it), the load statistics and, for the tensor-core FFN, the up
+        // projection's tile table
+        if (p_from_dispatch(cfg)) {
+            tail.p_partial = at<float>(ws, L.p_partial);
+            tail.p_nblk = router_blocks((int)s.T, (int)s.E, cfg->dtype, router_selects(cfg));
+            tail.p_out = p;
+        }
         tail.stats = s.T > 0;
         tail.p = p;
         tail.T = (int)s.T;
